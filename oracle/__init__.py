@@ -1,0 +1,10 @@
+"""fp64 CPU oracle for the attention forward pass (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+and reference legs may import this package.  The CUDA path never does.
+"""
+from .attention import (  # noqa: F401
+    decode, decode_bf16, decode_f16,
+    attention_reference, attention_reference_f64, attention_rows,
+    softmax_probabilities, online_softmax_attention,
+)

@@ -1,0 +1,437 @@
+"""Pins for the fp64 oracle: it is checked against what the pages and the
+mathematics fix, never against itself or the CUDA path.
+
+Each pin is a function of an implementation ``ref(q, k, v, causal, scale) ->
+(O, LSE)`` on float64 [B, S, H, D] arrays, so that ``test_pins_catch_planted_
+mistakes`` can run the same pins on deliberately broken copies of the oracle
+(planted on the CPU) and show that each plausible mistake fails at least one.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import fa_inputs
+from oracle import (attention_reference, attention_reference_f64,
+                    attention_rows, decode_bf16, decode_f16,
+                    online_softmax_attention, softmax_probabilities)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def _parse_golden(name):
+    env = {"ln": math.log}
+    out = {}
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, val = (x.strip() for x in line.split("=", 1))
+            vals = [float(eval(tok, {"__builtins__": {}}, env))
+                    for tok in val.split()]
+            out[key] = vals if len(vals) > 1 else vals[0]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# pins (each takes an implementation)
+
+def pin_golden_worked_example(ref):
+    g = _parse_golden("worked_example_two_tiles.txt")
+    q = np.array(g["q"]).reshape(1, 4, 1, 1)
+    k = np.array(g["k"]).reshape(1, 4, 1, 1)
+    v = np.array(g["v"]).reshape(1, 4, 1, 1)
+    O, L = ref(q, k, v, False, g["scale"])
+    np.testing.assert_allclose(O[0, :, 0, 0], g["noncausal_O"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(L[0, 0, :], g["noncausal_LSE"], rtol=0, atol=1e-13)
+    O, L = ref(q, k, v, True, g["scale"])
+    np.testing.assert_allclose(O[0, :, 0, 0], g["causal_O"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(L[0, 0, :], g["causal_LSE"], rtol=0, atol=1e-13)
+
+
+def pin_uniform_scores(ref):
+    g = _parse_golden("uniform_scores_n320.txt")
+    S = int(g["S"])
+    q = np.zeros((1, S, 1, 2))
+    k = np.stack([np.arange(S) % 7, -np.ones(S)], axis=1).reshape(1, S, 1, 2)
+    v = np.stack([np.arange(S), np.ones(S)], axis=1).reshape(1, S, 1, 2).astype(float)
+    O, L = ref(q, k, v, False, g["scale"])
+    np.testing.assert_allclose(O[0, :, 0, 0], g["noncausal_O0"], atol=1e-10)
+    np.testing.assert_allclose(O[0, :, 0, 1], 1.0, atol=1e-12)
+    np.testing.assert_allclose(L[0, 0], g["noncausal_LSE"], atol=1e-12)
+    O, L = ref(q, k, v, True, g["scale"])
+    i = np.arange(S)
+    np.testing.assert_allclose(O[0, :, 0, 0], i / 2.0, atol=1e-10)
+    np.testing.assert_allclose(L[0, 0], np.log(i + 1.0), atol=1e-12)
+
+
+def pin_identical_keys(ref):
+    """All keys equal -> uniform softmax: O = mean of visible V,
+    LSE_i = z_i0 + ln |N_i|."""
+    B, S, H, D = 1, 37, 2, 5
+    q = _rand((B, S, H, D), 1, 2.0)
+    k = np.repeat(_rand((B, 1, H, D), 2, 3.0), S, axis=1)
+    v = _rand((B, S, H, D), 3)
+    scale = 0.3
+    z0 = scale * np.einsum("bihd,bhd->bhi", q, k[:, 0])
+    O, L = ref(q, k, v, False, scale)
+    np.testing.assert_allclose(O, np.broadcast_to(v.mean(axis=1, keepdims=True), O.shape),
+                               atol=1e-12)
+    np.testing.assert_allclose(L, z0 + math.log(S), atol=1e-12)
+    O, L = ref(q, k, v, True, scale)
+    prefix = np.cumsum(v, axis=1) / np.arange(1, S + 1)[None, :, None, None]
+    np.testing.assert_allclose(O, prefix, atol=1e-12)
+    np.testing.assert_allclose(L, z0 + np.log(np.arange(1, S + 1))[None, None, :],
+                               atol=1e-12)
+
+
+def pin_causal_row0(ref):
+    """Causal row 0 sees only key 0: O_0 = V_0, LSE_0 = z_00."""
+    q, k, v = (_rand((2, 19, 3, 8), s) for s in (4, 5, 6))
+    scale = 0.25
+    O, L = ref(q, k, v, True, scale)
+    np.testing.assert_allclose(O[:, 0], v[:, 0], atol=1e-13)
+    np.testing.assert_allclose(L[:, :, 0], scale * np.einsum("bhd,bhd->bh", q[:, 0], k[:, 0]),
+                               atol=1e-13)
+
+
+def pin_single_key(ref):
+    """S = 1: O = V_0 and LSE = z_00 in both modes."""
+    q, k, v = (_rand((3, 1, 2, 4), s) for s in (7, 8, 9))
+    for causal in (False, True):
+        O, L = ref(q, k, v, causal, 0.5)
+        np.testing.assert_allclose(O, v, atol=1e-14)
+        np.testing.assert_allclose(L[:, :, 0], 0.5 * np.einsum("bhd,bhd->bh", q[:, 0], k[:, 0]),
+                                   atol=1e-14)
+
+
+def pin_vanishing_scale(ref):
+    """scale -> 0+: softmax -> uniform, O -> mean of visible V (error O(scale))."""
+    q, k, v = (_rand((1, 23, 2, 6), s) for s in (10, 11, 12))
+    O, L = ref(q, k, v, False, 1e-12)
+    np.testing.assert_allclose(O, np.broadcast_to(v.mean(axis=1, keepdims=True), O.shape),
+                               atol=1e-9)
+    np.testing.assert_allclose(L, math.log(23), atol=1e-9)
+    O, _ = ref(q, k, v, True, 1e-12)
+    prefix = np.cumsum(v, axis=1) / np.arange(1, 24)[None, :, None, None]
+    np.testing.assert_allclose(O, prefix, atol=1e-9)
+
+
+def pin_dominant_key(ref):
+    """One key's logit 40 above every other: O = V[j*] up to S*e^-40."""
+    S, jstar = 29, 17
+    q = np.ones((1, S, 1, 1))
+    k = np.zeros((1, S, 1, 1))
+    k[0, jstar, 0, 0] = 40.0 / 0.125
+    v = _rand((1, S, 1, 3), 13)
+    O, L = ref(q, k, v, False, 0.125)
+    np.testing.assert_allclose(O[0, :, 0], np.broadcast_to(v[0, jstar, 0], (S, 3)),
+                               atol=S * math.exp(-40) * 10)
+    np.testing.assert_allclose(L[0, 0], 40.0 + math.log1p((S - 1) * math.exp(-40)),
+                               atol=1e-12)
+
+
+def pin_key_permutation(ref):
+    """Non-causal attention is invariant under a joint permutation of K, V rows."""
+    q, k, v = (_rand((1, 31, 2, 7), s) for s in (14, 15, 16))
+    perm = np.random.default_rng(17).permutation(31)
+    O1, L1 = ref(q, k, v, False, 0.4)
+    O2, L2 = ref(q, k[:, perm], v[:, perm], False, 0.4)
+    np.testing.assert_allclose(O1, O2, atol=1e-12)
+    np.testing.assert_allclose(L1, L2, atol=1e-12)
+
+
+def pin_lse_bounds(ref):
+    """max_j z_ij <= LSE_i <= max_j z_ij + ln |N_i|."""
+    q, k, v = (_rand((2, 40, 2, 8), s, 3.0) for s in (18, 19, 20))
+    scale = 0.2
+    for causal in (False, True):
+        _, L = ref(q, k, v, causal, scale)
+        z = scale * np.einsum("bihd,bjhd->bhij", q, k)
+        n = np.arange(1, 41) if causal else np.full(40, 40)
+        if causal:
+            z = np.where(np.tril(np.ones((40, 40), bool)), z, -np.inf)
+        zmax = z.max(axis=-1)
+        assert np.all(L >= zmax - 1e-12)
+        assert np.all(L <= zmax + np.log(n) + 1e-12)
+
+
+def pin_torch_sdpa(ref):
+    """Agreement with torch's own attention and logsumexp (fp64, CPU)."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    q, k, v = (_rand((2, 45, 3, 16), s, 2.0) for s in (21, 22, 23))
+    scale = 0.17
+    for causal in (False, True):
+        O, L = ref(q, k, v, causal, scale)
+        tq, tk, tv = (torch.from_numpy(x).permute(0, 2, 1, 3) for x in (q, k, v))
+        with torch.nn.attention.sdpa_kernel(torch.nn.attention.SDPBackend.MATH):
+            to = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale)
+        np.testing.assert_allclose(O, to.permute(0, 2, 1, 3).numpy(), atol=1e-12)
+        logits = scale * (tq @ tk.transpose(-1, -2))
+        if causal:
+            logits = logits.masked_fill(~torch.ones(45, 45, dtype=torch.bool).tril(), -math.inf)
+        np.testing.assert_allclose(L, torch.logsumexp(logits, dim=-1).numpy(), atol=1e-12)
+
+
+def pin_brute_force(ref):
+    """Tiny inputs against a scalar loop with math.exp and exact summation."""
+    for (S, D, causal, seed) in [(1, 1, False, 30), (2, 1, True, 31), (3, 2, False, 32),
+                                 (4, 3, True, 33), (5, 2, True, 34), (5, 4, False, 35)]:
+        q, k, v = (_rand((1, S, 2, D), seed + 100 * t) for t in range(3))
+        scale = 0.6
+        O, L = ref(q, k, v, causal, scale)
+        for h in range(2):
+            for i in range(S):
+                keys = range(i + 1) if causal else range(S)
+                z = [scale * math.fsum(q[0, i, h, d] * k[0, j, h, d] for d in range(D))
+                     for j in keys]
+                mz = max(z)
+                w = [math.exp(x - mz) for x in z]
+                tot = math.fsum(w)
+                for d in range(D):
+                    o = math.fsum(w[n] * v[0, j, h, d] for n, j in enumerate(keys)) / tot
+                    assert abs(O[0, i, h, d] - o) < 1e-13
+                assert abs(L[0, h, i] - (mz + math.log(tot))) < 1e-13
+
+
+PINS = [pin_golden_worked_example, pin_uniform_scores, pin_identical_keys,
+        pin_causal_row0, pin_single_key, pin_vanishing_scale, pin_dominant_key,
+        pin_key_permutation, pin_lse_bounds, pin_torch_sdpa, pin_brute_force]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_reference_definition(pin):
+    pin(attention_reference_f64)
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+@pytest.mark.parametrize("block,tau", [(1, 0.0), (3, 0.0), (3, 8 * math.log(2)),
+                                       (16, 8 * math.log(2))])
+def test_online_recurrence(pin, block, tau):
+    """The pages' recurrence (with and without the lazy threshold) passes the
+    same pins as the definition."""
+    def ref(q, k, v, causal, scale):
+        return online_softmax_attention(q, k, v, causal, scale, block, tau)
+    pin(ref)
+
+
+# ---------------------------------------------------------------------------
+# further checks of individual pieces
+
+def test_golden_online_trace():
+    """The online state after each tile matches the hand-derived values."""
+    g = _parse_golden("worked_example_two_tiles.txt")
+    q = np.array(g["q"]).reshape(1, 4, 1, 1)
+    k = np.array(g["k"]).reshape(1, 4, 1, 1)
+    v = np.array(g["v"]).reshape(1, 4, 1, 1)
+    trace = []
+    online_softmax_attention(q, k, v, False, g["scale"], int(g["online_block"]), 0.0, trace)
+    (t0, m0, l0, o0), (t1, m1, l1, o1) = trace
+    assert abs(m0 - g["online_tile0_m"]) < 1e-14 and abs(l0 - g["online_tile0_l"]) < 1e-14
+    assert abs(o0[0] - g["online_tile0_o"]) < 1e-13
+    assert abs(m1 - g["online_tile1_m"]) < 1e-14 and abs(l1 - g["online_tile1_l"]) < 1e-14
+    assert abs(o1[0] - g["online_tile1_o"]) < 1e-13
+
+
+def test_rows_of_p_sum_to_one():
+    for w in ("stress",):
+        for causal in (False, True):
+            q, k, _ = (_rand((1, 200, 2, 16), s, 4.0) for s in (40, 41, 42))
+            for h in range(2):
+                P = softmax_probabilities(q, k, causal, 0.125, 0, h)
+                np.testing.assert_allclose(P.sum(axis=1), 1.0, atol=1e-12)
+                assert np.all(P >= 0)
+                if causal:
+                    assert np.all(np.triu(P, 1) == 0)
+
+
+@pytest.mark.parametrize("block,tau,n_tiles", [(128, 8 * math.log(2), True),
+                                               (64, 0.0, True), (128, 0.0, False)])
+def test_online_matches_definition_on_workload_shapes(block, tau, n_tiles):
+    """Tile size of the GPU kernel, a ragged length, masked tiles, peaky logits."""
+    rng = np.random.default_rng(50)
+    S, D = 300, 64
+    q = rng.standard_normal((1, S, 1, D)) * 4
+    k = rng.standard_normal((1, S, 1, D)) * 4
+    v = rng.uniform(-1, 1, (1, S, 1, D))
+    for causal in (False, True):
+        O, L = attention_reference_f64(q, k, v, causal, 0.125)
+        nt = (S + block - 1) // block if n_tiles else None
+        O2, L2 = online_softmax_attention(q, k, v, causal, 0.125, block, tau, n_tiles=nt)
+        np.testing.assert_allclose(O2, O, atol=1e-12)
+        np.testing.assert_allclose(L2, L, rtol=1e-13, atol=1e-12)
+
+
+def _half_by_formula(bits):
+    s = -1.0 if bits >> 15 else 1.0
+    e = (bits >> 10) & 0x1F
+    f = bits & 0x3FF
+    if e == 0:
+        return s * math.ldexp(f, -24)
+    if e == 31:
+        return s * math.inf if f == 0 else math.nan
+    return s * math.ldexp(1024 + f, e - 25)
+
+
+def _bf16_by_formula(bits):
+    s = -1.0 if bits >> 15 else 1.0
+    e = (bits >> 7) & 0xFF
+    f = bits & 0x7F
+    if e == 0:
+        return s * math.ldexp(f, -133)
+    if e == 255:
+        return s * math.inf if f == 0 else math.nan
+    return s * math.ldexp(128 + f, e - 134)
+
+
+def test_decoders_exact_on_every_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    h = decode_f16(bits)
+    b = decode_bf16(bits)
+    eh = np.array([_half_by_formula(int(x)) for x in range(65536)])
+    eb = np.array([_bf16_by_formula(int(x)) for x in range(65536)])
+    np.testing.assert_array_equal(np.isnan(h), np.isnan(eh))
+    np.testing.assert_array_equal(h[~np.isnan(h)], eh[~np.isnan(eh)])
+    np.testing.assert_array_equal(np.isnan(b), np.isnan(eb))
+    np.testing.assert_array_equal(b[~np.isnan(b)], eb[~np.isnan(eb)])
+    torch = pytest.importorskip("torch")
+    tb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(np.isnan(tb), np.isnan(b))
+    np.testing.assert_array_equal(tb[~np.isnan(tb)], b[~np.isnan(b)])
+
+
+def test_bit_entry_points_match_float_path():
+    """attention_reference / attention_rows decode the same values the float
+    path sees, for both 16-bit types."""
+    for dtype in ("f16", "bf16"):
+        qb, kb, vb = fa_inputs.make_qkv(2, 3, 70, 16, dtype, "stress", 7,
+                                        identical_key_head=(1, 2))
+        dec = decode_f16 if dtype == "f16" else decode_bf16
+        for causal in (False, True):
+            O, L = attention_reference(qb, kb, vb, dtype, causal, 0.25)
+            O2, L2 = attention_reference_f64(dec(qb), dec(kb), dec(vb), causal, 0.25)
+            np.testing.assert_array_equal(O, O2)
+            np.testing.assert_array_equal(L, L2)
+            rows = [0, 5, 69]
+            Or, Lr = attention_rows(qb, kb, vb, dtype, causal, 0.25, 1, 2, rows)
+            np.testing.assert_allclose(Or, O[1, rows, 2, :], atol=1e-14)
+            np.testing.assert_allclose(Lr, L[1, 2, rows], atol=1e-13)
+
+
+def test_stress_identical_key_head_closed_form():
+    """On the stress workload's identical-key head the oracle gives the mean /
+    prefix mean of V (the closed form), at a reduced length."""
+    qb, kb, vb = fa_inputs.make_qkv(3, 8, 150, 64, "f16", "stress", 1005,
+                                    identical_key_head=(2, 7))
+    v = decode_f16(vb)[2, :, 7, :]
+    for causal in (False, True):
+        O, _ = attention_reference(qb, kb, vb, "f16", causal, 0.125)
+        if causal:
+            want = np.cumsum(v, axis=0) / np.arange(1, 151)[:, None]
+        else:
+            want = np.broadcast_to(v.mean(axis=0), v.shape)
+        np.testing.assert_allclose(O[2, :, 7, :], want, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: every plausible slip in the oracle must fail some pin
+
+def _mutant(kind):
+    def ref(q, k, v, causal, scale):
+        q = np.asarray(q, float); k = np.asarray(k, float); v = np.asarray(v, float)
+        B, S, H, D = q.shape
+        O = np.empty((B, S, H, v.shape[3])); L = np.empty((B, H, S))
+        for b in range(B):
+            for h in range(H):
+                qh, kh, vh = q[b, :, h], k[b, :, h], v[b, :, h]
+                sc = {"no_scale": 1.0, "scale_twice": scale * scale}.get(kind, scale)
+                z = sc * (qh @ kh.T)
+                if kind == "transposed":
+                    z = sc * (kh @ qh.T)
+                i = np.arange(S)[:, None]; j = np.arange(S)[None, :]
+                vis = {"mask_flipped": j >= i, "mask_strict": j < i,
+                       }.get(kind, j <= i) if causal else np.ones((S, S), bool)
+                if kind == "mask_strict":
+                    vis = vis | ((i == 0) & (j == 0))
+                z = np.where(vis, z, -np.inf)
+                m = z.max(axis=1)
+                e = np.exp(z - m[:, None])
+                l = e.sum(axis=1)
+                p = e / l[:, None]
+                if kind == "norm_wrong_axis":
+                    p = e / np.maximum(e.sum(axis=0, keepdims=True), 1e-300)
+                o = p @ vh
+                if kind == "o_unnormalised":
+                    o = e @ vh
+                lse = m + np.log(l)
+                if kind == "lse_no_max":
+                    lse = np.log(l)
+                if kind == "lse_log2":
+                    lse = m + np.log2(l)
+                O[b, :, h] = o; L[b, h] = lse
+        return O, L
+    return ref
+
+
+def _online_mutant(kind):
+    def ref(q, k, v, causal, scale):
+        q = np.asarray(q, float); k = np.asarray(k, float); v = np.asarray(v, float)
+        B, S, H, D = q.shape
+        O = np.empty((B, S, H, v.shape[3])); L = np.empty((B, H, S))
+        for b in range(B):
+            for h in range(H):
+                for i in range(S):
+                    m, l, o = -math.inf, 0.0, np.zeros(v.shape[3])
+                    last = i if causal else S - 1
+                    for j0 in range(0, last + 1, 2):
+                        j1 = min(last + 1, j0 + 2)
+                        s = scale * (k[b, j0:j1, h] @ q[b, i, h])
+                        m_new = max(m, s.max())
+                        alpha = math.exp(m - m_new) if m > -math.inf else 0.0
+                        p = np.exp(s - m_new)
+                        l = (l if kind == "l_not_rescaled" else alpha * l) + p.sum()
+                        o = (o if kind == "o_not_rescaled" else alpha * o) + p @ v[b, j0:j1, h]
+                        m = m_new
+                    O[b, i, h] = o / l
+                    L[b, h, i] = m + math.log(l)
+        return O, L
+    return ref
+
+
+MUTANTS = ["no_scale", "scale_twice", "transposed", "mask_flipped", "mask_strict",
+           "norm_wrong_axis", "o_unnormalised", "lse_no_max", "lse_log2"]
+
+
+def _fails_some_pin(ref):
+    failed = []
+    for pin in PINS:
+        try:
+            pin(ref)
+        except AssertionError:
+            failed.append(pin.__name__)
+        except (ValueError, FloatingPointError, IndexError):
+            failed.append(pin.__name__)
+    return failed
+
+
+def test_unmutated_copy_passes_every_pin():
+    assert _fails_some_pin(_mutant("none")) == []
+    assert _fails_some_pin(_online_mutant("none")) == []
+
+
+@pytest.mark.parametrize("kind", MUTANTS)
+def test_pins_catch_planted_mistakes(kind):
+    assert _fails_some_pin(_mutant(kind)), f"no pin caught the planted mistake {kind}"
+
+
+@pytest.mark.parametrize("kind", ["o_not_rescaled", "l_not_rescaled"])
+def test_pins_catch_planted_recurrence_mistakes(kind):
+    assert _fails_some_pin(_online_mutant(kind)), kind
