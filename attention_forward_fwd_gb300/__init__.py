@@ -1,0 +1,128 @@
+"""FlashAttention-2 forward pass on one GB300 (sm_103a).
+
+Thin Python binding over the C-ABI of ``libfa_gb300.so`` (declared in
+``include/fa_gb300.h``).  This module only marshals arguments: every step of
+the computation runs in the library's CUDA kernel, on the caller's stream.
+There is no CPU or PyTorch fallback; if the library is missing the call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH, build  # noqa: F401
+
+__all__ = ["fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
+           "fa_device_status", "fa_kernels_per_call", "attention_forward",
+           "FaError", "library", "EXPORTED_SYMBOLS", "FA_F16", "FA_BF16"]
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_F16, FA_BF16 = 0, 1
+
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
+                    "fa_device_status", "fa_kernels_per_call")
+
+_LIB = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {fa_status_string(status)} (status {status})")
+
+
+def library() -> ctypes.CDLL:
+    """Load libfa_gb300.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "attention_forward_fwd_gb300.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        sig = [vp, vp, vp, vp, vp, i, i, i, i, i, f]
+        lib.fa_fwd.argtypes = sig + [i, vp]
+        lib.fa_fwd_f16.argtypes = sig + [vp]
+        lib.fa_fwd_bf16.argtypes = sig + [vp]
+        for fn in (lib.fa_fwd, lib.fa_fwd_f16, lib.fa_fwd_bf16):
+            fn.restype = i
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_device_status.argtypes = [i]
+        lib.fa_device_status.restype = i
+        lib.fa_kernels_per_call.argtypes = []
+        lib.fa_kernels_per_call.restype = i
+        _LIB = lib
+    return _LIB
+
+
+def fa_status_string(status: int) -> str:
+    return library().fa_status_string(int(status)).decode()
+
+
+def fa_device_status(clear: bool = False) -> int:
+    return int(library().fa_device_status(1 if clear else 0))
+
+
+def fa_kernels_per_call() -> int:
+    return int(library().fa_kernels_per_call())
+
+
+def fa_fwd(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype, stream) -> int:
+    """Raw C-ABI call with integer device pointers; returns the status."""
+    return int(library().fa_fwd(Q, K, V, O, LSE, int(B), int(H), int(S), int(D),
+                                int(bool(causal)), float(scale), int(dtype), stream))
+
+
+def fa_fwd_f16(Q, K, V, O, LSE, B, H, S, D, causal, scale, stream) -> int:
+    return int(library().fa_fwd_f16(Q, K, V, O, LSE, int(B), int(H), int(S), int(D),
+                                    int(bool(causal)), float(scale), stream))
+
+
+def fa_fwd_bf16(Q, K, V, O, LSE, B, H, S, D, causal, scale, stream) -> int:
+    return int(library().fa_fwd_bf16(Q, K, V, O, LSE, int(B), int(H), int(S), int(D),
+                                     int(bool(causal)), float(scale), stream))
+
+
+def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
+                      out=None, lse=None, with_lse: bool = True, stream=None):
+    """O, LSE for torch CUDA tensors q, k, v of shape [B, S, H, D].
+
+    q, k, v must be contiguous fp16 or bf16 tensors on the same CUDA device.
+    ``out`` / ``lse`` may be preallocated ([B, S, H, D] same dtype; [B, H, S]
+    fp32).  Work is enqueued on ``stream`` (default: the current stream) and
+    not waited for.
+    """
+    import torch
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must have the same dtype")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [B, S, H, D] with the same shape")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, S, H, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse is None and with_lse:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.shape != (B, H, S) or lse.dtype != torch.float32
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor")
+    dtype = FA_F16 if q.dtype == torch.float16 else FA_BF16
+    with torch.cuda.device(q.device):
+        st = torch.cuda.current_stream().cuda_stream if stream is None else int(stream)
+        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                    lse.data_ptr() if lse is not None else None,
+                    B, H, S, D, causal, scale, dtype, st)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return out, lse

@@ -1,0 +1,447 @@
+// fa_fwd_kernel.cuh -- FlashAttention-2 forward kernel for sm_103a.
+//
+// What it computes (page "CuTe 详解：以 FlashAttention-2 拆解 Layout、TiledCopy
+// 与 TiledMMA"): per query tile, S = Q K^T, P = softmax(S), O = P V (section
+// 先看全局), carried across key tiles with the running max m_i, running sum
+// l_i and unnormalised output o~_i of section 教学配置, updated with
+// alpha = exp(m_old - m_new) as in section 沿 C fragment 做 Online Softmax,
+// and normalised O = o~ / l only after the last key tile.  The max is taken
+// on the raw scores and the positive scale folded in afterwards (same
+// section, last paragraph), as exp2 with scale*log2(e) folded into one FMA.
+//
+// How it maps onto one GB300 SM (one CTA per SM, 320 threads):
+//   warps 0-3  softmax group 0: query tile 0 (rows q0 .. q0+127), thread =
+//              row = TMEM lane.  Also rescales O in TMEM when its max moves
+//              and runs the epilogue for its tile.
+//   warps 4-7  softmax group 1: query tile 1 (rows q0+128 .. q0+255).
+//   warp  8    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+//              with tcgen05.mma, accumulators in TMEM; allocates TMEM.
+//   warp  9    TMA producer (one thread): Q tiles once, then K_j / V_j tiles
+//              through an NS-slot ring paced by full/empty mbarriers.
+// TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
+// O_0 [256,256+D), O_1 [256+D,256+2D).  P_t (16-bit, packed in pairs) is
+// written over the first 64 columns of S_t and read from there as the A
+// operand of the second product; V stays [key][d] in shared memory and is
+// read as an MN-major B operand (the transpose is only a view, section
+// V 的转置只发生在视图里).
+//
+// Every wait is bounded in time.  A wait that runs out sets a shared abort
+// flag and the device status word; every role then stops issuing work, waits
+// (again bounded) for what it already has in flight, and the CTA frees its
+// TMEM and exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kBM = 128;              // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;              // keys per tile
+constexpr int kQTiles = 2;            // query tiles per CTA
+constexpr int kThreads = 320;         // 8 softmax warps + MMA warp + TMA warp
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kTauLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
+
+constexpr int kStatusTimeout = 4;
+
+// Device status word: 0, or the status of the first wait that ran out.
+__device__ int g_fa_device_status;
+
+struct FwdParams {
+    int B, H, S;
+    int causal;
+    float scale_log2;   // scale * log2(e)
+    float* lse;         // [B, H, S] fp32 or nullptr
+};
+
+template <int NS>
+struct Barriers {
+    uint64_t q_full;
+    uint64_t kv_full[NS];
+    uint64_t kv_empty[NS];
+    uint64_t s_full[kQTiles];
+    uint64_t p_full[kQTiles];
+    uint64_t o_done[kQTiles];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int D, int NS>
+struct SmemLayout {
+    static constexpr int kQBytes = kBM * D * 2;
+    static constexpr int kKVBytes = kBN * D * 2;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kOffQ + kQTiles * kQBytes;
+    static constexpr int kOffBar = kOffKV + NS * kKVBytes;
+    static constexpr int kBytes = kOffBar + static_cast<int>(sizeof(Barriers<NS>));
+    static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024
+};
+
+// Bounded wait on the phase of `bar` with parity `parity`.  Returns false
+// (and sets the abort flag) if the wait ran out of time, or false at once if
+// another role already aborted and `honour_abort` is set.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           bool honour_abort = true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((n & 31u) == 0) {
+            if (honour_abort && *abort_flag) return false;
+            if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicCAS(&g_fa_device_status, 0, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+template <int D, bool BF16, int NS>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FwdParams p) {
+    using L = SmemLayout<D, NS>;
+    constexpr int kChunks = D / 64;   // 128-byte column chunks per row (TMA box width)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    Barriers<NS>* bars = reinterpret_cast<Barriers<NS>*>(smem + L::kOffBar);
+    volatile int* abort_flag = &bars->abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int b = bh / p.H;
+    const int h = bh - b * p.H;
+    const int nqb = gridDim.y;
+    // causal: heaviest query blocks first
+    const int qb = p.causal ? (nqb - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
+    const int q0 = qb * (kQTiles * kBM);
+    const int nkv_all = (p.S + kBN - 1) / kBN;
+    // key tiles each query tile visits (0 for a tile entirely past S)
+    auto tiles_for = [&](int r0) {
+        return (r0 >= p.S) ? 0 : (p.causal ? min(nkv_all, (r0 + kBM - 1) / kBN + 1) : nkv_all);
+    };
+    const int nkv0 = tiles_for(q0);
+    const int nkv1 = tiles_for(q0 + kBM);
+    const int nkv = max(nkv0, nkv1);
+
+    auto bar_addr = [&](const uint64_t* bptr) { return ptx::smem_addr(bptr); };
+
+    // ---------------------------------------------------------------- setup
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar_addr(&bars->q_full), 1);
+        for (int s = 0; s < NS; ++s) {
+            ptx::mbar_init(bar_addr(&bars->kv_full[s]), 1);
+            ptx::mbar_init(bar_addr(&bars->kv_empty[s]), 1);
+        }
+        for (int t = 0; t < kQTiles; ++t) {
+            ptx::mbar_init(bar_addr(&bars->s_full[t]), 1);
+            ptx::mbar_init(bar_addr(&bars->p_full[t]), kBM);
+            ptx::mbar_init(bar_addr(&bars->o_done[t]), 1);
+        }
+        ptx::mbar_init(bar_addr(&bars->drain), 1);
+        bars->abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        ptx::tma_prefetch_map(&tmQ);
+        ptx::tma_prefetch_map(&tmK);
+        ptx::tma_prefetch_map(&tmV);
+        ptx::tma_prefetch_map(&tmO);
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == kLoadWarp) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint32_t qbar = bar_addr(&bars->q_full);
+            uint32_t qbytes = 0;
+            for (int t = 0; t < kQTiles; ++t)
+                if ((t == 0 ? nkv0 : nkv1) > 0) qbytes += L::kQBytes;
+            ptx::mbar_arrive_expect_tx(qbar, qbytes);
+            for (int t = 0; t < kQTiles; ++t) {
+                if ((t == 0 ? nkv0 : nkv1) == 0) continue;
+                for (int c = 0; c < kChunks; ++c)
+                    ptx::tma_load_4d(sbase + L::kOffQ + t * L::kQBytes + c * (kBM * 128), &tmQ, qbar,
+                                     c * 64, h, q0 + t * kBM, b);
+            }
+            int issued = 0;
+            for (int i = 0; i < 2 * nkv; ++i) {
+                const int slot = i % NS;
+                const int round = i / NS;
+                if (round > 0 &&
+                    !wait_phase(bar_addr(&bars->kv_empty[slot]), (round - 1) & 1, abort_flag))
+                    break;
+                const uint32_t fb = bar_addr(&bars->kv_full[slot]);
+                ptx::mbar_arrive_expect_tx(fb, L::kKVBytes);
+                const CUtensorMap* m = (i & 1) ? &tmV : &tmK;
+                const int j = i >> 1;
+                for (int c = 0; c < kChunks; ++c)
+                    ptx::tma_load_4d(sbase + L::kOffKV + slot * L::kKVBytes + c * (kBN * 128), m, fb,
+                                     c * 64, h, j * kBN, b);
+                issued = i + 1;
+            }
+            if (*abort_flag) {
+                // Let every copy this thread started land before the CTA exits.
+                wait_phase(qbar, 0, abort_flag, false);
+                for (int i = max(0, issued - NS); i < issued; ++i)
+                    wait_phase(bar_addr(&bars->kv_full[i % NS]), (i / NS) & 1, abort_flag, false);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
+            constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, D, BF16, true);
+            auto full_bar = [&](int i) { return bar_addr(&bars->kv_full[i % NS]); };
+            auto full_par = [&](int i) { return static_cast<uint32_t>((i / NS) & 1); };
+            auto slot_addr = [&](int i) { return sbase + L::kOffKV + (i % NS) * L::kKVBytes; };
+
+            // S_t = Q_t K^T over D in K=16 steps; both operands K-major.
+            auto issue_s = [&](int t, int ring) {
+                const uint64_t a0 = ptx::sdesc_sw128(sbase + L::kOffQ + t * L::kQBytes, 16, 1024);
+                const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t oa = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                    const uint32_t ob = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+                    ptx::mma_ss(tmem + t * kBN, a0 + (oa >> 4), b0 + (ob >> 4), kIdescQK, kk > 0);
+                }
+            };
+            // O_t (+)= P_t V over the tile's keys in K=16 steps; P from TMEM,
+            // V MN-major (64-column chunks kBN*128 bytes apart).
+            auto issue_pv = [&](int t, int ring, bool acc) {
+                const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), kBN * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + t * kBN + kk * 8,
+                                b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+
+            bool ok = wait_phase(bar_addr(&bars->q_full), 0, abort_flag);
+            if (ok) ok = wait_phase(full_bar(0), full_par(0), abort_flag);
+            if (ok) {
+                ptx::tc_fence_after_sync();
+                for (int t = 0; t < kQTiles; ++t) {
+                    if ((t == 0 ? nkv0 : nkv1) == 0) continue;
+                    issue_s(t, 0);
+                    ptx::tc_commit(bar_addr(&bars->s_full[t]));
+                }
+                ptx::tc_commit(bar_addr(&bars->kv_empty[0]));
+            }
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int iv = 2 * j + 1;
+                const int ik = 2 * j + 2;
+                const bool next = (j + 1) < nkv;
+                if (!(ok = wait_phase(full_bar(iv), full_par(iv), abort_flag))) break;
+                ptx::tc_fence_after_sync();
+                if (j < nkv0) {
+                    if (!(ok = wait_phase(bar_addr(&bars->p_full[0]), j & 1, abort_flag))) break;
+                    ptx::tc_fence_after_sync();
+                    issue_pv(0, iv, j > 0);
+                    ptx::tc_commit(bar_addr(&bars->o_done[0]));
+                }
+                if (next) {
+                    if (!(ok = wait_phase(full_bar(ik), full_par(ik), abort_flag))) break;
+                    ptx::tc_fence_after_sync();
+                }
+                if (j + 1 < nkv0) {
+                    issue_s(0, ik);
+                    ptx::tc_commit(bar_addr(&bars->s_full[0]));
+                }
+                if (j < nkv1) {
+                    if (!(ok = wait_phase(bar_addr(&bars->p_full[1]), j & 1, abort_flag))) break;
+                    ptx::tc_fence_after_sync();
+                    issue_pv(1, iv, j > 0);
+                    ptx::tc_commit(bar_addr(&bars->o_done[1]));
+                }
+                ptx::tc_commit(bar_addr(&bars->kv_empty[iv % NS]));
+                if (j + 1 < nkv1) {
+                    issue_s(1, ik);
+                    ptx::tc_commit(bar_addr(&bars->s_full[1]));
+                }
+                if (next) ptx::tc_commit(bar_addr(&bars->kv_empty[ik % NS]));
+            }
+            // Every MMA must be complete before TMEM is freed.
+            ptx::tc_commit(bar_addr(&bars->drain));
+            wait_phase(bar_addr(&bars->drain), 0, abort_flag, false);
+        }
+    } else {
+        // ----------------------------------------------------- softmax groups
+        const int t = warp >> 2;                 // query tile of this group
+        const int wq = warp & 3;                 // lane quarter of TMEM
+        const int r = wq * 32 + lane;            // row within the tile
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * kBN;
+        const uint32_t tO = tmem + lane_off + 2 * kBN + t * D;
+        const int r0 = q0 + t * kBM;
+        const int row = r0 + r;
+        const float c = p.scale_log2;
+        const int n_tiles = (t == 0) ? nkv0 : nkv1;
+
+        float m_use = -INFINITY;   // reference max, raw (unscaled) score units
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            ok = wait_phase(bar_addr(&bars->s_full[t]), j & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            ptx::tc_fence_after_sync();
+            uint32_t s[kBN];
+#pragma unroll
+            for (int q = 0; q < kBN / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence<kBN>(s);
+
+            const int kv0 = j * kBN;
+            // Mask keys past the end and, on diagonal tiles, keys after the row.
+            if (kv0 + kBN > p.S || (p.causal && kv0 + kBN - 1 > r0)) {
+                const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
+#pragma unroll
+                for (int k = 0; k < kBN; ++k)
+                    if (kv0 + k > last) s[k] = __float_as_uint(-INFINITY);
+            }
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int k = 0; k < kBN; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(s[k]));
+            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            const float m_new = fmaxf(m_use, m_tile);
+            // Lazy rescale: keep the old reference unless the max grew by more
+            // than kTauLog2 in log2 units (then p <= 2^kTauLog2).
+            const bool rescale = (m_new - m_use) * c > kTauLog2;
+            float alpha = 1.f;
+            if (rescale) {
+                alpha = ptx::ex2_approx((m_use - m_new) * c);
+                m_use = m_new;
+            }
+            const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
+
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < kBN / 32; ++q) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[q * 32 + 2 * k]), c, -mc));
+                    const float p1 =
+                        ptx::ex2_approx(fmaf(__uint_as_float(s[q * 32 + 2 * k + 1]), c, -mc));
+                    sum[k & 3] += p0 + p1;
+                    pk[k] = pack2<BF16>(p0, p1);
+                }
+                ptx::tmem_st_32x32b_x16(tS + q * 16, pk);
+            }
+            l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+
+            // O_t was last written by P V of tile j-1, which completed before
+            // S_t of tile j (same issuing thread, in order).
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence<32>(o);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    ptx::tmem_st_32x32b_x32(tO + q * 32, o);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(bar_addr(&bars->p_full[t]));
+        }
+
+        if (n_tiles > 0) {
+            // ---------------------------------------------------- epilogue
+            // Every warp of the group reaches the named barrier below exactly
+            // once, whether or not it aborted, so the barrier cannot hang.
+            bool eok = ok && wait_phase(bar_addr(&bars->o_done[t]), (n_tiles - 1) & 1, abort_flag);
+            eok = __all_sync(0xffffffffu, eok);
+            // Stage O_t in this tile's Q buffer (no longer read by any MMA),
+            // laid out as the 128-byte-swizzled TMA box.
+            uint8_t* stage = smem + L::kOffQ + t * L::kQBytes;
+            const float inv_l = 1.f / l;
+            if (eok) {
+                ptx::tc_fence_after_sync();
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence<32>(o);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {   // four 16-byte chunks of 8 values
+                        const int cc = q * 4 + u;   // chunk index along the row
+                        const int half = cc >> 3;
+                        const int phys = (cc & 7) ^ (r & 7);
+                        uint4 v;
+                        v.x = pack2<BF16>(__uint_as_float(o[u * 8 + 0]) * inv_l,
+                                          __uint_as_float(o[u * 8 + 1]) * inv_l);
+                        v.y = pack2<BF16>(__uint_as_float(o[u * 8 + 2]) * inv_l,
+                                          __uint_as_float(o[u * 8 + 3]) * inv_l);
+                        v.z = pack2<BF16>(__uint_as_float(o[u * 8 + 4]) * inv_l,
+                                          __uint_as_float(o[u * 8 + 5]) * inv_l);
+                        v.w = pack2<BF16>(__uint_as_float(o[u * 8 + 6]) * inv_l,
+                                          __uint_as_float(o[u * 8 + 7]) * inv_l);
+                        *reinterpret_cast<uint4*>(stage + half * (kBM * 128) + r * 128 + phys * 16) = v;
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+            }
+            const bool all_ok = ptx::named_barrier_and(1 + t, kBM, eok);
+            if (all_ok && r == 0) {
+                for (int cch = 0; cch < kChunks; ++cch)
+                    ptx::tma_store_4d(&tmO, ptx::smem_addr(stage + cch * (kBM * 128)), cch * 64, h, r0,
+                                      b);
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group_all();
+            }
+            if (all_ok && p.lse != nullptr && row < p.S) {
+                // LSE = scale * m + ln l = ln2 * (m * scale * log2e + log2 l)
+                p.lse[static_cast<size_t>(bh) * p.S + row] =
+                    (m_use * c + log2f(l)) * 0.69314718055994530942f;
+            }
+        }
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace fa

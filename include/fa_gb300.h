@@ -1,0 +1,103 @@
+/*
+ * fa_gb300.h -- FlashAttention-2 forward pass for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (page "CuTe 详解：以 FlashAttention-2 拆解 Layout、TiledCopy 与
+ * TiledMMA", section 先看全局: S = Q K^T, P = softmax(S), O = P V; the running
+ * state m_i, l_i, o~_i of section 教学配置; the online update of section
+ * 沿 C fragment 做 Online Softmax; the O + softmax-LSE output contract of
+ * section 与官方 FA2 比较时，先对齐契约):
+ *
+ *   for batch b < B, head h < H, query row i < S, key j < S:
+ *     z_ij       = scale * sum_d Q[b,i,h,d] * K[b,j,h,d]
+ *     visible(j) = (j <= i) if causal else true
+ *     O[b,i,h,:] = sum_{visible j} softmax_j(z_i.) * V[b,j,h,:]
+ *     LSE[b,h,i] = ln sum_{visible j} exp(z_ij)          (natural log)
+ *
+ * computed tile by tile with an online softmax so that the S x S scores never
+ * reach device memory.  Products of Q K^T and P V run on the tcgen05 tensor
+ * cores with fp32 accumulation in tensor memory; P is rounded to the input
+ * type before the second product; the row sum uses the unrounded fp32 P.
+ *
+ * Memory layout (all buffers are caller-owned DEVICE memory):
+ *   Q, K, V, O : contiguous [B, S, H, D], element type fp16 or bf16 (all four
+ *                the same), D in {64, 128}; base addresses 16-byte aligned.
+ *   LSE        : contiguous fp32 [B, H, S], or NULL to skip writing it.
+ *
+ * Ownership and ordering: the library keeps no pointer after a call returns
+ * and allocates no device memory.  Work is enqueued on `stream` (0 = the
+ * legacy default stream) and the call returns without waiting for it; the
+ * caller orders any use of O / LSE after the stream.
+ *
+ * Errors: every entry point validates its arguments before launching and
+ * returns an fa_status_t.  Nothing is launched when the status is not FA_OK.
+ *   FA_ERR_INVALID_ARG  a NULL Q/K/V/O, B/H/S < 1, scale not finite or <= 0,
+ *                       an unknown dtype, or sizes whose element count
+ *                       overflows 64 bits
+ *   FA_ERR_UNSUPPORTED  D not in {64, 128}, a base address not 16-byte
+ *                       aligned, or S / B*H beyond the launch limits
+ *   FA_ERR_CUDA         a CUDA runtime or driver call failed (the CUDA error
+ *                       is left set for the caller to read)
+ *   FA_ERR_TIMEOUT      reported by fa_device_status(): a device-side wait
+ *                       exceeded its time limit and the kernel returned early
+ *                       (the outputs of that call are undefined)
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,
+    FA_ERR_UNSUPPORTED = 2,
+    FA_ERR_CUDA = 3,
+    FA_ERR_TIMEOUT = 4
+} fa_status_t;
+
+typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype_t;
+
+/*
+ * Forward pass on fp16 tensors.  Q, K, V, O: [B, S, H, D] fp16 device
+ * pointers; LSE: [B, H, S] fp32 device pointer or NULL; causal: 0 or non-zero
+ * (key j visible to query i iff j <= i); scale: finite, > 0 (1/sqrt(D) is the
+ * usual choice).  Returns an fa_status_t.
+ */
+int fa_fwd_f16(const void* Q, const void* K, const void* V, void* O, float* LSE,
+               int B, int H, int S, int D, int causal, float scale,
+               fa_stream_t stream);
+
+/* The same on bf16 tensors. */
+int fa_fwd_bf16(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                int B, int H, int S, int D, int causal, float scale,
+                fa_stream_t stream);
+
+/* The same with the element type passed as an fa_dtype_t value. */
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+           int B, int H, int S, int D, int causal, float scale, int dtype,
+           fa_stream_t stream);
+
+/* Static text for a status code (never NULL). */
+const char* fa_status_string(int status);
+
+/*
+ * Device-side status of the calls made so far on the current device:
+ * FA_OK, or FA_ERR_TIMEOUT if some kernel gave up on a wait.  Synchronises
+ * the device.  clear != 0 resets the word to FA_OK.  Returns FA_ERR_CUDA if the
+ * status word cannot be read.
+ */
+int fa_device_status(int clear);
+
+/* Number of kernels one fa_fwd call launches (for launch accounting). */
+int fa_kernels_per_call(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,53 @@
+"""Helpers shared by the GPU parity tests (not collected by pytest)."""
+import numpy as np
+
+import fa_inputs
+
+TOL_O = {"f16": 2e-3, "bf16": 8e-3}
+
+
+def lse_tol(ref_lse):
+    return 1e-4 * np.abs(ref_lse) + 1e-4
+
+
+def run_gpu(qb, kb, vb, dtype, causal, scale, with_lse=True, stream=None):
+    """Copy 16-bit inputs to cuda:0, run the library, return (O f64, LSE f64)."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    q, k, v = (fa_inputs.to_torch(x, dtype).cuda() for x in (qb, kb, vb))
+    o, lse = fa.attention_forward(q, k, v, causal=causal, scale=scale, with_lse=with_lse,
+                                  stream=stream)
+    torch.cuda.synchronize()
+    O = o.double().cpu().numpy()
+    L = lse.double().cpu().numpy() if lse is not None else None
+    return O, L
+
+
+# significant bits of the 16-bit output types
+_PREC = {"f16": 11, "bf16": 8}
+_EMIN = {"f16": -14, "bf16": -126}
+
+
+def half_ulp(x, dtype):
+    """Half the spacing of the 16-bit output type at |x|: the error that the
+    final rounding of O to its storage type may add on its own."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** _EMIN[dtype])))
+    return 0.5 * np.exp2(e - (_PREC[dtype] - 1))
+
+
+def o_tol(Oref, dtype):
+    """max|dO| bound: the stated tolerance on the result, plus the half ulp
+    of the 16-bit type that O is stored in."""
+    return TOL_O[dtype] + half_ulp(Oref, dtype)
+
+
+def assert_close(O, L, Oref, Lref, dtype, what=""):
+    dO = np.abs(O - Oref)
+    assert np.all(np.isfinite(O)), f"{what}: non-finite O"
+    bad = dO > o_tol(Oref, dtype)
+    assert not bad.any(), f"{what}: max|dO| = {dO.max():.3e} at {np.unravel_index(dO.argmax(), dO.shape)}"
+    if L is not None:
+        dL = np.abs(L - Lref)
+        bad = dL > lse_tol(Lref)
+        assert not bad.any(), f"{what}: |dLSE| = {dL.max():.3e} at {np.unravel_index(dL.argmax(), dL.shape)}"

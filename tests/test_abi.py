@@ -1,0 +1,93 @@
+"""The C-ABI library builds, loads and exports every declared symbol, and
+rejects bad arguments before touching the GPU.  No compute call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_forward_fwd_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa.build()
+    return fa.library()
+
+
+def _declared_functions():
+    names = []
+    for hdr in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not hdr.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    assert set(fa.EXPORTED_SYMBOLS) <= set(names), names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert fa.fa_status_string(code)
+    assert fa.fa_status_string(99) == "unknown status"
+
+
+def test_kernels_per_call(lib):
+    assert fa.fa_kernels_per_call() == 1
+
+
+GOOD = dict(Q=4096, K=8192, V=12288, O=16384, LSE=20480, B=1, H=1, S=128, D=64,
+            causal=0, scale=0.125, dtype=fa.FA_F16, stream=None)
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(Q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(K=None), fa.FA_ERR_INVALID_ARG),
+    (dict(V=None), fa.FA_ERR_INVALID_ARG),
+    (dict(O=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(S=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(Q=4096 + 8), fa.FA_ERR_UNSUPPORTED),
+    (dict(O=16384 + 2), fa.FA_ERR_UNSUPPORTED),
+    (dict(LSE=20480 + 2), fa.FA_ERR_UNSUPPORTED),
+    (dict(S=256 * 65535 + 1), fa.FA_ERR_UNSUPPORTED),
+])
+def test_bad_arguments_are_rejected_before_launch(lib, change, status):
+    args = dict(GOOD, **change)
+    rc = fa.fa_fwd(args["Q"], args["K"], args["V"], args["O"], args["LSE"], args["B"],
+                   args["H"], args["S"], args["D"], args["causal"], args["scale"],
+                   args["dtype"], args["stream"])
+    assert rc == status
+
+
+def test_dtype_specific_entry_points_validate(lib):
+    assert fa.fa_fwd_f16(None, 1, 1, 1, None, 1, 1, 1, 64, 0, 1.0, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_bf16(16, 16, 16, 16, None, 1, 1, 1, 80, 0, 1.0, None) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_binding_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 8, 1, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        fa.attention_forward(q, q, q)

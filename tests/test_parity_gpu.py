@@ -1,0 +1,169 @@
+"""GPU parity: the sm_103a kernel (through the C-ABI) against the fp64 oracle.
+
+Tolerances: |O_gpu - O_ref| <= 2e-3 (fp16) / 8e-3 (bf16) plus half an ulp of
+the 16-bit type O is stored in (at O_ref: the final rounding of O to that
+type can by itself move it by up to that much), and
+|LSE_gpu - LSE_ref| <= 1e-4 |LSE_ref| + 1e-4, the oracle computing the plain
+definition in fp64 from the same 16-bit inputs.
+"""
+import numpy as np
+import pytest
+
+import fa_inputs
+from oracle import attention_reference, attention_rows
+
+from gpu_common import assert_close, o_tol, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    fa.build()
+    fa.library()
+    fa.fa_device_status(clear=True)
+    yield
+    assert fa.fa_device_status(clear=False) == 0, "a device-side wait timed out"
+
+
+def _full_case(B, H, S, D, dtype, dist, seed, causal, scale=None, ikh=()):
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dtype, dist, seed, identical_key_head=ikh)
+    scale = scale if scale is not None else D ** -0.5
+    O, L = run_gpu(qb, kb, vb, dtype, causal, scale)
+    Oref, Lref = attention_reference(qb, kb, vb, dtype, causal, scale)
+    assert_close(O, L, Oref, Lref, dtype, f"B{B} H{H} S{S} D{D} {dtype} causal={causal}")
+    return O, L, Oref, Lref
+
+
+# ------------------------------------------------------------ small / ragged
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S", [1, 2, 17, 64, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 640])
+def test_ragged_lengths_f16_d64(S, causal):
+    _full_case(2, 3, S, 64, "f16", "normal", 10 + S, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S", [1, 100, 128, 300, 513])
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (128, "f16"), (64, "bf16")])
+def test_ragged_lengths_other_types(S, D, dtype, causal):
+    _full_case(1, 2, S, D, dtype, "normal", 20 + S, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_peaky_logits(causal):
+    """Q, K scaled by 4: max moves by many units across tiles (lazy rescale)."""
+    _full_case(1, 4, 700, 64, "f16", "stress", 5, causal)
+
+
+def test_many_heads_and_batches_layout():
+    """[B, S, H, D] with H > 1 and B > 1: heads and batches land in place."""
+    _full_case(3, 5, 200, 64, "f16", "normal", 6, False)
+    _full_case(3, 5, 200, 128, "bf16", "normal", 7, True)
+
+
+# ------------------------------------------------------------- the workloads
+def test_workload_s256():
+    w = fa_inputs.WORKLOADS["s256"]
+    qb, kb, vb = fa_inputs.make_qkv_for(w)
+    for causal in w.modes:
+        O, L = run_gpu(qb, kb, vb, w.dtype, causal, w.scale)
+        Oref, Lref = attention_reference(qb, kb, vb, w.dtype, causal, w.scale)
+        assert_close(O, L, Oref, Lref, w.dtype, "s256")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_workload_s4096(causal):
+    w = fa_inputs.WORKLOADS["s4096"]
+    qb, kb, vb = fa_inputs.make_qkv_for(w)
+    O, L = run_gpu(qb, kb, vb, w.dtype, causal, w.scale)
+    Oref, Lref = attention_reference(qb, kb, vb, w.dtype, causal, w.scale)
+    assert_close(O, L, Oref, Lref, w.dtype, "s4096")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_workload_stress_full(causal):
+    """B=3,H=8,S=1999 peaky logits, every element against the oracle; the
+    identical-key head equals the (prefix) mean of V."""
+    w = fa_inputs.WORKLOADS["stress"]
+    qb, kb, vb = fa_inputs.make_qkv_for(w)
+    O, L = run_gpu(qb, kb, vb, w.dtype, causal, w.scale)
+    Oref, Lref = attention_reference(qb, kb, vb, w.dtype, causal, w.scale)
+    assert_close(O, L, Oref, Lref, w.dtype, "stress")
+    b, h = w.identical_key_head
+    v = Oref[b, :, h, :]
+    assert np.all(np.abs(O[b, :, h, :] - v) <= o_tol(v, "f16"))
+
+
+def _sampled_rows(S, rng, n=24):
+    fixed = [0, 1, 127, 128, 129, 255, 256, 257, S // 2, S - 129, S - 128, S - 2, S - 1]
+    rows = set(r for r in fixed if 0 <= r < S)
+    rows.update(rng.integers(0, S, size=n - len(rows)).tolist())
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name,causal", [("b4h16", True), ("b2h16d128", True),
+                                         ("b2h16d128", False)])
+def test_workload_full_size_sampled(name, causal):
+    """Full-size workloads in the launch configuration the bench times;
+    sampled rows of several heads against the oracle row by row."""
+    w = fa_inputs.WORKLOADS[name]
+    qb, kb, vb = fa_inputs.make_qkv_for(w)
+    O, L = run_gpu(qb, kb, vb, w.dtype, causal, w.scale)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+    rng = np.random.default_rng(123)
+    heads = [(0, 0), (w.B - 1, w.H - 1)] + [(int(rng.integers(w.B)), int(rng.integers(w.H)))
+                                            for _ in range(4)]
+    for b, h in heads:
+        rows = _sampled_rows(w.S, rng)
+        Oref, Lref = attention_rows(qb, kb, vb, w.dtype, causal, w.scale, b, h, rows)
+        assert_close(O[b, rows, h, :], L[b, h, rows], Oref, Lref, w.dtype, f"{name} b{b} h{h}")
+
+
+# ------------------------------------------------------------ API behaviour
+def test_no_lse_pointer():
+    qb, kb, vb = fa_inputs.make_qkv(1, 2, 300, 64, "f16", "normal", 8)
+    O, L = run_gpu(qb, kb, vb, "f16", True, 0.125, with_lse=False)
+    assert L is None
+    Oref, _ = attention_reference(qb, kb, vb, "f16", True, 0.125)
+    assert np.all(np.abs(O - Oref) <= o_tol(Oref, "f16"))
+
+
+def test_side_stream_and_repeatability():
+    """Bit-identical results over repeated calls on a non-default stream."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    qb, kb, vb = fa_inputs.make_qkv(2, 4, 1000, 64, "f16", "stress", 9)
+    q, k, v = (fa_inputs.to_torch(x, "f16").cuda() for x in (qb, kb, vb))
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(10):
+            o, lse = fa.attention_forward(q, k, v, causal=True, scale=0.125)
+            outs.append((o.clone(), lse.clone()))
+    s.synchronize()
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+
+
+def test_output_written_only_inside_the_tensor():
+    """Rows past S must not be written: surround O with guard bands."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    B, H, S, D = 1, 2, 300, 64
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, "f16", "normal", 11)
+    q, k, v = (fa_inputs.to_torch(x, "f16").cuda() for x in (qb, kb, vb))
+    n = B * S * H * D
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 7.0, dtype=torch.float16, device="cuda")
+    o = buf[guard:guard + n].view(B, S, H, D)
+    lbuf = torch.full((B * H * S + 2 * 64,), 3.0, dtype=torch.float32, device="cuda")
+    lse = lbuf[64:64 + B * H * S].view(B, H, S)
+    fa.attention_forward(q, k, v, causal=False, scale=0.125, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:guard] == 7.0) and torch.all(buf[guard + n:] == 7.0)
+    assert torch.all(lbuf[:64] == 3.0) and torch.all(lbuf[64 + B * H * S:] == 3.0)
+    Oref, Lref = attention_reference(qb, kb, vb, "f16", False, 0.125)
+    assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), Oref, Lref, "f16")
