@@ -15,13 +15,15 @@ from .build import LIB_PATH, build  # noqa: F401
 
 __all__ = ["fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
            "fa_device_status", "fa_kernels_per_call", "attention_forward",
+           "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_launches",
            "FaError", "library", "EXPORTED_SYMBOLS", "FA_F16", "FA_BF16"]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 FA_F16, FA_BF16 = 0, 1
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
-                    "fa_device_status", "fa_kernels_per_call")
+                    "fa_device_status", "fa_kernels_per_call", "fa_splitkv_workspace_size",
+                    "fa_splitkv_launches", "fa_fwd_splitkv")
 
 _LIB = None
 
@@ -53,6 +55,12 @@ def library() -> ctypes.CDLL:
         lib.fa_device_status.restype = i
         lib.fa_kernels_per_call.argtypes = []
         lib.fa_kernels_per_call.restype = i
+        lib.fa_splitkv_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_splitkv_workspace_size.restype = i
+        lib.fa_splitkv_launches.argtypes = [i, i, i, i, i]
+        lib.fa_splitkv_launches.restype = i
+        lib.fa_fwd_splitkv.argtypes = sig + [i, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_splitkv.restype = i
         _LIB = lib
     return _LIB
 
@@ -85,14 +93,54 @@ def fa_fwd_bf16(Q, K, V, O, LSE, B, H, S, D, causal, scale, stream) -> int:
                                      int(bool(causal)), float(scale), stream))
 
 
+def fa_splitkv_workspace_size(B, H, S, D, causal) -> int:
+    """Workspace bytes fa_fwd_splitkv needs on the current device (0: no split)."""
+    n = ctypes.c_size_t(0)
+    rc = int(library().fa_splitkv_workspace_size(int(B), int(H), int(S), int(D),
+                                                 int(bool(causal)), ctypes.byref(n)))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_splitkv_workspace_size")
+    return int(n.value)
+
+
+def fa_splitkv_launches(B, H, S, D, causal) -> int:
+    return int(library().fa_splitkv_launches(int(B), int(H), int(S), int(D), int(bool(causal))))
+
+
+def fa_fwd_splitkv(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype, workspace,
+                   workspace_bytes, stream) -> int:
+    """Raw C-ABI call of the split-over-keys entry point; returns the status."""
+    return int(library().fa_fwd_splitkv(Q, K, V, O, LSE, int(B), int(H), int(S), int(D),
+                                        int(bool(causal)), float(scale), int(dtype),
+                                        workspace, int(workspace_bytes), stream))
+
+
+# workspace buffers of the split path, one per (device, stream): calls on one
+# stream are ordered, so they may share it
+_WORKSPACES = {}
+
+
+def _workspace(device, stream_handle: int, nbytes: int):
+    import torch
+    key = (str(device), int(stream_handle))
+    buf = _WORKSPACES.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _WORKSPACES[key] = buf
+    return buf
+
+
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
-                      out=None, lse=None, with_lse: bool = True, stream=None):
+                      out=None, lse=None, with_lse: bool = True, stream=None,
+                      split_kv: bool = True):
     """O, LSE for torch CUDA tensors q, k, v of shape [B, S, H, D].
 
     q, k, v must be contiguous fp16 or bf16 tensors on the same CUDA device.
     ``out`` / ``lse`` may be preallocated ([B, S, H, D] same dtype; [B, H, S]
     fp32).  Work is enqueued on ``stream`` (default: the current stream) and
-    not waited for.
+    not waited for.  ``split_kv`` lets the library split the keys of each
+    query block over several CTAs when the shape leaves SMs idle (the
+    workspace is allocated with torch and cached per device and stream).
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -120,9 +168,16 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     dtype = FA_F16 if q.dtype == torch.float16 else FA_BF16
     with torch.cuda.device(q.device):
         st = torch.cuda.current_stream().cuda_stream if stream is None else int(stream)
-        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                    lse.data_ptr() if lse is not None else None,
-                    B, H, S, D, causal, scale, dtype, st)
+        lse_ptr = lse.data_ptr() if lse is not None else None
+        nbytes = fa_splitkv_workspace_size(B, H, S, D, causal) if split_kv else 0
+        if nbytes > 0:
+            ws = _workspace(q.device, st, nbytes)
+            rc = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse_ptr, B, H, S, D, causal, scale, dtype, ws.data_ptr(),
+                                ws.numel(), st)
+        else:
+            rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                        B, H, S, D, causal, scale, dtype, st)
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
     return out, lse

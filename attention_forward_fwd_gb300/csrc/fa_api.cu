@@ -56,9 +56,68 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int B, int S, int H, 
     return r == CUDA_SUCCESS;
 }
 
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// How the keys of each query block are split over CTAs.
+struct SplitPlan {
+    int chunk = 0;          // key tiles per split (0: no split)
+    int max_splits = 1;     // splits of the longest query block
+    int ctas_per_head = 0;  // gridDim.y
+};
+
+long long ctas_per_head_for(int S, bool causal, int chunk) {
+    const int nqb = (S + fa::kQTiles * fa::kBM - 1) / (fa::kQTiles * fa::kBM);
+    long long n = 0;
+    for (int qb = 0; qb < nqb; ++qb) n += (fa::key_tiles_for_block(qb, S, causal) + chunk - 1) / chunk;
+    return n;
+}
+
+// Split the keys only when one CTA per query block leaves most of the SMs
+// idle; then take the smallest chunk (>= 2 key tiles) whose grid still fits in
+// one wave of `sms` CTAs.
+SplitPlan plan_split(int B, int H, int S, bool causal, int sms) {
+    SplitPlan plan;
+    const int rows_per_cta = fa::kQTiles * fa::kBM;
+    const int nqb = (S + rows_per_cta - 1) / rows_per_cta;
+    const int nkv_all = (S + fa::kBN - 1) / fa::kBN;
+    plan.ctas_per_head = nqb;
+    const long long base = static_cast<long long>(B) * H * nqb;
+    if (sms <= 0 || base * 4 >= static_cast<long long>(sms) * 3 || nkv_all <= 2) return plan;
+    int lo = 2, hi = nkv_all;   // grid size is non-increasing in the chunk
+    if (static_cast<long long>(B) * H * ctas_per_head_for(S, causal, hi) > sms) return plan;
+    while (lo < hi) {
+        const int mid = (lo + hi) / 2;
+        if (static_cast<long long>(B) * H * ctas_per_head_for(S, causal, mid) <= sms) hi = mid;
+        else lo = mid + 1;
+    }
+    const int max_splits = (nkv_all + lo - 1) / lo;
+    if (max_splits <= 1) return plan;
+    plan.chunk = lo;
+    plan.max_splits = max_splits;
+    plan.ctas_per_head = static_cast<int>(ctas_per_head_for(S, causal, lo));
+    return plan;
+}
+
+size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D) {
+    if (plan.chunk == 0) return 0;
+    const size_t ntq = (S + fa::kBM - 1) / fa::kBM;
+    const size_t slots = static_cast<size_t>(B) * H * ntq * plan.max_splits;
+    return slots * (static_cast<size_t>(fa::kBM) * D + 2 * fa::kBM) * sizeof(float);
+}
+
 template <int D, bool BF16, int NS>
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int S,
-           int causal, float scale, cudaStream_t stream) {
+           int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace) {
     auto kern = fa::fa_fwd_kernel<D, BF16, NS>;
     constexpr int kSmem = fa::SmemLayout<D, NS>::kAlloc;
     // The dynamic shared-memory opt-in is per device; remember it per device.
@@ -85,10 +144,35 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.lse = LSE;
     const int rows_per_cta = fa::kQTiles * fa::kBM;
+    p.nqb = (S + rows_per_cta - 1) / rows_per_cta;
+    p.kv_chunk = plan.chunk;
+    p.max_splits = plan.max_splits;
+    const size_t ntq = (S + fa::kBM - 1) / fa::kBM;
+    const size_t o_floats = static_cast<size_t>(B) * H * ntq * plan.max_splits * fa::kBM * D;
+    p.ws_o = plan.chunk ? static_cast<float*>(workspace) : nullptr;
+    p.ws_ml = plan.chunk ? static_cast<float*>(workspace) + o_floats : nullptr;
     const dim3 grid(static_cast<unsigned>(B) * static_cast<unsigned>(H),
-                    static_cast<unsigned>((S + rows_per_cta - 1) / rows_per_cta));
+                    static_cast<unsigned>(plan.ctas_per_head));
     kern<<<grid, fa::kThreads, kSmem, stream>>>(mq, mk, mv, mo, p);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    if (plan.chunk == 0) return FA_OK;
+
+    // merge the partials; programmatic dependent launch hides the launch gap
+    cudaLaunchConfig_t cfg = {};
+    constexpr int kPerTile = fa::kBM / (fa::kCombineThreads / (D / 8));
+    cfg.gridDim = dim3(static_cast<unsigned>(ntq * kPerTile),
+                       static_cast<unsigned>(B) * static_cast<unsigned>(H));
+    cfg.blockDim = dim3(fa::kCombineThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fa::fa_combine_kernel<D, BF16>, p, O) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
 }
 
 int validate(const void* Q, const void* K, const void* V, void* O, const float* LSE, int B, int H,
@@ -109,6 +193,17 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
     return FA_OK;
 }
 
+int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int S,
+             int D, int causal, float scale, int dtype, cudaStream_t st, const SplitPlan& plan,
+             void* ws) {
+    if (dtype == FA_F16) {
+        if (D == 64) return launch<64, false, 6>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+        return launch<128, false, 4>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+    }
+    if (D == 64) return launch<64, true, 6>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+    return launch<128, true, 4>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+}
+
 }  // namespace
 
 extern "C" {
@@ -117,13 +212,37 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
            int D, int causal, float scale, int dtype, fa_stream_t stream) {
     const int v = validate(Q, K, V, O, LSE, B, H, S, D, scale, dtype);
     if (v != FA_OK) return v;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (dtype == FA_F16) {
-        if (D == 64) return launch<64, false, 6>(Q, K, V, O, LSE, B, H, S, causal, scale, st);
-        return launch<128, false, 4>(Q, K, V, O, LSE, B, H, S, causal, scale, st);
-    }
-    if (D == 64) return launch<64, true, 6>(Q, K, V, O, LSE, B, H, S, causal, scale, st);
-    return launch<128, true, 4>(Q, K, V, O, LSE, B, H, S, causal, scale, st);
+    return dispatch(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype,
+                    reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr);
+}
+
+int fa_splitkv_workspace_size(int B, int H, int S, int D, int causal, size_t* bytes) {
+    if (bytes == nullptr || B < 1 || H < 1 || S < 1) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    const int sms = num_sms();
+    if (sms <= 0) return FA_ERR_CUDA;
+    *bytes = workspace_bytes_for(plan_split(B, H, S, causal != 0, sms), B, H, S, D);
+    return FA_OK;
+}
+
+int fa_splitkv_launches(int B, int H, int S, int D, int causal) {
+    if (B < 1 || H < 1 || S < 1 || (D != 64 && D != 128)) return 0;
+    return plan_split(B, H, S, causal != 0, num_sms()).chunk ? 2 : 1;
+}
+
+int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                   int S, int D, int causal, float scale, int dtype, void* workspace,
+                   size_t workspace_bytes, fa_stream_t stream) {
+    const int v = validate(Q, K, V, O, LSE, B, H, S, D, scale, dtype);
+    if (v != FA_OK) return v;
+    const int sms = num_sms();
+    if (sms <= 0) return FA_ERR_CUDA;
+    const SplitPlan plan = plan_split(B, H, S, causal != 0, sms);
+    const size_t need = workspace_bytes_for(plan, B, H, S, D);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FA_ERR_INVALID_ARG;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 15u)) return FA_ERR_UNSUPPORTED;
+    return dispatch(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype,
+                    reinterpret_cast<cudaStream_t>(stream), plan, workspace);
 }
 
 int fa_fwd_f16(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,

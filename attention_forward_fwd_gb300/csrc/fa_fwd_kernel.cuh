@@ -61,7 +61,43 @@ struct FwdParams {
     int causal;
     float scale_log2;   // scale * log2(e)
     float* lse;         // [B, H, S] fp32 or nullptr
+    // Split over keys (0 = off).  With kv_chunk > 0 the CTAs of one head are
+    // the (query block, split) pairs, heaviest blocks first when causal; split
+    // s of a query block covers key tiles [s*kv_chunk, (s+1)*kv_chunk).  A
+    // block with more than one split writes partial results (see
+    // PartialLayout) that fa_combine_kernel merges.
+    int nqb;            // query blocks of kQTiles*kBM rows per head
+    int kv_chunk;       // key tiles per split, 0 = no split
+    int max_splits;     // splits of the longest query block
+    float* ws_o;        // partial o~ tiles (fp32)
+    float* ws_ml;       // partial (m * scale * log2e, l) per row
 };
+
+// Workspace of the split-over-keys path.  One partial slot per (b*H + h,
+// query tile qt of 128 rows, split s):
+//   slot = ((bh * ntq) + qt) * max_splits + s,   ntq = ceil(S / 128)
+//   ws_o  + slot * 128 * D  : o~ rows, fp32, as [D/4][128] float4 (column
+//                             chunk major, so a warp's stores are contiguous)
+//   ws_ml + slot * 256      : [0,128) m in log2 units, [128,256) l
+// A tile that saw no key in a split records l = 0 (and m = -inf).
+__host__ __device__ inline size_t partial_slot(int bh, int ntq, int qt, int max_splits, int s) {
+    return (static_cast<size_t>(bh) * ntq + qt) * max_splits + s;
+}
+
+// Key tiles (of kBN) that a query tile starting at row r0 visits: all tiles
+// holding a key < S, or, when causal, up to the tile holding its last row.
+__host__ __device__ inline int key_tiles_for(int r0, int S, bool causal) {
+    const int nkv_all = (S + kBN - 1) / kBN;
+    if (r0 >= S) return 0;
+    return causal ? min(nkv_all, (r0 + kBM - 1) / kBN + 1) : nkv_all;
+}
+
+// Key tiles of a query block (the longest of its kQTiles query tiles).
+__host__ __device__ inline int key_tiles_for_block(int qb, int S, bool causal) {
+    int n = 0;
+    for (int t = 0; t < kQTiles; ++t) n = max(n, key_tiles_for(qb * kQTiles * kBM + t * kBM, S, causal));
+    return n;
+}
 
 template <int NS>
 struct Barriers {
@@ -137,18 +173,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = blockIdx.x;
     const int b = bh / p.H;
     const int h = bh - b * p.H;
-    const int nqb = gridDim.y;
-    // causal: heaviest query blocks first
-    const int qb = p.causal ? (nqb - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
+    const bool causal = p.causal != 0;
+    // ---- which query block and which key tiles this CTA owns
+    int qb, jb, je, nsplit, split;
+    if (p.kv_chunk <= 0) {
+        // causal: heaviest query blocks first
+        qb = causal ? (p.nqb - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
+        jb = 0;
+        je = 0x7fffffff;
+        nsplit = 1;
+        split = 0;
+    } else {
+        int y = static_cast<int>(blockIdx.y);
+        qb = 0;
+        nsplit = 1;
+        for (int i = 0; i < p.nqb; ++i) {
+            const int qbi = causal ? (p.nqb - 1 - i) : i;
+            const int ns = (key_tiles_for_block(qbi, p.S, causal) + p.kv_chunk - 1) / p.kv_chunk;
+            if (y < ns) {
+                qb = qbi;
+                nsplit = ns;
+                break;
+            }
+            y -= ns;
+        }
+        split = y;
+        jb = split * p.kv_chunk;
+        je = jb + p.kv_chunk;
+    }
     const int q0 = qb * (kQTiles * kBM);
-    const int nkv_all = (p.S + kBN - 1) / kBN;
-    // key tiles each query tile visits (0 for a tile entirely past S)
-    auto tiles_for = [&](int r0) {
-        return (r0 >= p.S) ? 0 : (p.causal ? min(nkv_all, (r0 + kBM - 1) / kBN + 1) : nkv_all);
-    };
-    const int nkv0 = tiles_for(q0);
-    const int nkv1 = tiles_for(q0 + kBM);
+    // tiles [jb, jb + nkv_t) of this CTA's key range for query tile t
+    const int nkv0 = max(0, min(je, key_tiles_for(q0, p.S, causal)) - jb);
+    const int nkv1 = max(0, min(je, key_tiles_for(q0 + kBM, p.S, causal)) - jb);
     const int nkv = max(nkv0, nkv1);
+    const bool partial = nsplit > 1;
 
     auto bar_addr = [&](const uint64_t* bptr) { return ptx::smem_addr(bptr); };
 
@@ -182,6 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
+    // A dependent combine launch (split over keys) may be scheduled as soon
+    // as every CTA of this grid is running; it waits for this grid to finish.
+    ptx::launch_dependents();
 
     if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
@@ -210,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = i >> 1;
                 for (int c = 0; c < kChunks; ++c)
                     ptx::tma_load_4d(sbase + L::kOffKV + slot * L::kKVBytes + c * (kBN * 128), m, fb,
-                                     c * 64, h, j * kBN, b);
+                                     c * 64, h, (jb + j) * kBN, b);
                 issued = i + 1;
             }
             if (*abort_flag) {
@@ -325,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld_wait();
             ptx::reg_fence<kBN>(s);
 
-            const int kv0 = j * kBN;
+            const int kv0 = (jb + j) * kBN;
             // Mask keys past the end and, on diagonal tiles, keys after the row.
             if (kv0 + kBN > p.S || (p.causal && kv0 + kBN - 1 > r0)) {
                 const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
@@ -383,7 +444,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive(bar_addr(&bars->p_full[t]));
         }
 
-        if (n_tiles > 0) {
+        if (partial) {
+            // ------------------------------------ epilogue: partial result
+            // o~ stays unnormalised (fp32); m and l go beside it.  A query
+            // tile that saw no key of this split records l = 0.
+            if (r0 < p.S) {
+                const int ntq = (p.S + kBM - 1) / kBM;
+                const size_t slot = partial_slot(bh, ntq, r0 / kBM, p.max_splits, split);
+                float* ml = p.ws_ml + slot * (2 * kBM);
+                float4* po = reinterpret_cast<float4*>(p.ws_o + slot * static_cast<size_t>(kBM * D));
+                bool eok = ok;
+                if (n_tiles > 0)
+                    eok = eok && wait_phase(bar_addr(&bars->o_done[t]), (n_tiles - 1) & 1, abort_flag);
+                eok = __all_sync(0xffffffffu, eok);
+                if (eok && n_tiles > 0) {
+                    ptx::tc_fence_after_sync();
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence<32>(o);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            po[(q * 8 + u) * kBM + r] =
+                                make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
+                                            __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]));
+                    }
+                    ml[r] = m_use * c;
+                    ml[kBM + r] = l;
+                } else if (eok) {
+                    ml[r] = -INFINITY;
+                    ml[kBM + r] = 0.f;
+                }
+            }
+        } else if (n_tiles > 0) {
             // ---------------------------------------------------- epilogue
             // Every warp of the group reaches the named barrier below exactly
             // once, whether or not it aborted, so the barrier cannot hang.
@@ -442,6 +537,103 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Merges the partial results of the split-over-keys path: for each row,
+// M = max_s m_s, l = sum_s l_s 2^(m_s - M), O = sum_s o~_s 2^(m_s - M) / l and
+// LSE = ln2 (M + log2 l) -- the same rescaling by alpha = exp(m_old - m_new)
+// as the online update of section 沿 C fragment 做 Online Softmax, applied
+// across splits instead of across tiles.  A CTA covers kCombineRows rows of
+// one query tile of one (b, h); thread (r, c) produces the 8 outputs of row r,
+// columns [8c, 8c+8).  Launched as a programmatic dependent of the main
+// kernel: it waits for that grid to complete before reading its partials.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineMaxSplits = 16;   // weights kept in registers up to this
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kCombineThreads) fa_combine_kernel(const FwdParams p, void* O) {
+    constexpr int kCols = D / 8;                        // 8-column chunks per row
+    constexpr int kRows = kCombineThreads / kCols;      // rows per CTA
+    constexpr int kPerTile = kBM / kRows;               // CTAs per query tile
+    const int qt = blockIdx.x / kPerTile;
+    const int bh = blockIdx.y;
+    const bool causal = p.causal != 0;
+    const int ns = (key_tiles_for_block(qt / kQTiles, p.S, causal) + p.kv_chunk - 1) / p.kv_chunk;
+    if (ns <= 1) return;   // this tile was written by the main kernel
+    ptx::grid_dependency_wait();
+    const int r = (blockIdx.x % kPerTile) * kRows + static_cast<int>(threadIdx.x) % kRows;
+    const int cchunk = static_cast<int>(threadIdx.x) / kRows;
+    const int row = qt * kBM + r;
+    if (row >= p.S) return;
+    const int b = bh / p.H;
+    const int h = bh - b * p.H;
+    const int ntq = (p.S + kBM - 1) / kBM;
+    const size_t slot0 = partial_slot(bh, ntq, qt, p.max_splits, 0);
+    const float* ml0 = p.ws_ml + slot0 * (2 * kBM);
+    const float4* po0 = reinterpret_cast<const float4*>(p.ws_o + slot0 * static_cast<size_t>(kBM * D));
+    constexpr size_t kSlotMl = 2 * kBM;
+    constexpr size_t kSlotO = static_cast<size_t>(kBM) * D / 4;   // float4 per slot
+
+    float M = -INFINITY;
+    float msp[kCombineMaxSplits], lsp[kCombineMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kCombineMaxSplits; ++s) {
+        msp[s] = -INFINITY;
+        lsp[s] = 0.f;
+        if (s < ns) {
+            msp[s] = ml0[s * kSlotMl + r];
+            lsp[s] = ml0[s * kSlotMl + kBM + r];
+        }
+    }
+    for (int s = kCombineMaxSplits; s < ns; ++s)
+        if (ml0[s * kSlotMl + kBM + r] > 0.f) M = fmaxf(M, ml0[s * kSlotMl + r]);
+#pragma unroll
+    for (int s = 0; s < kCombineMaxSplits; ++s)
+        if (lsp[s] > 0.f) M = fmaxf(M, msp[s]);
+    float Lsum = 0.f;
+#pragma unroll
+    for (int s = 0; s < kCombineMaxSplits; ++s) {
+        // weight of split s before normalisation (0 when it saw no key)
+        msp[s] = lsp[s] > 0.f ? ptx::ex2_approx(msp[s] - M) : 0.f;
+        Lsum += lsp[s] * msp[s];
+    }
+    for (int s = kCombineMaxSplits; s < ns; ++s) {
+        const float ls = ml0[s * kSlotMl + kBM + r];
+        if (ls > 0.f) Lsum += ls * ptx::ex2_approx(ml0[s * kSlotMl + r] - M);
+    }
+    const float inv_l = 1.f / Lsum;
+
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const float4* pa = po0 + (2 * cchunk) * kBM + r;
+#pragma unroll
+    for (int s = 0; s < kCombineMaxSplits; ++s) {
+        if (s < ns && msp[s] > 0.f) {
+            const float4 x = pa[s * kSlotO];
+            const float4 y = pa[s * kSlotO + kBM];
+            const float w = msp[s];
+            acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+            acc[4] += w * y.x; acc[5] += w * y.y; acc[6] += w * y.z; acc[7] += w * y.w;
+        }
+    }
+    for (int s = kCombineMaxSplits; s < ns; ++s) {
+        const float ls = ml0[s * kSlotMl + kBM + r];
+        if (!(ls > 0.f)) continue;
+        const float w = ptx::ex2_approx(ml0[s * kSlotMl + r] - M);
+        const float4 x = pa[s * kSlotO];
+        const float4 y = pa[s * kSlotO + kBM];
+        acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+        acc[4] += w * y.x; acc[5] += w * y.y; acc[6] += w * y.z; acc[7] += w * y.w;
+    }
+    uint4 v;
+    v.x = pack2<BF16>(acc[0] * inv_l, acc[1] * inv_l);
+    v.y = pack2<BF16>(acc[2] * inv_l, acc[3] * inv_l);
+    v.z = pack2<BF16>(acc[4] * inv_l, acc[5] * inv_l);
+    v.w = pack2<BF16>(acc[6] * inv_l, acc[7] * inv_l);
+    uint16_t* out = reinterpret_cast<uint16_t*>(O) +
+                    ((static_cast<size_t>(b) * p.S + row) * p.H + h) * D + cchunk * 8;
+    *reinterpret_cast<uint4*>(out) = v;
+    if (p.lse != nullptr && cchunk == 0)
+        p.lse[static_cast<size_t>(bh) * p.S + row] = (M + log2f(Lsum)) * 0.69314718055994530942f;
 }
 
 }  // namespace fa

@@ -248,6 +248,19 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// --------------------------------------------- programmatic dependent launch
+// Lets a dependent grid launched with programmatic stream serialisation be
+// scheduled once every CTA of this grid has issued this (or exited).
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on have completed and their memory
+// operations are visible (a no-op without such a dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

@@ -6,7 +6,9 @@
 
 One step = one pass of the hot path over one batch of the workload: every
 mask mode the workload is run with (s4096: non-causal and causal), each one
-call of the C-ABI entry point.  Metric: attention forward TFLOP/s, counting
+call of the C-ABI entry point fa_fwd_splitkv (which splits the keys of each
+query block over several CTAs when the shape would leave SMs idle, and then
+launches the merge kernel as a second launch).  Metric: attention forward TFLOP/s, counting
 4*B*H*S^2*D FLOPs per call (half when causal), and its fraction of the
 measured dense bf16/fp16 tensor peak.
 
@@ -147,34 +149,32 @@ def _dist_env():
 
 
 # --------------------------------------------------------------------- oracle
-def cpu_baseline(w: fa_inputs.Workload, budget_s: float = 15.0):
+def cpu_baseline(w: fa_inputs.Workload, budget_s: float = 15.0, inputs=None):
     """Time the fp64 oracle on a bounded sample of the workload: whole heads
-    of the workload, one after another, until the budget is spent (at least
-    one head per mode)."""
+    (all rows, every mask mode of the workload) one after another, cycling
+    over the workload's heads, until ``budget_s`` seconds are spent (at least
+    one head)."""
     from oracle import attention_rows
-    qb, kb, vb = fa_inputs.make_qkv_for(w)
+    qb, kb, vb = inputs if inputs is not None else fa_inputs.make_qkv_for(w)
     flops = 0.0
     heads = 0
-    t0 = time.perf_counter()
     rows = np.arange(w.S)
-    done = False
-    for b in range(w.B):
-        for h in range(w.H):
-            for causal in w.modes:
-                attention_rows(qb, kb, vb, w.dtype, causal, w.scale, b, h, rows)
-                flops += fa_inputs.attention_flops(1, 1, w.S, w.D, causal)
-            heads += 1
-            if time.perf_counter() - t0 > budget_s:
-                done = True
-                break
-        if done:
+    order = [(b, h) for b in range(w.B) for h in range(w.H)]
+    t0 = time.perf_counter()
+    while True:
+        b, h = order[heads % len(order)]
+        for causal in w.modes:
+            attention_rows(qb, kb, vb, w.dtype, causal, w.scale, b, h, rows)
+            flops += fa_inputs.attention_flops(1, 1, w.S, w.D, causal)
+        heads += 1
+        if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{heads} of {w.B * w.H} heads of {w.name}, all {w.S} rows, "
-                      f"modes {['causal' if c else 'non-causal' for c in w.modes]}, "
-                      f"fp64 numpy (BLAS threads = cores), {dt:.1f} s"}
+            "sample": f"{heads} (b,h) heads of {w.name} ({w.B * w.H} in the workload), all "
+                      f"{w.S} rows, modes {['causal' if c else 'non-causal' for c in w.modes]}; "
+                      f"fp64 numpy, BLAS threads = cores; {dt:.1f} s"}
 
 
 def run_reference(args, w):
@@ -185,8 +185,11 @@ def run_reference(args, w):
         pass  # the oracle has no warm state; warm-up steps are not needed
     times = []
     cb = None
+    inputs = fa_inputs.make_qkv_for(w)
+    # keep the whole run within a couple of minutes whatever --steps is
+    per_step = max(0.5, min(args.ref_budget, 120.0 / max(1, args.steps)))
     for _ in range(args.steps):
-        cb = cpu_baseline(w, budget_s=args.ref_budget)
+        cb = cpu_baseline(w, budget_s=per_step, inputs=inputs)
         times.append(cb["value"])
     value = statistics.median(times)
     cb["value"] = value
@@ -230,17 +233,22 @@ def run_ours(args, w):
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    # split-over-keys workspace (0 bytes when the shape fills the GPU)
+    ws_bytes = max(fa.fa_splitkv_workspace_size(w.B, w.H, w.S, w.D, c) for c in modes)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    def call(qp, kp, vp, o, lse, causal):
+        rc = lib.fa_fwd_splitkv(qp, kp, vp, o.data_ptr(), lse.data_ptr(), w.B, w.H, w.S, w.D,
+                                int(causal), w.scale, dtype_code, ws.data_ptr(), ws.numel(), sp)
+        if rc != 0:
+            raise fa.FaError(rc, "fa_fwd_splitkv")
 
     def step():
         for causal, o, lse in zip(modes, outs, lses):
-            rc = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                            lse.data_ptr(), w.B, w.H, w.S, w.D, int(causal), w.scale,
-                            dtype_code, sp)
-            if rc != 0:
-                raise fa.FaError(rc, "fa_fwd")
+            call(q.data_ptr(), k.data_ptr(), v.data_ptr(), o, lse, causal)
 
     flops_step = sum(fa_inputs.attention_flops(w.B, w.H, w.S, w.D, c) for c in modes)
-    launches_per_step = len(modes) * fa.fa_kernels_per_call()
+    launches_per_step = sum(fa.fa_splitkv_launches(w.B, w.H, w.S, w.D, c) for c in modes)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -292,11 +300,7 @@ def run_ours(args, w):
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
             for causal, o, lse, h_o, h_l in zip(modes, outs, lses, ho, hl):
-                rc = lib.fa_fwd(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o.data_ptr(),
-                                lse.data_ptr(), w.B, w.H, w.S, w.D, int(causal), w.scale,
-                                dtype_code, sp)
-                if rc != 0:
-                    raise fa.FaError(rc, "fa_fwd")
+                call(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o, lse, causal)
                 h_o.copy_(o, non_blocking=True)
                 h_l.copy_(lse, non_blocking=True)
 
@@ -327,7 +331,8 @@ def run_ours(args, w):
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": _traffic(w.name),
                 "peak_kind": f"{peak_kind} bf16 burst (fp16 has the same dense rate)",
-                "kernel": "fa::fa_fwd_kernel", "algorithmic_flops_per_step": flops_step,
+                "kernel": "fa::fa_fwd_kernel (+ fa::fa_combine_kernel when split; timed together)",
+                "algorithmic_flops_per_step": flops_step,
                 "launches_per_step": launches_per_step}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -366,6 +371,8 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
         o = torch.empty_like(q)
         lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
         code = fa.FA_F16 if w.dtype == "f16" else fa.FA_BF16
+        nws = max(fa.fa_splitkv_workspace_size(w.B, w.H, w.S, w.D, c) for c in w.modes)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
         for causal in w.modes:
             ms = []
             with torch.cuda.stream(stream):
@@ -374,9 +381,10 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
-                    rc = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                    lse.data_ptr(), w.B, w.H, w.S, w.D, int(causal), w.scale,
-                                    code, stream.cuda_stream)
+                    rc = lib.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            o.data_ptr(), lse.data_ptr(), w.B, w.H, w.S, w.D,
+                                            int(causal), w.scale, code, ws.data_ptr(),
+                                            ws.numel(), stream.cuda_stream)
                     e1.record(stream)
                     assert rc == 0
                     if i >= 3:
@@ -385,8 +393,9 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
             t = statistics.median(a.elapsed_time(b) for a, b in ms)
             tf = fa_inputs.attention_flops(w.B, w.H, w.S, w.D, causal) / (t * 1e-3) / 1e12
             res[f"{name}/{'causal' if causal else 'non-causal'}"] = {
-                "ms": t, "tflops": tf, "pct_of_peak": 100.0 * tf / peak}
-        del q, k, v, o, lse
+                "ms": t, "tflops": tf, "pct_of_peak": 100.0 * tf / peak,
+                "launches": fa.fa_splitkv_launches(w.B, w.H, w.S, w.D, causal)}
+        del q, k, v, o, lse, ws
     return res
 
 

@@ -44,6 +44,8 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -81,6 +83,32 @@ int fa_fwd_bf16(const void* Q, const void* K, const void* V, void* O, float* LSE
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
            int B, int H, int S, int D, int causal, float scale, int dtype,
            fa_stream_t stream);
+
+/*
+ * Split over keys (for shapes whose B * H * ceil(S / 256) query blocks leave
+ * most SMs idle).  The keys of each query block are divided among several
+ * CTAs; each writes a partial result (unnormalised fp32 output rows, the row
+ * max and the row sum) to `workspace`, and a second kernel, launched on the
+ * same stream as a programmatic dependent of the first, merges them with the
+ * same exp(m_old - m_new) rescaling that the online softmax uses across key
+ * tiles (page "CuTe 详解：以 FlashAttention-2 拆解 Layout、TiledCopy 与 TiledMMA",
+ * section 沿 C fragment 做 Online Softmax).
+ *
+ * fa_splitkv_workspace_size: bytes of device workspace fa_fwd_splitkv needs
+ * for this shape on the current device (0 when the shape is not split).
+ * fa_splitkv_launches: kernels one fa_fwd_splitkv call launches (1 or 2; 0
+ * for invalid sizes).
+ * fa_fwd_splitkv: as fa_fwd, plus a caller-owned device workspace of
+ * workspace_bytes bytes (16-byte aligned; may be NULL when the size query
+ * returned 0).  Its contents need no initialisation and are overwritten.
+ * Calls that share a workspace must be ordered on one stream.  Returns
+ * FA_ERR_INVALID_ARG when the workspace is missing or too small.
+ */
+int fa_splitkv_workspace_size(int B, int H, int S, int D, int causal, size_t* bytes);
+int fa_splitkv_launches(int B, int H, int S, int D, int causal);
+int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                   int B, int H, int S, int D, int causal, float scale, int dtype,
+                   void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /* Static text for a status code (never NULL). */
 const char* fa_status_string(int status);

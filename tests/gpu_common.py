@@ -10,13 +10,13 @@ def lse_tol(ref_lse):
     return 1e-4 * np.abs(ref_lse) + 1e-4
 
 
-def run_gpu(qb, kb, vb, dtype, causal, scale, with_lse=True, stream=None):
+def run_gpu(qb, kb, vb, dtype, causal, scale, with_lse=True, stream=None, split_kv=True):
     """Copy 16-bit inputs to cuda:0, run the library, return (O f64, LSE f64)."""
     import torch
     import attention_forward_fwd_gb300 as fa
     q, k, v = (fa_inputs.to_torch(x, dtype).cuda() for x in (qb, kb, vb))
     o, lse = fa.attention_forward(q, k, v, causal=causal, scale=scale, with_lse=with_lse,
-                                  stream=stream)
+                                  stream=stream, split_kv=split_kv)
     torch.cuda.synchronize()
     O = o.double().cpu().numpy()
     L = lse.double().cpu().numpy() if lse is not None else None

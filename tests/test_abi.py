@@ -91,3 +91,18 @@ def test_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 8, 1, 64, dtype=torch.float16)
     with pytest.raises(ValueError):
         fa.attention_forward(q, q, q)
+
+
+def test_splitkv_entry_points_validate_before_cuda(lib):
+    import ctypes
+    assert lib.fa_splitkv_workspace_size(1, 1, 128, 64, 0, None) == fa.FA_ERR_INVALID_ARG
+    n = ctypes.c_size_t(0)
+    assert lib.fa_splitkv_workspace_size(1, 1, 128, 80, 0, ctypes.byref(n)) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_splitkv_workspace_size(0, 1, 128, 64, 0, ctypes.byref(n)) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_splitkv_launches(1, 1, 0, 64, 0) == 0
+    bad = fa.fa_fwd_splitkv(None, 16, 16, 16, None, 1, 1, 128, 64, 0, 0.125, fa.FA_F16,
+                            None, 0, None)
+    assert bad == fa.FA_ERR_INVALID_ARG
+    bad = fa.fa_fwd_splitkv(16, 16, 16, 16, None, 1, 1, 128, 96, 0, 0.125, fa.FA_F16,
+                            None, 0, None)
+    assert bad == fa.FA_ERR_UNSUPPORTED

@@ -29,33 +29,73 @@ def _lib():
     assert fa.fa_device_status(clear=False) == 0, "a device-side wait timed out"
 
 
-def _full_case(B, H, S, D, dtype, dist, seed, causal, scale=None, ikh=()):
+def _full_case(B, H, S, D, dtype, dist, seed, causal, scale=None, ikh=(), split_kv=False):
     qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dtype, dist, seed, identical_key_head=ikh)
     scale = scale if scale is not None else D ** -0.5
-    O, L = run_gpu(qb, kb, vb, dtype, causal, scale)
+    O, L = run_gpu(qb, kb, vb, dtype, causal, scale, split_kv=split_kv)
     Oref, Lref = attention_reference(qb, kb, vb, dtype, causal, scale)
-    assert_close(O, L, Oref, Lref, dtype, f"B{B} H{H} S{S} D{D} {dtype} causal={causal}")
+    assert_close(O, L, Oref, Lref, dtype,
+                 f"B{B} H{H} S{S} D{D} {dtype} causal={causal} split={split_kv}")
     return O, L, Oref, Lref
 
 
+def _splits(B, H, S, D, causal):
+    import attention_forward_fwd_gb300 as fa
+    return fa.fa_splitkv_launches(B, H, S, D, causal) == 2
+
+
 # ------------------------------------------------------------ small / ragged
+@pytest.mark.parametrize("split_kv", [False, True], ids=["one-cta-per-block", "split-kv"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("S", [1, 2, 17, 64, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 640])
-def test_ragged_lengths_f16_d64(S, causal):
-    _full_case(2, 3, S, 64, "f16", "normal", 10 + S, causal)
+def test_ragged_lengths_f16_d64(S, causal, split_kv):
+    _full_case(2, 3, S, 64, "f16", "normal", 10 + S, causal, split_kv=split_kv)
 
 
+@pytest.mark.parametrize("split_kv", [False, True], ids=["one-cta-per-block", "split-kv"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("S", [1, 100, 128, 300, 513])
 @pytest.mark.parametrize("D,dtype", [(128, "bf16"), (128, "f16"), (64, "bf16")])
-def test_ragged_lengths_other_types(S, D, dtype, causal):
-    _full_case(1, 2, S, D, dtype, "normal", 20 + S, causal)
+def test_ragged_lengths_other_types(S, D, dtype, causal, split_kv):
+    _full_case(1, 2, S, D, dtype, "normal", 20 + S, causal, split_kv=split_kv)
+
+
+@pytest.mark.parametrize("split_kv", [False, True], ids=["one-cta-per-block", "split-kv"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_peaky_logits(causal, split_kv):
+    """Q, K scaled by 4: max moves by many units across tiles (lazy rescale)."""
+    _full_case(1, 4, 700, 64, "f16", "stress", 5, causal, split_kv=split_kv)
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_peaky_logits(causal):
-    """Q, K scaled by 4: max moves by many units across tiles (lazy rescale)."""
-    _full_case(1, 4, 700, 64, "f16", "stress", 5, causal)
+@pytest.mark.parametrize("S,D,dtype", [(700, 64, "f16"), (1999, 64, "f16"), (2048, 128, "bf16"),
+                                       (3000, 128, "f16"), (4096, 64, "bf16")])
+def test_split_kv_path_is_taken_and_exact(S, D, dtype, causal):
+    """Shapes with one head: the keys are split over CTAs and the partial
+    results merged; the result matches the oracle like the unsplit path."""
+    assert _splits(1, 1, S, D, causal)
+    _full_case(1, 1, S, D, dtype, "stress", 30 + S, causal, split_kv=True)
+
+
+def test_split_kv_workspace_checks():
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    B, H, S, D = 1, 1, 2048, 64
+    need = fa.fa_splitkv_workspace_size(B, H, S, D, False)
+    assert need > 0
+    q = torch.zeros(B, S, H, D, dtype=torch.float16, device="cuda")
+    o = torch.empty_like(q)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    args = (q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), None, B, H, S, D, 0, 0.125,
+            fa.FA_F16)
+    assert fa.fa_fwd_splitkv(*args, None, need, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need - 1, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr() + 4, need, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need, None) == fa.FA_OK
+    torch.cuda.synchronize()
+    # a shape that fills the GPU needs no workspace and takes one launch
+    assert fa.fa_splitkv_workspace_size(4, 16, 4096, 64, True) == 0
+    assert fa.fa_splitkv_launches(4, 16, 4096, 64, True) == 1
 
 
 def test_many_heads_and_batches_layout():
@@ -74,11 +114,12 @@ def test_workload_s256():
         assert_close(O, L, Oref, Lref, w.dtype, "s256")
 
 
+@pytest.mark.parametrize("split_kv", [False, True], ids=["one-cta-per-block", "split-kv"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_workload_s4096(causal):
+def test_workload_s4096(causal, split_kv):
     w = fa_inputs.WORKLOADS["s4096"]
     qb, kb, vb = fa_inputs.make_qkv_for(w)
-    O, L = run_gpu(qb, kb, vb, w.dtype, causal, w.scale)
+    O, L = run_gpu(qb, kb, vb, w.dtype, causal, w.scale, split_kv=split_kv)
     Oref, Lref = attention_reference(qb, kb, vb, w.dtype, causal, w.scale)
     assert_close(O, L, Oref, Lref, w.dtype, "s4096")
 
