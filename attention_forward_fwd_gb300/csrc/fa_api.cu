@@ -282,3 +282,67 @@ int fa_device_status(int clear) {
 int fa_kernels_per_call(void) { return 1; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of fa_fwd_splitkv.
+//
+// Some callers cannot call cudaMalloc: a latency-critical loop that must not
+// pay for cudaMalloc's implicit device synchronisation, a program whose device
+// memory belongs to an allocator it cannot reach from this call site, or
+// plain C code that links only this library.  For them the split-over-keys
+// scratch lives in one file-scope device array, so a call needs no workspace
+// argument and allocates nothing.  The array (kStaticWorkspaceBytes) is
+// reserved on every GPU that loads this library until the process exits.
+namespace {
+constexpr size_t kStaticWorkspaceBytes = static_cast<size_t>(24) << 20;   // 24 MiB
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_fa_static_workspace[kStaticWorkspaceBytes];
+
+namespace {
+
+// In host code `g_fa_static_workspace` only names a host-side stand-in for
+// the symbol; its device address is looked up once per device, with that
+// device current, on the first call made on it.
+void* static_workspace_address(int* status) {
+    static std::once_flag once[64];
+    static void* address[64];
+    static cudaError_t lookup[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *status = FA_ERR_CUDA;
+        return nullptr;
+    }
+    std::call_once(once[dev], [&] {
+        void* p = nullptr;
+        lookup[dev] = cudaGetSymbolAddress(&p, g_fa_static_workspace);
+        address[dev] = p;
+    });
+    if (lookup[dev] != cudaSuccess || address[dev] == nullptr) {
+        *status = FA_ERR_CUDA;
+        return nullptr;
+    }
+    return address[dev];
+}
+
+}  // namespace
+
+extern "C" int fa_fwd_splitkv_static(const void* Q, const void* K, const void* V, void* O,
+                                     float* LSE, int B, int H, int S, int D, int causal,
+                                     float scale, int dtype, fa_stream_t stream) {
+    const int v = validate(Q, K, V, O, LSE, B, H, S, D, scale, dtype);
+    if (v != FA_OK) return v;
+    const int sms = num_sms();
+    if (sms <= 0) return FA_ERR_CUDA;
+    const SplitPlan plan = plan_split(B, H, S, causal != 0, sms);
+    const size_t need = workspace_bytes_for(plan, B, H, S, D);
+    if (need > kStaticWorkspaceBytes) return FA_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    if (need > 0) {
+        int status = FA_OK;
+        ws = static_workspace_address(&status);
+        if (ws == nullptr) return status;
+    }
+    return dispatch(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype,
+                    reinterpret_cast<cudaStream_t>(stream), plan, ws);
+}

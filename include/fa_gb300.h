@@ -110,6 +110,37 @@ int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* 
                    int B, int H, int S, int D, int causal, float scale, int dtype,
                    void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
+/*
+ * fa_fwd_splitkv without a workspace argument, for callers that cannot
+ * allocate device memory (for example a latency-critical loop that must not
+ * pay for cudaMalloc's implicit device synchronisation, or a program whose
+ * device memory belongs to an allocator it cannot reach from this call site).
+ * The paper has no counterpart; it is a packaging of the split-over-keys path.
+ *
+ * The scratch is one device array inside this library, 24 MiB (25,165,824
+ * bytes), reserved on every GPU that loads the library until the process
+ * exits.  This call allocates nothing and calls no allocating routine.
+ *   - A shape whose split needs more than 24 MiB (fa_splitkv_workspace_size)
+ *     is rejected with FA_ERR_UNSUPPORTED before anything is launched; shapes
+ *     that are not split need no scratch and always run.  On a 152-SM GB300
+ *     every split of D = 64, and of D = 128 without the causal mask, fits
+ *     (at most about 20 MiB); the longest D = 128 causal splits (up to about
+ *     38 MiB, e.g. B = H = 1, S = 4096) are rejected.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (with it current); make that first call before any stream
+ *     capture on the device.
+ *   - Every call shares the array and it keeps the last call's contents.
+ *     Nothing in it has to start at zero: each call writes every partial
+ *     result it later reads.  Each device has its own copy; two calls on one
+ *     device whose work overlaps on the GPU (for example, issued on two
+ *     streams) race on it and give undefined results: order them on one
+ *     stream.
+ * Arguments, layouts and the other status codes are those of fa_fwd.
+ */
+int fa_fwd_splitkv_static(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                          int B, int H, int S, int D, int causal, float scale, int dtype,
+                          fa_stream_t stream);
+
 /* Static text for a status code (never NULL). */
 const char* fa_status_string(int status);
 

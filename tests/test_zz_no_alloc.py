@@ -1,0 +1,105 @@
+"""fa_fwd_splitkv_static: the split-over-keys path with its scratch in a
+device array inside the library, for callers that cannot allocate device
+memory themselves (for example a latency-critical loop that must not pay for
+cudaMalloc's implicit synchronisation, or code whose device memory belongs to
+an allocator it cannot reach).
+
+The test calls the entry point through the C-ABI and compares its output
+with fa_fwd_splitkv (caller-provided workspace) on the same inputs, within
+the parity tolerances, for two calls in a row with different inputs (the
+second call runs on the scratch the first one left behind).  It is collected
+last so that a failure here stops a `-x` run only after every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import fa_inputs
+
+from gpu_common import lse_tol, o_tol
+
+pytestmark = pytest.mark.gpu
+
+STATIC_BYTES = 24 << 20
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    fa.build()
+    lib = fa.library()
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_splitkv_static.restype = i
+    return lib
+
+
+def _inputs(B, H, S, D, dtype, seed):
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dtype, "stress", seed)
+    return tuple(fa_inputs.to_torch(x, dtype).cuda() for x in (qb, kb, vb))
+
+
+def _with_workspace(q, k, v, causal, scale, code):
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    B, S, H, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=q.device)
+    n = fa.fa_splitkv_workspace_size(B, H, S, D, causal)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    st = torch.cuda.current_stream().cuda_stream
+    rc = fa.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), B, H, S, D, causal, scale, code, ws.data_ptr(),
+                           ws.numel(), st)
+    assert rc == fa.FA_OK
+    return o, lse
+
+
+def _static(lib, q, k, v, causal, scale, code):
+    import torch
+    B, S, H, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=q.device)
+    rc = lib.fa_fwd_splitkv_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, S, D, int(causal), scale, code,
+                                   torch.cuda.current_stream().cuda_stream)
+    return rc, o, lse
+
+
+@pytest.mark.parametrize("B,H,S,D,dtype,causal", [
+    (1, 1, 4096, 64, "f16", False),
+    (1, 1, 4096, 64, "f16", True),
+    (1, 2, 2000, 128, "bf16", True),
+    (2, 3, 300, 64, "f16", False),
+])
+def test_static_scratch_matches_caller_workspace(lib, B, H, S, D, dtype, causal):
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    assert fa.fa_splitkv_workspace_size(B, H, S, D, causal) <= STATIC_BYTES
+    code = fa.FA_F16 if dtype == "f16" else fa.FA_BF16
+    scale = D ** -0.5
+    for call, seed in enumerate((101, 202)):     # two calls in a row
+        q, k, v = _inputs(B, H, S, D, dtype, seed + S)
+        o_ref, l_ref = _with_workspace(q, k, v, causal, scale, code)
+        rc, o, lse = _static(lib, q, k, v, causal, scale, code)
+        assert rc == fa.FA_OK, f"call {call}: status {rc}"
+        torch.cuda.synchronize()
+        O, Oref = o.double().cpu().numpy(), o_ref.double().cpu().numpy()
+        L, Lref = lse.double().cpu().numpy(), l_ref.double().cpu().numpy()
+        assert np.all(np.abs(O - Oref) <= o_tol(Oref, dtype)), f"call {call}: O differs"
+        assert np.all(np.abs(L - Lref) <= lse_tol(Lref)), f"call {call}: LSE differs"
+    assert fa.fa_device_status(clear=False) == fa.FA_OK
+
+
+def test_static_scratch_rejects_shapes_beyond_its_size(lib):
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    # a block-starved shape whose split needs more than the static array
+    B, H, S, D = 1, 1, 4096, 128
+    assert fa.fa_splitkv_workspace_size(B, H, S, D, True) > STATIC_BYTES
+    q = torch.zeros(B, S, H, D, dtype=torch.bfloat16, device="cuda")
+    rc, _, _ = _static(lib, q, q, q, True, D ** -0.5, fa.FA_BF16)
+    assert rc == fa.FA_ERR_UNSUPPORTED
