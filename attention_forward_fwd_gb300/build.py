@@ -7,6 +7,7 @@ repository root.
 from __future__ import annotations
 
 import os
+import re
 import shutil
 import subprocess
 
@@ -41,6 +42,35 @@ def needs_build() -> bool:
     return any(os.path.getmtime(d) > t for d in _sources())
 
 
+# Registers per thread the attention kernel must launch with: its warpgroups
+# re-split exactly this budget with setmaxnreg (fa_fwd_kernel.cuh, kLaunchRegs),
+# and a smaller launch budget would leave the increasing warpgroups waiting
+# for registers that never come.
+KERNEL_LAUNCH_REGS = 168
+
+
+def check_launch_registers(ptxas_log: str) -> None:
+    """Raise unless every fa_fwd_kernel instantiation uses KERNEL_LAUNCH_REGS."""
+    current = None
+    seen = 0
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current is not None:
+            if "fa_fwd_kernel" in current:
+                seen += 1
+                if int(m.group(1)) != KERNEL_LAUNCH_REGS:
+                    raise RuntimeError(
+                        f"{current} uses {m.group(1)} registers per thread, not "
+                        f"{KERNEL_LAUNCH_REGS}: its setmaxnreg split would not fit")
+            current = None
+    if seen == 0:
+        raise RuntimeError("no fa_fwd_kernel register report in the ptxas output")
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile the library if it is missing or older than its sources."""
     if not force and not needs_build():
@@ -56,6 +86,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
         f.write(" ".join(cmd) + "\n" + res.stdout + res.stderr)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stderr[-4000:]}")
+    try:
+        check_launch_registers(res.stdout + res.stderr)
+    except RuntimeError:
+        os.remove(tmp)
+        raise
     os.replace(tmp, LIB_PATH)
     if verbose:
         print(res.stderr)

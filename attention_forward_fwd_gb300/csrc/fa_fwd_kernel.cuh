@@ -15,9 +15,12 @@
 //              and runs the epilogue for its tile.
 //   warps 4-7  softmax group 1: query tile 1 (rows q0+128 .. q0+255).
 //   warp  8    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
-//              with tcgen05.mma, accumulators in TMEM; allocates TMEM.
+//              with tcgen05.mma, accumulators in TMEM; allocates TMEM.  With
+//              separate P (below) it issues for query tile 0 only and
+//   warp 10    issues for query tile 1.
 //   warp  9    TMA producer (one thread): Q tiles once, then K_j / V_j tiles
 //              through an NS-slot ring paced by full/empty mbarriers.
+//   warp 11    idle (completes the fourth warpgroup).
 // TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
 // O_0 [256,256+D), O_1 [256+D,256+2D).  P_t (16-bit, packed in pairs) is
 // written over the first 64 columns of S_t and read from there as the A
@@ -44,9 +47,19 @@ namespace fa {
 constexpr int kBM = 128;              // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;              // keys per tile
 constexpr int kQTiles = 2;            // query tiles per CTA
-constexpr int kThreads = 320;         // 8 softmax warps + MMA warp + TMA warp
-constexpr int kMmaWarp = 8;
+constexpr int kThreads = 384;         // 8 softmax warps, 2 MMA warps, TMA warp, 1 idle
+constexpr int kMmaWarp = 8;           // MMA issuer of query tile 0 (also allocates TMEM)
 constexpr int kLoadWarp = 9;
+constexpr int kMmaWarp1 = 10;         // MMA issuer of query tile 1
+// Register budget: the kernel launches with kLaunchRegs per thread (checked
+// against ptxas by the build); the two softmax warpgroups then take
+// kSoftmaxRegs and the control warpgroup (warps 8-11) gives back down to
+// kControlRegs.  256 * kSoftmaxRegs + 128 * kControlRegs == 384 * kLaunchRegs.
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kSoftmaxRegs = 224;
+constexpr uint32_t kControlRegs = 56;
+static_assert(256 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch budget");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kTauLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
@@ -105,9 +118,10 @@ struct Barriers {
     uint64_t kv_full[NS];
     uint64_t kv_empty[NS];
     uint64_t s_full[kQTiles];
+    uint64_t s_free[kQTiles];   // S_t read into registers (separate-P schedule)
     uint64_t p_full[kQTiles];
     uint64_t o_done[kQTiles];
-    uint64_t drain;
+    uint64_t drain[kQTiles];
     uint32_t tmem_base;
     int abort;
 };
@@ -161,6 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const FwdParams p) {
     using L = SmemLayout<D, NS>;
     constexpr int kChunks = D / 64;   // 128-byte column chunks per row (TMA box width)
+    // Separate-P schedule (when TMEM has room: 2*kBN + 2*D + 2*64 <= 512, i.e.
+    // D = 64): P_t gets its own 64 TMEM columns, so S_t of the next key tile
+    // can be computed as soon as the softmax has read S_t into registers,
+    // while P_t V of this tile is still pending.  Otherwise P_t is written
+    // over S_t and the next S_t waits for P_t V (same thread, in order).
+    constexpr bool kSepP = (2 * kBN + 2 * D + kQTiles * (kBN / 2)) <= static_cast<int>(kTmemCols);
+    constexpr int kPCol0 = kSepP ? (2 * kBN + 2 * D) : 0;   // P_0 column
+    constexpr int kPColStride = kSepP ? (kBN / 2) : kBN;     // P_1 - P_0
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -207,6 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkv1 = max(0, min(je, key_tiles_for(q0 + kBM, p.S, causal)) - jb);
     const int nkv = max(nkv0, nkv1);
     const bool partial = nsplit > 1;
+    // Order of the K / V tiles through the ring.  Aliased P: K0 V0 K1 V1 ...
+    // Separate P: K0 K1 V0 K2 V1 ... K(n-1) V(n-2) V(n-1), since S_t(j+1) is
+    // issued before P_t(j) V_j.
+    auto ring_k = [&](int j) { return kSepP ? (j == 0 ? 0 : 2 * j - 1) : 2 * j; };
+    auto ring_v = [&](int j) { return kSepP ? (j == nkv - 1 ? 2 * nkv - 1 : 2 * j + 2) : 2 * j + 1; };
 
     auto bar_addr = [&](const uint64_t* bptr) { return ptx::smem_addr(bptr); };
 
@@ -215,14 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar_addr(&bars->q_full), 1);
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(bar_addr(&bars->kv_full[s]), 1);
-            ptx::mbar_init(bar_addr(&bars->kv_empty[s]), 1);
+            ptx::mbar_init(bar_addr(&bars->kv_empty[s]), kSepP ? kQTiles : 1);   // one per MMA issuer
         }
         for (int t = 0; t < kQTiles; ++t) {
             ptx::mbar_init(bar_addr(&bars->s_full[t]), 1);
+            ptx::mbar_init(bar_addr(&bars->s_free[t]), kBM);
             ptx::mbar_init(bar_addr(&bars->p_full[t]), kBM);
             ptx::mbar_init(bar_addr(&bars->o_done[t]), 1);
+            ptx::mbar_init(bar_addr(&bars->drain[t]), 1);
         }
-        ptx::mbar_init(bar_addr(&bars->drain), 1);
         bars->abort = 0;
         ptx::fence_barrier_init();
     }
@@ -244,7 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // as every CTA of this grid is running; it waits for this grid to finish.
     ptx::launch_dependents();
 
-    if (warp == kLoadWarp) {
+    // Each warpgroup changes its register budget with one instruction that
+    // dominates all of its role code (ptxas allocates each region for it).
+    if (warp >= kMmaWarp) {
+        ptx::setmaxnreg_dec<kControlRegs>();
+        if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint32_t qbar = bar_addr(&bars->q_full);
@@ -267,8 +299,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 const uint32_t fb = bar_addr(&bars->kv_full[slot]);
                 ptx::mbar_arrive_expect_tx(fb, L::kKVBytes);
-                const CUtensorMap* m = (i & 1) ? &tmV : &tmK;
-                const int j = i >> 1;
+                bool is_v;
+                int j;
+                if (!kSepP) {
+                    is_v = (i & 1) != 0;
+                    j = i >> 1;
+                } else if (i == 0) {
+                    is_v = false;
+                    j = 0;
+                } else if (i == 2 * nkv - 1) {
+                    is_v = true;
+                    j = nkv - 1;
+                } else if (i & 1) {
+                    is_v = false;
+                    j = (i + 1) >> 1;
+                } else {
+                    is_v = true;
+                    j = (i - 2) >> 1;
+                }
+                const CUtensorMap* m = is_v ? &tmV : &tmK;
                 for (int c = 0; c < kChunks; ++c)
                     ptx::tma_load_4d(sbase + L::kOffKV + slot * L::kKVBytes + c * (kBN * 128), m, fb,
                                      c * 64, h, (jb + j) * kBN, b);
@@ -281,16 +330,112 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wait_phase(bar_addr(&bars->kv_full[i % NS]), (i / NS) & 1, abort_flag, false);
             }
         }
-    } else if (warp == kMmaWarp) {
-        // -------------------------------------------------------- MMA issuer
+    } else if (kSepP && (warp == kMmaWarp || warp == kMmaWarp1)) {
+        // ------------------------------------------- MMA issuers (separate P)
+        // One issuing thread per query tile, so that each tile's products
+        // wait only on its own softmax.  Both issuers see every K / V tile of
+        // the ring in the same order and release each slot once (a commit
+        // after the products that read it, or a plain arrive once it has
+        // landed when this tile has no work on it).
+        if (lane == 0) {
+            const int t = (warp == kMmaWarp) ? 0 : 1;
+            const int n_t = (t == 0) ? nkv0 : nkv1;
+            constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
+            constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, D, BF16, true);
+            auto full_bar = [&](int i) { return bar_addr(&bars->kv_full[i % NS]); };
+            auto full_par = [&](int i) { return static_cast<uint32_t>((i / NS) & 1); };
+            auto slot_addr = [&](int i) { return sbase + L::kOffKV + (i % NS) * L::kKVBytes; };
+            const uint32_t s_full = bar_addr(&bars->s_full[t]);
+            const uint32_t s_free = bar_addr(&bars->s_free[t]);
+            const uint32_t p_full = bar_addr(&bars->p_full[t]);
+            const uint32_t o_done = bar_addr(&bars->o_done[t]);
+
+            // S_t = Q_t K^T over D in K=16 steps; both operands K-major.
+            auto issue_s = [&](int ring) {
+                const uint64_t a0 = ptx::sdesc_sw128(sbase + L::kOffQ + t * L::kQBytes, 16, 1024);
+                const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t oa = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                    const uint32_t ob = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+                    ptx::mma_ss(tmem + t * kBN, a0 + (oa >> 4), b0 + (ob >> 4), kIdescQK, kk > 0);
+                }
+                ptx::tc_commit(s_full);
+                ptx::tc_commit(bar_addr(&bars->kv_empty[ring % NS]));
+            };
+            // O_t (+)= P_t V over the tile's keys in K=16 steps; P from TMEM,
+            // V MN-major (64-column chunks kBN*128 bytes apart).
+            auto issue_pv = [&](int ring, bool acc) {
+                const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), kBN * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + kPCol0 + t * kPColStride + kk * 8,
+                                b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                }
+                ptx::tc_commit(o_done);
+                ptx::tc_commit(bar_addr(&bars->kv_empty[ring % NS]));
+            };
+            // wait for item `ring` to land; release it at once when `use` is false
+            auto acquire = [&](int ring, bool use) {
+                if (!wait_phase(full_bar(ring), full_par(ring), abort_flag)) return false;
+                if (use) ptx::tc_fence_after_sync();
+                else ptx::mbar_arrive(bar_addr(&bars->kv_empty[ring % NS]));
+                return true;
+            };
+
+            bool ok = (n_t == 0) || wait_phase(bar_addr(&bars->q_full), 0, abort_flag);
+            if (ok) ok = acquire(ring_k(0), n_t > 0);
+            if (ok && n_t > 0) issue_s(ring_k(0));
+            for (int j = 0; ok && j < nkv; ++j) {
+                const bool next = (j + 1) < nkv;
+                if constexpr (kSepP) {
+                    // S_t(j+1) as soon as the softmax holds S_t(j), then P_t V(j)
+                    if (next) {
+                        const bool use = (j + 1) < n_t;
+                        if (!(ok = acquire(ring_k(j + 1), use))) break;
+                        if (use) {
+                            if (!(ok = wait_phase(s_free, j & 1, abort_flag))) break;
+                            ptx::tc_fence_after_sync();
+                            issue_s(ring_k(j + 1));
+                        }
+                    }
+                    if (!(ok = acquire(ring_v(j), j < n_t))) break;
+                    if (j < n_t) {
+                        if (!(ok = wait_phase(p_full, j & 1, abort_flag))) break;
+                        ptx::tc_fence_after_sync();
+                        issue_pv(ring_v(j), j > 0);
+                    }
+                } else {
+                    // P_t V(j) first: S_t(j+1) overwrites P_t, which it reads
+                    if (!(ok = acquire(ring_v(j), j < n_t))) break;
+                    if (j < n_t) {
+                        if (!(ok = wait_phase(p_full, j & 1, abort_flag))) break;
+                        ptx::tc_fence_after_sync();
+                        issue_pv(ring_v(j), j > 0);
+                    }
+                    if (next) {
+                        const bool use = (j + 1) < n_t;
+                        if (!(ok = acquire(ring_k(j + 1), use))) break;
+                        if (use) issue_s(ring_k(j + 1));
+                    }
+                }
+            }
+            // Every MMA of this issuer must be complete before TMEM is freed.
+            ptx::tc_commit(bar_addr(&bars->drain[t]));
+            wait_phase(bar_addr(&bars->drain[t]), 0, abort_flag, false);
+        }
+    } else if (!kSepP && warp == kMmaWarp) {
+        // ----------------------------------------------- MMA issuer (P over S)
+        // One thread issues both tiles' products in the order
+        //   S0(0) S1(0) | P0V(j) S0(j+1) P1V(j) S1(j+1) | ...
+        // so that one tile's softmax runs while the other tile's products do;
+        // S_t(j+1) follows P_t V(j), which reads the P_t it overwrites.
         if (lane == 0) {
             constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
             constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, D, BF16, true);
             auto full_bar = [&](int i) { return bar_addr(&bars->kv_full[i % NS]); };
             auto full_par = [&](int i) { return static_cast<uint32_t>((i / NS) & 1); };
             auto slot_addr = [&](int i) { return sbase + L::kOffKV + (i % NS) * L::kKVBytes; };
-
-            // S_t = Q_t K^T over D in K=16 steps; both operands K-major.
             auto issue_s = [&](int t, int ring) {
                 const uint64_t a0 = ptx::sdesc_sw128(sbase + L::kOffQ + t * L::kQBytes, 16, 1024);
                 const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), 16, 1024);
@@ -300,32 +445,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t ob = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
                     ptx::mma_ss(tmem + t * kBN, a0 + (oa >> 4), b0 + (ob >> 4), kIdescQK, kk > 0);
                 }
+                ptx::tc_commit(bar_addr(&bars->s_full[t]));
             };
-            // O_t (+)= P_t V over the tile's keys in K=16 steps; P from TMEM,
-            // V MN-major (64-column chunks kBN*128 bytes apart).
             auto issue_pv = [&](int t, int ring, bool acc) {
                 const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), kBN * 128, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + t * kBN + kk * 8,
+                    ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + kPCol0 + t * kPColStride + kk * 8,
                                 b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
+                ptx::tc_commit(bar_addr(&bars->o_done[t]));
             };
 
             bool ok = wait_phase(bar_addr(&bars->q_full), 0, abort_flag);
-            if (ok) ok = wait_phase(full_bar(0), full_par(0), abort_flag);
+            if (ok) ok = wait_phase(full_bar(ring_k(0)), full_par(ring_k(0)), abort_flag);
             if (ok) {
                 ptx::tc_fence_after_sync();
-                for (int t = 0; t < kQTiles; ++t) {
-                    if ((t == 0 ? nkv0 : nkv1) == 0) continue;
-                    issue_s(t, 0);
-                    ptx::tc_commit(bar_addr(&bars->s_full[t]));
-                }
-                ptx::tc_commit(bar_addr(&bars->kv_empty[0]));
+                if (nkv0 > 0) issue_s(0, ring_k(0));
+                if (nkv1 > 0) issue_s(1, ring_k(0));
+                ptx::tc_commit(bar_addr(&bars->kv_empty[ring_k(0) % NS]));
             }
             for (int j = 0; ok && j < nkv; ++j) {
-                const int iv = 2 * j + 1;
-                const int ik = 2 * j + 2;
+                const int iv = ring_v(j);
+                const int ik = ring_k(j + 1);
                 const bool next = (j + 1) < nkv;
                 if (!(ok = wait_phase(full_bar(iv), full_par(iv), abort_flag))) break;
                 ptx::tc_fence_after_sync();
@@ -333,34 +475,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_phase(bar_addr(&bars->p_full[0]), j & 1, abort_flag))) break;
                     ptx::tc_fence_after_sync();
                     issue_pv(0, iv, j > 0);
-                    ptx::tc_commit(bar_addr(&bars->o_done[0]));
                 }
                 if (next) {
                     if (!(ok = wait_phase(full_bar(ik), full_par(ik), abort_flag))) break;
                     ptx::tc_fence_after_sync();
                 }
-                if (j + 1 < nkv0) {
-                    issue_s(0, ik);
-                    ptx::tc_commit(bar_addr(&bars->s_full[0]));
-                }
+                if (j + 1 < nkv0) issue_s(0, ik);
                 if (j < nkv1) {
                     if (!(ok = wait_phase(bar_addr(&bars->p_full[1]), j & 1, abort_flag))) break;
                     ptx::tc_fence_after_sync();
                     issue_pv(1, iv, j > 0);
-                    ptx::tc_commit(bar_addr(&bars->o_done[1]));
                 }
                 ptx::tc_commit(bar_addr(&bars->kv_empty[iv % NS]));
-                if (j + 1 < nkv1) {
-                    issue_s(1, ik);
-                    ptx::tc_commit(bar_addr(&bars->s_full[1]));
-                }
+                if (j + 1 < nkv1) issue_s(1, ik);
                 if (next) ptx::tc_commit(bar_addr(&bars->kv_empty[ik % NS]));
             }
             // Every MMA must be complete before TMEM is freed.
-            ptx::tc_commit(bar_addr(&bars->drain));
-            wait_phase(bar_addr(&bars->drain), 0, abort_flag, false);
+            ptx::tc_commit(bar_addr(&bars->drain[0]));
+            wait_phase(bar_addr(&bars->drain[0]), 0, abort_flag, false);
         }
+    }
     } else {
+        ptx::setmaxnreg_inc<kSoftmaxRegs>();
         // ----------------------------------------------------- softmax groups
         const int t = warp >> 2;                 // query tile of this group
         const int wq = warp & 3;                 // lane quarter of TMEM
@@ -368,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + t * kBN;
         const uint32_t tO = tmem + lane_off + 2 * kBN + t * D;
+        const uint32_t tP = tmem + lane_off + kPCol0 + t * kPColStride;
         const int r0 = q0 + t * kBM;
         const int row = r0 + r;
         const float c = p.scale_log2;
@@ -385,6 +522,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < kBN / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
             ptx::tmem_ld_wait();
             ptx::reg_fence<kBN>(s);
+            if constexpr (kSepP) {
+                // S_t is in registers: the next S_t may overwrite it
+                ptx::tc_fence_before_sync();
+                ptx::mbar_arrive(bar_addr(&bars->s_free[t]));
+            }
 
             const int kv0 = (jb + j) * kBN;
             // Mask keys past the end and, on diagonal tiles, keys after the row.
@@ -396,7 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int k = 0; k < kBN; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(s[k]));
+            for (int k = 0; k < kBN / 2; ++k)
+                mx[k & 3] = ptx::fmax3(mx[k & 3], __uint_as_float(s[2 * k]),
+                                       __uint_as_float(s[2 * k + 1]));
             const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             const float m_new = fmaxf(m_use, m_tile);
             // Lazy rescale: keep the old reference unless the max grew by more
@@ -409,23 +553,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
 
-            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+            // p = 2^(s*c - m*c), two columns per packed FMA / add
+            const float2 c2 = make_float2(c, c);
+            const float2 nmc2 = make_float2(-mc, -mc);
+            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int q = 0; q < kBN / 32; ++q) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[q * 32 + 2 * k]), c, -mc));
-                    const float p1 =
-                        ptx::ex2_approx(fmaf(__uint_as_float(s[q * 32 + 2 * k + 1]), c, -mc));
-                    sum[k & 3] += p0 + p1;
-                    pk[k] = pack2<BF16>(p0, p1);
+                    const float2 x = __ffma2_rn(
+                        make_float2(__uint_as_float(s[q * 32 + 2 * k]),
+                                    __uint_as_float(s[q * 32 + 2 * k + 1])),
+                        c2, nmc2);
+                    const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+                    sum2[k & 1] = __fadd2_rn(sum2[k & 1], pp);
+                    pk[k] = pack2<BF16>(pp.x, pp.y);
                 }
-                ptx::tmem_st_32x32b_x16(tS + q * 16, pk);
+                if (kSepP && q == 0 && j > 0) {
+                    // P_t and O_t are still read / written by P_t V of tile j-1
+                    ok = wait_phase(bar_addr(&bars->o_done[t]), (j - 1) & 1, abort_flag);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                }
+                ptx::tmem_st_32x32b_x16(tP + q * 16, pk);
             }
-            l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+            if (!ok) break;
+            const float2 sum = __fadd2_rn(sum2[0], sum2[1]);
+            l = l * alpha + (sum.x + sum.y);
 
-            // O_t was last written by P V of tile j-1, which completed before
+            // O_t was last written by P V of tile j-1: with separate P its
+            // completion was awaited above; with P over S it completed before
             // S_t of tile j (same issuing thread, in order).
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
