@@ -42,15 +42,24 @@ def needs_build() -> bool:
     return any(os.path.getmtime(d) > t for d in _sources())
 
 
-# Registers per thread the attention kernel must launch with: its warpgroups
-# re-split exactly this budget with setmaxnreg (fa_fwd_kernel.cuh, kLaunchRegs),
-# and a smaller launch budget would leave the increasing warpgroups waiting
-# for registers that never come.
-KERNEL_LAUNCH_REGS = 168
+# Registers per thread the attention kernel must launch with, by its last
+# template argument (softmax threads per row): its warpgroups re-split this
+# budget with setmaxnreg (fa_fwd_kernel.cuh, WarpLayout::kLaunchRegs), and a
+# smaller launch budget would leave the increasing warpgroups waiting for
+# registers that never come.
+KERNEL_LAUNCH_REGS = {1: 168, 2: 96}
+
+
+def _expected_regs(mangled: str) -> int:
+    m = re.search(r"fa_fwd_kernelILi\d+ELb[01]ELi\d+ELi(\d+)EE", mangled)
+    if not m:
+        raise RuntimeError(f"cannot read the template arguments of {mangled}")
+    return KERNEL_LAUNCH_REGS[int(m.group(1))]
 
 
 def check_launch_registers(ptxas_log: str) -> None:
-    """Raise unless every fa_fwd_kernel instantiation uses KERNEL_LAUNCH_REGS."""
+    """Raise unless every fa_fwd_kernel instantiation launches with the
+    register count its setmaxnreg split assumes."""
     current = None
     seen = 0
     for line in ptxas_log.splitlines():
@@ -62,10 +71,11 @@ def check_launch_registers(ptxas_log: str) -> None:
         if m and current is not None:
             if "fa_fwd_kernel" in current:
                 seen += 1
-                if int(m.group(1)) != KERNEL_LAUNCH_REGS:
+                want = _expected_regs(current)
+                if int(m.group(1)) != want:
                     raise RuntimeError(
                         f"{current} uses {m.group(1)} registers per thread, not "
-                        f"{KERNEL_LAUNCH_REGS}: its setmaxnreg split would not fit")
+                        f"{want}: its setmaxnreg split would not fit")
             current = None
     if seen == 0:
         raise RuntimeError("no fa_fwd_kernel register report in the ptxas output")

@@ -56,6 +56,16 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int B, int S, int H, 
     return r == CUDA_SUCCESS;
 }
 
+// softmax threads per query row, per head dimension
+#ifndef FA_ROW_SPLIT_D64
+#define FA_ROW_SPLIT_D64 1
+#endif
+#ifndef FA_ROW_SPLIT_D128
+#define FA_ROW_SPLIT_D128 2
+#endif
+constexpr int kRowSplitD64 = FA_ROW_SPLIT_D64;
+constexpr int kRowSplitD128 = FA_ROW_SPLIT_D128;
+
 int num_sms() {
     static int cached[64] = {0};
     int dev = 0;
@@ -115,11 +125,11 @@ size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D) {
     return slots * (static_cast<size_t>(fa::kBM) * D + 2 * fa::kBM) * sizeof(float);
 }
 
-template <int D, bool BF16, int NS>
+template <int D, bool BF16, int NS, int RS>
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int S,
            int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace) {
-    auto kern = fa::fa_fwd_kernel<D, BF16, NS>;
-    constexpr int kSmem = fa::SmemLayout<D, NS>::kAlloc;
+    auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS>;
+    constexpr int kSmem = fa::SmemLayout<D, NS, RS>::kAlloc;
     // The dynamic shared-memory opt-in is per device; remember it per device.
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
@@ -153,7 +163,7 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.ws_ml = plan.chunk ? static_cast<float*>(workspace) + o_floats : nullptr;
     const dim3 grid(static_cast<unsigned>(B) * static_cast<unsigned>(H),
                     static_cast<unsigned>(plan.ctas_per_head));
-    kern<<<grid, fa::kThreads, kSmem, stream>>>(mq, mk, mv, mo, p);
+    kern<<<grid, fa::Roles<RS>::kThreads, kSmem, stream>>>(mq, mk, mv, mo, p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     if (plan.chunk == 0) return FA_OK;
 
@@ -196,12 +206,15 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
 int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int S,
              int D, int causal, float scale, int dtype, cudaStream_t st, const SplitPlan& plan,
              void* ws) {
+    // <head dim, bf16, K/V ring slots, softmax threads per query row>
     if (dtype == FA_F16) {
-        if (D == 64) return launch<64, false, 6>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
-        return launch<128, false, 4>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+        if (D == 64)
+            return launch<64, false, 6, kRowSplitD64>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+        return launch<128, false, 4, kRowSplitD128>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
     }
-    if (D == 64) return launch<64, true, 6>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
-    return launch<128, true, 4>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+    if (D == 64)
+        return launch<64, true, 6, kRowSplitD64>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+    return launch<128, true, 4, kRowSplitD128>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
 }
 
 }  // namespace

@@ -9,18 +9,22 @@
 // on the raw scores and the positive scale folded in afterwards (same
 // section, last paragraph), as exp2 with scale*log2(e) folded into one FMA.
 //
-// How it maps onto one GB300 SM (one CTA per SM, 320 threads):
-//   warps 0-3  softmax group 0: query tile 0 (rows q0 .. q0+127), thread =
-//              row = TMEM lane.  Also rescales O in TMEM when its max moves
-//              and runs the epilogue for its tile.
-//   warps 4-7  softmax group 1: query tile 1 (rows q0+128 .. q0+255).
-//   warp  8    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
-//              with tcgen05.mma, accumulators in TMEM; allocates TMEM.  With
-//              separate P (below) it issues for query tile 0 only and
-//   warp 10    issues for query tile 1.
-//   warp  9    TMA producer (one thread): Q tiles once, then K_j / V_j tiles
-//              through an NS-slot ring paced by full/empty mbarriers.
-//   warp 11    idle (completes the fourth warpgroup).
+// How it maps onto one GB300 SM (one CTA per SM; RS softmax threads per
+// query row, RS = 1 or 2, 128*(2*RS+1) threads):
+//   warps [0, 4RS)     softmax for query tile 0 (rows q0 .. q0+127): each row
+//                      (a TMEM lane) is handled by RS threads, one per 128/RS
+//                      score columns.  They also rescale O in TMEM when the
+//                      row max moves and run the epilogue of the tile.
+//   warps [4RS, 8RS)   the same for query tile 1 (rows q0+128 .. q0+255).
+//   warp  8RS          MMA issuer (one thread): S_t = Q_t K_j^T and
+//                      O_t += P_t V_j with tcgen05.mma, accumulators in TMEM;
+//                      allocates TMEM.  With separate P (below) it issues for
+//                      query tile 0 only and
+//   warp  8RS+2        issues for query tile 1.
+//   warp  8RS+1        TMA producer (one thread): Q tiles once, then K_j / V_j
+//                      tiles through an NS-slot ring paced by full/empty
+//                      mbarriers.
+//   warp  8RS+3        idle (completes the control warpgroup).
 // TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
 // O_0 [256,256+D), O_1 [256+D,256+2D).  P_t (16-bit, packed in pairs) is
 // written over the first 64 columns of S_t and read from there as the A
@@ -47,19 +51,41 @@ namespace fa {
 constexpr int kBM = 128;              // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;              // keys per tile
 constexpr int kQTiles = 2;            // query tiles per CTA
-constexpr int kThreads = 384;         // 8 softmax warps, 2 MMA warps, TMA warp, 1 idle
-constexpr int kMmaWarp = 8;           // MMA issuer of query tile 0 (also allocates TMEM)
-constexpr int kLoadWarp = 9;
-constexpr int kMmaWarp1 = 10;         // MMA issuer of query tile 1
+// Warp roles for RS softmax threads per query row (RS = 1: one thread per
+// row; RS = 2: each row split into two column halves).  Warps [0, 8*RS) run
+// the softmax, the last warpgroup holds the MMA issuers and the TMA producer.
 // Register budget: the kernel launches with kLaunchRegs per thread (checked
-// against ptxas by the build); the two softmax warpgroups then take
-// kSoftmaxRegs and the control warpgroup (warps 8-11) gives back down to
-// kControlRegs.  256 * kSoftmaxRegs + 128 * kControlRegs == 384 * kLaunchRegs.
-constexpr uint32_t kLaunchRegs = 168;
-constexpr uint32_t kSoftmaxRegs = 224;
-constexpr uint32_t kControlRegs = 56;
-static_assert(256 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
-              "register split exceeds the launch budget");
+// against ptxas by the build); the softmax warpgroups then take kSoftmaxRegs
+// and the control warpgroup gives back down to kControlRegs, within the
+// launch total.
+template <int RS>
+struct WarpLayout;
+template <>
+struct WarpLayout<1> {
+    static constexpr int kSoftmaxWarps = 8;
+    static constexpr uint32_t kLaunchRegs = 168;
+    static constexpr uint32_t kSoftmaxRegs = 224;
+    static constexpr uint32_t kControlRegs = 56;
+};
+template <>
+struct WarpLayout<2> {
+    static constexpr int kSoftmaxWarps = 16;
+    static constexpr uint32_t kLaunchRegs = 96;
+    static constexpr uint32_t kSoftmaxRegs = 104;
+    static constexpr uint32_t kControlRegs = 56;
+};
+template <int RS>
+struct Roles : WarpLayout<RS> {
+    using B = WarpLayout<RS>;
+    static constexpr int kThreads = 32 * B::kSoftmaxWarps + 128;
+    static constexpr int kMmaWarp = B::kSoftmaxWarps;       // MMA issuer, tile 0; TMEM alloc
+    static constexpr int kLoadWarp = B::kSoftmaxWarps + 1;  // TMA producer
+    static constexpr int kMmaWarp1 = B::kSoftmaxWarps + 2;  // MMA issuer, tile 1
+    static constexpr int kTileThreads = 128 * RS;           // softmax threads per query tile
+    static_assert(32u * B::kSoftmaxWarps * B::kSoftmaxRegs + 128u * B::kControlRegs <=
+                      kThreads * B::kLaunchRegs,
+                  "register split exceeds the launch budget");
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr float kTauLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
@@ -112,7 +138,7 @@ __host__ __device__ inline int key_tiles_for_block(int qb, int S, bool causal) {
     return n;
 }
 
-template <int NS>
+template <int NS, int RS>
 struct Barriers {
     uint64_t q_full;
     uint64_t kv_full[NS];
@@ -124,16 +150,20 @@ struct Barriers {
     uint64_t drain[kQTiles];
     uint32_t tmem_base;
     int abort;
+    // the RS threads of a row swap partial row maxima (double-buffered over
+    // key tiles) and, at the end, partial row sums
+    float row_max[2][kQTiles][RS][kBM];
+    float row_sum[kQTiles][RS][kBM];
 };
 
-template <int D, int NS>
+template <int D, int NS, int RS>
 struct SmemLayout {
     static constexpr int kQBytes = kBM * D * 2;
     static constexpr int kKVBytes = kBN * D * 2;
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQTiles * kQBytes;
     static constexpr int kOffBar = kOffKV + NS * kKVBytes;
-    static constexpr int kBytes = kOffBar + static_cast<int>(sizeof(Barriers<NS>));
+    static constexpr int kBytes = kOffBar + static_cast<int>(sizeof(Barriers<NS, RS>));
     static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024
 };
 
@@ -168,12 +198,18 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-template <int D, bool BF16, int NS>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool BF16, int NS, int RS>
+__global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const FwdParams p) {
-    using L = SmemLayout<D, NS>;
+    using L = SmemLayout<D, NS, RS>;
+    using R = Roles<RS>;
+    constexpr int kRowSplit = RS;
+    constexpr int kMmaWarp = R::kMmaWarp;
+    constexpr int kLoadWarp = R::kLoadWarp;
+    constexpr int kMmaWarp1 = R::kMmaWarp1;
+    constexpr int kTileThreads = R::kTileThreads;
     constexpr int kChunks = D / 64;   // 128-byte column chunks per row (TMA box width)
     // Separate-P schedule (when TMEM has room: 2*kBN + 2*D + 2*64 <= 512, i.e.
     // D = 64): P_t gets its own 64 TMEM columns, so S_t of the next key tile
@@ -183,11 +219,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kSepP = (2 * kBN + 2 * D + kQTiles * (kBN / 2)) <= static_cast<int>(kTmemCols);
     constexpr int kPCol0 = kSepP ? (2 * kBN + 2 * D) : 0;   // P_0 column
     constexpr int kPColStride = kSepP ? (kBN / 2) : kBN;     // P_1 - P_0
+    // Each of the kRowSplit threads of a row writes the packed P of its
+    // kBN/kRowSplit keys as kBN/(2*kRowSplit) columns: contiguous in the
+    // separate region, over the start of its own S columns otherwise.
+    constexpr int kPHalfStride = kSepP ? (kBN / (2 * kRowSplit)) : (kBN / kRowSplit);
+    constexpr int kStepsPerHalf = (kBN / kRowSplit) / 16;   // K=16 steps per half
+    // TMEM column of the A operand (P_t) for K step kk of P_t V
+    auto p_col = [](int t, int kk) {
+        return kPCol0 + t * kPColStride + (kk / kStepsPerHalf) * kPHalfStride + (kk % kStepsPerHalf) * 8;
+    };
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = ptx::smem_addr(smem);
-    Barriers<NS>* bars = reinterpret_cast<Barriers<NS>*>(smem + L::kOffBar);
+    Barriers<NS, RS>* bars = reinterpret_cast<Barriers<NS, RS>*>(smem + L::kOffBar);
     volatile int* abort_flag = &bars->abort;
 
     const int warp = threadIdx.x >> 5;
@@ -246,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < kQTiles; ++t) {
             ptx::mbar_init(bar_addr(&bars->s_full[t]), 1);
-            ptx::mbar_init(bar_addr(&bars->s_free[t]), kBM);
-            ptx::mbar_init(bar_addr(&bars->p_full[t]), kBM);
+            ptx::mbar_init(bar_addr(&bars->s_free[t]), kTileThreads);
+            ptx::mbar_init(bar_addr(&bars->p_full[t]), kTileThreads);
             ptx::mbar_init(bar_addr(&bars->o_done[t]), 1);
             ptx::mbar_init(bar_addr(&bars->drain[t]), 1);
         }
@@ -275,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Each warpgroup changes its register budget with one instruction that
     // dominates all of its role code (ptxas allocates each region for it).
     if (warp >= kMmaWarp) {
-        ptx::setmaxnreg_dec<kControlRegs>();
+        ptx::setmaxnreg_dec<R::kControlRegs>();
         if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -369,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), kBN * 128, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + kPCol0 + t * kPColStride + kk * 8,
+                    ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + p_col(t, kk),
                                 b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
                 ptx::tc_commit(o_done);
@@ -451,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), kBN * 128, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + kPCol0 + t * kPColStride + kk * 8,
+                    ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + p_col(t, kk),
                                 b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
                 ptx::tc_commit(bar_addr(&bars->o_done[t]));
@@ -496,55 +541,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     } else {
-        ptx::setmaxnreg_inc<kSoftmaxRegs>();
+        ptx::setmaxnreg_inc<R::kSoftmaxRegs>();
         // ----------------------------------------------------- softmax groups
-        const int t = warp >> 2;                 // query tile of this group
-        const int wq = warp & 3;                 // lane quarter of TMEM
-        const int r = wq * 32 + lane;            // row within the tile
+        // Warp w works on query tile t = w / (4 RS), score columns
+        // [hf*128/RS, (hf+1)*128/RS) of each key tile (hf = (w / 4) % RS),
+        // rows 32*wq .. 32*wq+31 of the tile (wq = w % 4, the TMEM lane
+        // quarter it may access).  With RS = 2 the two threads of a row swap
+        // their partial maxima every key tile, so both keep the same reference
+        // max; each keeps its own partial row sum.  On an abort every warp
+        // still runs every swap barrier (with no TMEM work), so the barriers
+        // cannot hang.
+        constexpr int kHalf = kBN / kRowSplit;      // score columns per thread
+        constexpr int kDH = D / kRowSplit;          // O columns per thread
+        const int t = warp / (4 * kRowSplit);
+        const int hf = (warp >> 2) % kRowSplit;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;               // row within the tile
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_off + t * kBN;
-        const uint32_t tO = tmem + lane_off + 2 * kBN + t * D;
-        const uint32_t tP = tmem + lane_off + kPCol0 + t * kPColStride;
+        const uint32_t tS = tmem + lane_off + t * kBN + hf * kHalf;
+        const uint32_t tO = tmem + lane_off + 2 * kBN + t * D + hf * kDH;
+        // P: kHalf/2 packed columns per thread, in the separate P region or
+        // over the first kHalf/2 columns of this thread's own part of S_t
+        const uint32_t tP = tmem + lane_off +
+                            (kSepP ? (kPCol0 + t * kPColStride + hf * (kHalf / 2)) : (t * kBN + hf * kHalf));
+        const uint32_t pair_bar = 1 + t * 4 + wq;   // the RS warps sharing these rows
+        const uint32_t tile_bar = 1 + 4 * kQTiles + t;
         const int r0 = q0 + t * kBM;
         const int row = r0 + r;
         const float c = p.scale_log2;
         const int n_tiles = (t == 0) ? nkv0 : nkv1;
 
         float m_use = -INFINITY;   // reference max, raw (unscaled) score units
-        float l = 0.f;
+        float l = 0.f;             // this thread's part of the row sum
         bool ok = true;
+        // After an abort, one thread per row simply leaves the loop; with the
+        // row split, a warp keeps running its loop without TMEM stores or
+        // arrivals instead, so that the swap barriers stay matched.
+        constexpr bool kBreakOnAbort = (kRowSplit == 1);
         for (int j = 0; j < n_tiles; ++j) {
-            ok = wait_phase(bar_addr(&bars->s_full[t]), j & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            ok = (kBreakOnAbort || ok) && wait_phase(bar_addr(&bars->s_full[t]), j & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (kBreakOnAbort && !ok) break;
             ptx::tc_fence_after_sync();
-            uint32_t s[kBN];
+            uint32_t s[kHalf];
 #pragma unroll
-            for (int q = 0; q < kBN / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
+            for (int q = 0; q < kHalf / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
             ptx::tmem_ld_wait();
-            ptx::reg_fence<kBN>(s);
-            if constexpr (kSepP) {
+            ptx::reg_fence<kHalf>(s);
+            if (kSepP && (kBreakOnAbort || ok)) {
                 // S_t is in registers: the next S_t may overwrite it
                 ptx::tc_fence_before_sync();
                 ptx::mbar_arrive(bar_addr(&bars->s_free[t]));
             }
 
-            const int kv0 = (jb + j) * kBN;
+            const int kv0 = (jb + j) * kBN + hf * kHalf;   // key of column 0
             // Mask keys past the end and, on diagonal tiles, keys after the row.
-            if (kv0 + kBN > p.S || (p.causal && kv0 + kBN - 1 > r0)) {
+            if (kv0 + kHalf > p.S || (p.causal && kv0 + kHalf - 1 > r0)) {
                 const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
 #pragma unroll
-                for (int k = 0; k < kBN; ++k)
+                for (int k = 0; k < kHalf; ++k)
                     if (kv0 + k > last) s[k] = __float_as_uint(-INFINITY);
             }
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int k = 0; k < kBN / 2; ++k)
+            for (int k = 0; k < kHalf / 2; ++k)
                 mx[k & 3] = ptx::fmax3(mx[k & 3], __uint_as_float(s[2 * k]),
                                        __uint_as_float(s[2 * k + 1]));
-            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            if constexpr (kRowSplit > 1) {
+                bars->row_max[j & 1][t][hf][r] = m_tile;
+                ptx::named_barrier_sync(pair_bar, 32 * kRowSplit);
+                m_tile = fmaxf(m_tile, bars->row_max[j & 1][t][hf ^ 1][r]);
+            }
             const float m_new = fmaxf(m_use, m_tile);
             // Lazy rescale: keep the old reference unless the max grew by more
-            // than kTauLog2 in log2 units (then p <= 2^kTauLog2).
+            // than kTauLog2 in log2 units (then p <= 2^kTauLog2).  The RS
+            // threads of a row see the same maxima, so they decide alike.
             const bool rescale = (m_new - m_use) * c > kTauLog2;
             float alpha = 1.f;
             if (rescale) {
@@ -558,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 nmc2 = make_float2(-mc, -mc);
             float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int q = 0; q < kBN / 32; ++q) {
+            for (int q = 0; q < kHalf / 32; ++q) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
@@ -570,27 +642,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sum2[k & 1] = __fadd2_rn(sum2[k & 1], pp);
                     pk[k] = pack2<BF16>(pp.x, pp.y);
                 }
-                if (kSepP && q == 0 && j > 0) {
+                if (kSepP && q == 0 && j > 0 && ok) {
                     // P_t and O_t are still read / written by P_t V of tile j-1
                     ok = wait_phase(bar_addr(&bars->o_done[t]), (j - 1) & 1, abort_flag);
-                    if (!__all_sync(0xffffffffu, ok)) {
-                        ok = false;
-                        break;
-                    }
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (kBreakOnAbort && !ok) break;
                     ptx::tc_fence_after_sync();
                 }
-                ptx::tmem_st_32x32b_x16(tP + q * 16, pk);
+                if (kBreakOnAbort || ok) ptx::tmem_st_32x32b_x16(tP + q * 16, pk);
             }
-            if (!ok) break;
+            if (kBreakOnAbort && !ok) break;
             const float2 sum = __fadd2_rn(sum2[0], sum2[1]);
             l = l * alpha + (sum.x + sum.y);
 
             // O_t was last written by P V of tile j-1: with separate P its
             // completion was awaited above; with P over S it completed before
             // S_t of tile j (same issuing thread, in order).
-            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+            if ((kBreakOnAbort || ok) && j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
+                for (int q = 0; q < kDH / 32; ++q) {
                     uint32_t o[32];
                     ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
                     ptx::tmem_ld_wait();
@@ -600,94 +670,101 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_st_32x32b_x32(tO + q * 32, o);
                 }
             }
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(bar_addr(&bars->p_full[t]));
+            if (kBreakOnAbort || ok) {
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before_sync();
+                ptx::mbar_arrive(bar_addr(&bars->p_full[t]));
+            }
         }
 
-        if (partial) {
-            // ------------------------------------ epilogue: partial result
-            // o~ stays unnormalised (fp32); m and l go beside it.  A query
-            // tile that saw no key of this split records l = 0.
-            if (r0 < p.S) {
+        if (r0 < p.S) {
+            // --------------------------------------------------- epilogues
+            bool eok = ok;
+            if (n_tiles > 0)
+                eok = eok && wait_phase(bar_addr(&bars->o_done[t]), (n_tiles - 1) & 1, abort_flag);
+            eok = __all_sync(0xffffffffu, eok);
+            // whole-row sum from the RS parts
+            float l_row = l;
+            if constexpr (kRowSplit > 1) {
+                bars->row_sum[t][hf][r] = l;
+                ptx::named_barrier_sync(pair_bar, 32 * kRowSplit);
+                l_row = l + bars->row_sum[t][hf ^ 1][r];
+            }
+            if (partial) {
+                // partial result: o~ stays unnormalised (fp32), m and l go
+                // beside it; a tile that saw no key of this split records l = 0
                 const int ntq = (p.S + kBM - 1) / kBM;
                 const size_t slot = partial_slot(bh, ntq, r0 / kBM, p.max_splits, split);
                 float* ml = p.ws_ml + slot * (2 * kBM);
                 float4* po = reinterpret_cast<float4*>(p.ws_o + slot * static_cast<size_t>(kBM * D));
-                bool eok = ok;
-                if (n_tiles > 0)
-                    eok = eok && wait_phase(bar_addr(&bars->o_done[t]), (n_tiles - 1) & 1, abort_flag);
-                eok = __all_sync(0xffffffffu, eok);
                 if (eok && n_tiles > 0) {
                     ptx::tc_fence_after_sync();
 #pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
+                    for (int q = 0; q < kDH / 32; ++q) {
                         uint32_t o[32];
                         ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
                         ptx::tmem_ld_wait();
                         ptx::reg_fence<32>(o);
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
-                            po[(q * 8 + u) * kBM + r] =
+                            po[(hf * (kDH / 4) + q * 8 + u) * kBM + r] =
                                 make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
                                             __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]));
                     }
-                    ml[r] = m_use * c;
-                    ml[kBM + r] = l;
-                } else if (eok) {
+                    if (hf == 0) {
+                        ml[r] = m_use * c;
+                        ml[kBM + r] = l_row;
+                    }
+                } else if (eok && hf == 0) {
                     ml[r] = -INFINITY;
                     ml[kBM + r] = 0.f;
                 }
-            }
-        } else if (n_tiles > 0) {
-            // ---------------------------------------------------- epilogue
-            // Every warp of the group reaches the named barrier below exactly
-            // once, whether or not it aborted, so the barrier cannot hang.
-            bool eok = ok && wait_phase(bar_addr(&bars->o_done[t]), (n_tiles - 1) & 1, abort_flag);
-            eok = __all_sync(0xffffffffu, eok);
-            // Stage O_t in this tile's Q buffer (no longer read by any MMA),
-            // laid out as the 128-byte-swizzled TMA box.
-            uint8_t* stage = smem + L::kOffQ + t * L::kQBytes;
-            const float inv_l = 1.f / l;
-            if (eok) {
-                ptx::tc_fence_after_sync();
+            } else if (n_tiles > 0) {
+                // final result: stage O_t in this tile's Q buffer (no longer
+                // read by any MMA) as the 128-byte-swizzled TMA box, then one
+                // thread stores it; rows past S are dropped by the store
+                uint8_t* stage = smem + L::kOffQ + t * L::kQBytes;
+                const float inv_l = 1.f / l_row;
+                if (eok) {
+                    ptx::tc_fence_after_sync();
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    uint32_t o[32];
-                    ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
-                    ptx::tmem_ld_wait();
-                    ptx::reg_fence<32>(o);
+                    for (int q = 0; q < kDH / 32; ++q) {
+                        uint32_t o[32];
+                        ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence<32>(o);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {   // four 16-byte chunks of 8 values
-                        const int cc = q * 4 + u;   // chunk index along the row
-                        const int half = cc >> 3;
-                        const int phys = (cc & 7) ^ (r & 7);
-                        uint4 v;
-                        v.x = pack2<BF16>(__uint_as_float(o[u * 8 + 0]) * inv_l,
-                                          __uint_as_float(o[u * 8 + 1]) * inv_l);
-                        v.y = pack2<BF16>(__uint_as_float(o[u * 8 + 2]) * inv_l,
-                                          __uint_as_float(o[u * 8 + 3]) * inv_l);
-                        v.z = pack2<BF16>(__uint_as_float(o[u * 8 + 4]) * inv_l,
-                                          __uint_as_float(o[u * 8 + 5]) * inv_l);
-                        v.w = pack2<BF16>(__uint_as_float(o[u * 8 + 6]) * inv_l,
-                                          __uint_as_float(o[u * 8 + 7]) * inv_l);
-                        *reinterpret_cast<uint4*>(stage + half * (kBM * 128) + r * 128 + phys * 16) = v;
+                        for (int u = 0; u < 4; ++u) {   // four 16-byte chunks of 8 values
+                            const int cc = hf * (kDH / 8) + q * 4 + u;   // chunk along the row
+                            const int box = cc >> 3;
+                            const int phys = (cc & 7) ^ (r & 7);
+                            uint4 v;
+                            v.x = pack2<BF16>(__uint_as_float(o[u * 8 + 0]) * inv_l,
+                                              __uint_as_float(o[u * 8 + 1]) * inv_l);
+                            v.y = pack2<BF16>(__uint_as_float(o[u * 8 + 2]) * inv_l,
+                                              __uint_as_float(o[u * 8 + 3]) * inv_l);
+                            v.z = pack2<BF16>(__uint_as_float(o[u * 8 + 4]) * inv_l,
+                                              __uint_as_float(o[u * 8 + 5]) * inv_l);
+                            v.w = pack2<BF16>(__uint_as_float(o[u * 8 + 6]) * inv_l,
+                                              __uint_as_float(o[u * 8 + 7]) * inv_l);
+                            *reinterpret_cast<uint4*>(stage + box * (kBM * 128) + r * 128 + phys * 16) = v;
+                        }
                     }
+                    ptx::fence_proxy_async_smem();
                 }
-                ptx::fence_proxy_async_smem();
-            }
-            const bool all_ok = ptx::named_barrier_and(1 + t, kBM, eok);
-            if (all_ok && r == 0) {
-                for (int cch = 0; cch < kChunks; ++cch)
-                    ptx::tma_store_4d(&tmO, ptx::smem_addr(stage + cch * (kBM * 128)), cch * 64, h, r0,
-                                      b);
-                ptx::bulk_commit_group();
-                ptx::bulk_wait_group_all();
-            }
-            if (all_ok && p.lse != nullptr && row < p.S) {
-                // LSE = scale * m + ln l = ln2 * (m * scale * log2e + log2 l)
-                p.lse[static_cast<size_t>(bh) * p.S + row] =
-                    (m_use * c + log2f(l)) * 0.69314718055994530942f;
+                const bool all_ok = ptx::named_barrier_and(tile_bar, kTileThreads, eok);
+                if (all_ok && r == 0 && hf == 0) {
+                    for (int cch = 0; cch < kChunks; ++cch)
+                        ptx::tma_store_4d(&tmO, ptx::smem_addr(stage + cch * (kBM * 128)), cch * 64, h,
+                                          r0, b);
+                    ptx::bulk_commit_group();
+                    ptx::bulk_wait_group_all();
+                }
+                if (all_ok && hf == 0 && p.lse != nullptr && row < p.S) {
+                    // LSE = scale * m + ln l = ln2 * (m * scale * log2e + log2 l)
+                    p.lse[static_cast<size_t>(bh) * p.S + row] =
+                        (m_use * c + log2f(l_row)) * 0.69314718055994530942f;
+                }
             }
         }
     }
