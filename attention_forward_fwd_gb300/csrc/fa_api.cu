@@ -102,7 +102,9 @@ SplitPlan plan_split(int B, int H, int S, bool causal, int sms) {
     const int nkv_all = (S + fa::kBN - 1) / fa::kBN;
     plan.ctas_per_head = nqb;
     const long long base = static_cast<long long>(B) * H * nqb;
-    if (sms <= 0 || base * 4 >= static_cast<long long>(sms) * 3 || nkv_all <= 2) return plan;
+    if (sms <= 0 || base * 4 >= static_cast<long long>(sms) * 3 || nkv_all <= 2 ||
+        nqb > fa::kMaxSplitBlocks)
+        return plan;
     int lo = 2, hi = nkv_all;   // grid size is non-increasing in the chunk
     if (static_cast<long long>(B) * H * ctas_per_head_for(S, causal, hi) > sms) return plan;
     while (lo < hi) {
@@ -161,6 +163,17 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     const size_t o_floats = static_cast<size_t>(B) * H * ntq * plan.max_splits * fa::kBM * D;
     p.ws_o = plan.chunk ? static_cast<float*>(workspace) : nullptr;
     p.ws_ml = plan.chunk ? static_cast<float*>(workspace) + o_floats : nullptr;
+    if (plan.chunk) {
+        // first CTA (blockIdx.y) of each query block's splits, in visit order
+        const bool c = causal != 0;
+        int y = 0;
+        for (int i = 0; i < p.nqb; ++i) {
+            p.split_begin[i] = static_cast<uint16_t>(y);
+            const int qb = c ? (p.nqb - 1 - i) : i;
+            y += (fa::key_tiles_for_block(qb, S, c) + plan.chunk - 1) / plan.chunk;
+        }
+        p.split_begin[p.nqb] = static_cast<uint16_t>(y);
+    }
     const dim3 grid(static_cast<unsigned>(B) * static_cast<unsigned>(H),
                     static_cast<unsigned>(plan.ctas_per_head));
     kern<<<grid, fa::Roles<RS>::kThreads, kSmem, stream>>>(mq, mk, mv, mo, p);

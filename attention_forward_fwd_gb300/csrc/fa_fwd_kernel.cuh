@@ -95,6 +95,9 @@ constexpr int kStatusTimeout = 4;
 // Device status word: 0, or the status of the first wait that ran out.
 __device__ int g_fa_device_status;
 
+// query blocks per head beyond which the keys are never split
+constexpr int kMaxSplitBlocks = 128;
+
 struct FwdParams {
     int B, H, S;
     int causal;
@@ -110,6 +113,9 @@ struct FwdParams {
     int max_splits;     // splits of the longest query block
     float* ws_o;        // partial o~ tiles (fp32)
     float* ws_ml;       // partial (m * scale * log2e, l) per row
+    // split mode: CTAs [split_begin[i], split_begin[i+1]) of a head hold the
+    // splits of the i-th query block visited (heaviest first when causal)
+    uint16_t split_begin[kMaxSplitBlocks + 1];
 };
 
 // Workspace of the split-over-keys path.  One partial slot per (b*H + h,
@@ -234,9 +240,10 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     const uint32_t sbase = ptx::smem_addr(smem);
     Barriers<NS, RS>* bars = reinterpret_cast<Barriers<NS, RS>*>(smem + L::kOffBar);
     volatile int* abort_flag = &bars->abort;
-
+    auto bar_addr = [&](const uint64_t* bptr) { return ptx::smem_addr(bptr); };
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+
     const int bh = blockIdx.x;
     const int b = bh / p.H;
     const int h = bh - b * p.H;
@@ -251,20 +258,17 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         nsplit = 1;
         split = 0;
     } else {
-        int y = static_cast<int>(blockIdx.y);
-        qb = 0;
-        nsplit = 1;
-        for (int i = 0; i < p.nqb; ++i) {
-            const int qbi = causal ? (p.nqb - 1 - i) : i;
-            const int ns = (key_tiles_for_block(qbi, p.S, causal) + p.kv_chunk - 1) / p.kv_chunk;
-            if (y < ns) {
-                qb = qbi;
-                nsplit = ns;
-                break;
-            }
-            y -= ns;
+        // the visit index i with split_begin[i] <= y < split_begin[i+1]
+        const int y = static_cast<int>(blockIdx.y);
+        int lo = 0, hi = p.nqb;   // split_begin[lo] <= y < split_begin[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.split_begin[mid] <= y) lo = mid;
+            else hi = mid;
         }
-        split = y;
+        qb = causal ? (p.nqb - 1 - lo) : lo;
+        nsplit = p.split_begin[lo + 1] - p.split_begin[lo];
+        split = y - p.split_begin[lo];
         jb = split * p.kv_chunk;
         je = jb + p.kv_chunk;
     }
@@ -280,10 +284,42 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     auto ring_k = [&](int j) { return kSepP ? (j == 0 ? 0 : 2 * j - 1) : 2 * j; };
     auto ring_v = [&](int j) { return kSepP ? (j == nkv - 1 ? 2 * nkv - 1 : 2 * j + 2) : 2 * j + 1; };
 
-    auto bar_addr = [&](const uint64_t* bptr) { return ptx::smem_addr(bptr); };
+
+    // The producer thread initialises the barriers and starts the Q loads and
+    // the first round of the K / V ring before the CTA-wide sync, so that
+    // their latency overlaps the TMEM allocation.
+    const uint32_t qbar = bar_addr(&bars->q_full);
+    // ring item i -> (K or V, key tile j of this CTA's range)
+    auto load_item = [&](int i, int slot) {
+        const uint32_t fb = bar_addr(&bars->kv_full[slot]);
+        ptx::mbar_arrive_expect_tx(fb, L::kKVBytes);
+        bool is_v;
+        int j;
+        if (!kSepP) {
+            is_v = (i & 1) != 0;
+            j = i >> 1;
+        } else if (i == 0) {
+            is_v = false;
+            j = 0;
+        } else if (i == 2 * nkv - 1) {
+            is_v = true;
+            j = nkv - 1;
+        } else if (i & 1) {
+            is_v = false;
+            j = (i + 1) >> 1;
+        } else {
+            is_v = true;
+            j = (i - 2) >> 1;
+        }
+        const CUtensorMap* m = is_v ? &tmV : &tmK;
+        for (int c = 0; c < kChunks; ++c)
+            ptx::tma_load_4d(sbase + L::kOffKV + slot * L::kKVBytes + c * (kBN * 128), m, fb, c * 64, h,
+                             (jb + j) * kBN, b);
+    };
+    const int first_round = min(NS, 2 * nkv);   // ring items loaded before the sync
 
     // ---------------------------------------------------------------- setup
-    if (threadIdx.x == 0) {
+    if (warp == kLoadWarp && lane == 0) {
         ptx::mbar_init(bar_addr(&bars->q_full), 1);
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(bar_addr(&bars->kv_full[s]), 1);
@@ -298,16 +334,25 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         }
         bars->abort = 0;
         ptx::fence_barrier_init();
-    }
-    if (warp == kMmaWarp) {
-        ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kTmemCols);
-        ptx::tmem_relinquish();
-    }
-    if (warp == kLoadWarp && lane == 0) {
         ptx::tma_prefetch_map(&tmQ);
         ptx::tma_prefetch_map(&tmK);
         ptx::tma_prefetch_map(&tmV);
         ptx::tma_prefetch_map(&tmO);
+        uint32_t qbytes = 0;
+        for (int t = 0; t < kQTiles; ++t)
+            if ((t == 0 ? nkv0 : nkv1) > 0) qbytes += L::kQBytes;
+        ptx::mbar_arrive_expect_tx(qbar, qbytes);
+        for (int t = 0; t < kQTiles; ++t) {
+            if ((t == 0 ? nkv0 : nkv1) == 0) continue;
+            for (int c = 0; c < kChunks; ++c)
+                ptx::tma_load_4d(sbase + L::kOffQ + t * L::kQBytes + c * (kBM * 128), &tmQ, qbar,
+                                 c * 64, h, q0 + t * kBM, b);
+        }
+        for (int i = 0; i < first_round; ++i) load_item(i, i);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kTmemCols);
+        ptx::tmem_relinquish();
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -324,48 +369,13 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint32_t qbar = bar_addr(&bars->q_full);
-            uint32_t qbytes = 0;
-            for (int t = 0; t < kQTiles; ++t)
-                if ((t == 0 ? nkv0 : nkv1) > 0) qbytes += L::kQBytes;
-            ptx::mbar_arrive_expect_tx(qbar, qbytes);
-            for (int t = 0; t < kQTiles; ++t) {
-                if ((t == 0 ? nkv0 : nkv1) == 0) continue;
-                for (int c = 0; c < kChunks; ++c)
-                    ptx::tma_load_4d(sbase + L::kOffQ + t * L::kQBytes + c * (kBM * 128), &tmQ, qbar,
-                                     c * 64, h, q0 + t * kBM, b);
-            }
-            int issued = 0;
-            for (int i = 0; i < 2 * nkv; ++i) {
+            // Q and the first round of the ring were started before the sync
+            int issued = first_round;
+            for (int i = first_round; i < 2 * nkv; ++i) {
                 const int slot = i % NS;
                 const int round = i / NS;
-                if (round > 0 &&
-                    !wait_phase(bar_addr(&bars->kv_empty[slot]), (round - 1) & 1, abort_flag))
-                    break;
-                const uint32_t fb = bar_addr(&bars->kv_full[slot]);
-                ptx::mbar_arrive_expect_tx(fb, L::kKVBytes);
-                bool is_v;
-                int j;
-                if (!kSepP) {
-                    is_v = (i & 1) != 0;
-                    j = i >> 1;
-                } else if (i == 0) {
-                    is_v = false;
-                    j = 0;
-                } else if (i == 2 * nkv - 1) {
-                    is_v = true;
-                    j = nkv - 1;
-                } else if (i & 1) {
-                    is_v = false;
-                    j = (i + 1) >> 1;
-                } else {
-                    is_v = true;
-                    j = (i - 2) >> 1;
-                }
-                const CUtensorMap* m = is_v ? &tmV : &tmK;
-                for (int c = 0; c < kChunks; ++c)
-                    ptx::tma_load_4d(sbase + L::kOffKV + slot * L::kKVBytes + c * (kBN * 128), m, fb,
-                                     c * 64, h, (jb + j) * kBN, b);
+                if (!wait_phase(bar_addr(&bars->kv_empty[slot]), (round - 1) & 1, abort_flag)) break;
+                load_item(i, slot);
                 issued = i + 1;
             }
             if (*abort_flag) {
@@ -584,6 +594,25 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             if (kBreakOnAbort && !ok) break;
             ptx::tc_fence_after_sync();
             uint32_t s[kHalf];
+            const int kv0 = (jb + j) * kBN + hf * kHalf;   // key of column 0
+            // Keys past the end and, on diagonal tiles, keys after the row are masked.
+            const bool need_mask = kv0 + kHalf > p.S || (p.causal && kv0 + kHalf - 1 > r0);
+            const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
+            constexpr int kChains = 4;
+            float mx[kChains];
+#pragma unroll
+            for (int i = 0; i < kChains; ++i) mx[i] = -INFINITY;
+            auto mask_max = [&](int k0, int k1) {
+                if (need_mask) {
+#pragma unroll
+                    for (int k = k0; k < k1; ++k)
+                        if (kv0 + k > last) s[k] = __float_as_uint(-INFINITY);
+                }
+#pragma unroll
+                for (int k = k0 / 2; k < k1 / 2; ++k)
+                    mx[k % kChains] = ptx::fmax3(mx[k % kChains], __uint_as_float(s[2 * k]),
+                                                 __uint_as_float(s[2 * k + 1]));
+            };
 #pragma unroll
             for (int q = 0; q < kHalf / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
             ptx::tmem_ld_wait();
@@ -593,21 +622,10 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 ptx::tc_fence_before_sync();
                 ptx::mbar_arrive(bar_addr(&bars->s_free[t]));
             }
-
-            const int kv0 = (jb + j) * kBN + hf * kHalf;   // key of column 0
-            // Mask keys past the end and, on diagonal tiles, keys after the row.
-            if (kv0 + kHalf > p.S || (p.causal && kv0 + kHalf - 1 > r0)) {
-                const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
+            mask_max(0, kHalf);
+            float m_tile = mx[0];
 #pragma unroll
-                for (int k = 0; k < kHalf; ++k)
-                    if (kv0 + k > last) s[k] = __float_as_uint(-INFINITY);
-            }
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int k = 0; k < kHalf / 2; ++k)
-                mx[k & 3] = ptx::fmax3(mx[k & 3], __uint_as_float(s[2 * k]),
-                                       __uint_as_float(s[2 * k + 1]));
-            float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            for (int i = 1; i < kChains; ++i) m_tile = fmaxf(m_tile, mx[i]);
             if constexpr (kRowSplit > 1) {
                 bars->row_max[j & 1][t][hf][r] = m_tile;
                 ptx::named_barrier_sync(pair_bar, 32 * kRowSplit);
