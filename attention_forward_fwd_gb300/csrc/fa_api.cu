@@ -82,7 +82,7 @@ int num_sms() {
 struct SplitPlan {
     int chunk = 0;          // key tiles per split (0: no split)
     int max_splits = 1;     // splits of the longest query block
-    int ctas_per_head = 0;  // gridDim.y
+    int ctas_per_head = 0;  // work items per head
 };
 
 long long ctas_per_head_for(int S, bool causal, int chunk) {
@@ -174,9 +174,13 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
         }
         p.split_begin[p.nqb] = static_cast<uint16_t>(y);
     }
-    const dim3 grid(static_cast<unsigned>(B) * static_cast<unsigned>(H),
-                    static_cast<unsigned>(plan.ctas_per_head));
-    kern<<<grid, fa::Roles<RS>::kThreads, kSmem, stream>>>(mq, mk, mv, mo, p);
+    // one CTA per SM, each running its share of the work items (at most one
+    // CTA per item)
+    const long long items = static_cast<long long>(B) * H * plan.ctas_per_head;
+    p.items = static_cast<int>(items);
+    const int sms = num_sms();
+    const long long ctas = (sms > 0 && items > sms) ? sms : items;
+    kern<<<dim3(static_cast<unsigned>(ctas)), fa::Roles<RS>::kThreads, kSmem, stream>>>(mq, mk, mv, mo, p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     if (plan.chunk == 0) return FA_OK;
 
@@ -209,10 +213,12 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
                           reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O);
     if (mis & 15u) return FA_ERR_UNSUPPORTED;
     if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return FA_ERR_UNSUPPORTED;
-    // grid limits: B*H blocks in x, ceil(S / 256) in y (<= 65535)
+    // work items (query blocks of 256 rows times B*H) are numbered with an
+    // int; a head holds at most 65535 query blocks
     const long long rows_per_cta = static_cast<long long>(fa::kQTiles) * fa::kBM;
-    if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-    if ((static_cast<long long>(S) + rows_per_cta - 1) / rows_per_cta > 65535) return FA_ERR_UNSUPPORTED;
+    const long long nqb = (static_cast<long long>(S) + rows_per_cta - 1) / rows_per_cta;
+    if (nqb > 65535) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * H * nqb > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     return FA_OK;
 }
 

@@ -72,7 +72,7 @@ struct WarpLayout<2> {
     static constexpr int kSoftmaxWarps = 16;
     static constexpr uint32_t kLaunchRegs = 96;
     static constexpr uint32_t kSoftmaxRegs = 104;
-    static constexpr uint32_t kControlRegs = 56;
+    static constexpr uint32_t kControlRegs = 64;
 };
 template <int RS>
 struct Roles : WarpLayout<RS> {
@@ -101,6 +101,13 @@ constexpr int kMaxSplitBlocks = 128;
 struct FwdParams {
     int B, H, S;
     int causal;
+    // Work items: the (query block, split) pairs of every head, numbered
+    // w = y * (B*H) + b*H + h with y the block's visit index (heaviest first
+    // when causal).  Each CTA runs items blockIdx.x, 2G-1-blockIdx.x,
+    // 2G+blockIdx.x, ... (G = gridDim.x, every other round reversed), so a
+    // grid of one CTA per SM keeps its set-up across items and the rounds of
+    // heavy and light blocks even out.
+    int items;
     float scale_log2;   // scale * log2(e)
     float* lse;         // [B, H, S] fp32 or nullptr
     // Split over keys (0 = off).  With kv_chunk > 0 the CTAs of one head are
@@ -144,9 +151,16 @@ __host__ __device__ inline int key_tiles_for_block(int qb, int S, bool causal) {
     return n;
 }
 
+// P_t in TMEM columns of its own (when 2*kBN + 2*D + kQTiles*kBN/2 fit in
+// 512, i.e. D = 64), else written over S_t.
+__host__ __device__ constexpr bool separate_p(int D) {
+    return (2 * kBN + 2 * D + kQTiles * (kBN / 2)) <= static_cast<int>(kTmemCols);
+}
+
 template <int NS, int RS>
 struct Barriers {
     uint64_t q_full;
+    uint64_t q_empty;   // the Q buffer may be loaded with the next item's Q
     uint64_t kv_full[NS];
     uint64_t kv_empty[NS];
     uint64_t s_full[kQTiles];
@@ -157,21 +171,85 @@ struct Barriers {
     uint32_t tmem_base;
     int abort;
     // the RS threads of a row swap partial row maxima (double-buffered over
-    // key tiles) and, at the end, partial row sums
+    // key tiles) and, at the end of an item, partial row sums (double-buffered
+    // over items)
     float row_max[2][kQTiles][RS][kBM];
-    float row_sum[kQTiles][RS][kBM];
+    float row_sum[2][kQTiles][RS][kBM];
 };
 
+// Shared memory: Q tiles, the K / V ring and, where there is room (D = 64),
+// a buffer of its own for staging the O tiles of the TMA-store epilogue, so
+// that the next item's Q can be loaded while the O of this one is stored.
+// Otherwise O is staged in the Q buffer it replaces.
 template <int D, int NS, int RS>
 struct SmemLayout {
     static constexpr int kQBytes = kBM * D * 2;
     static constexpr int kKVBytes = kBN * D * 2;
+    static constexpr bool kStageInQ = !separate_p(D);
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQTiles * kQBytes;
-    static constexpr int kOffBar = kOffKV + NS * kKVBytes;
+    static constexpr int kOffStage = kStageInQ ? kOffQ : kOffKV + NS * kKVBytes;
+    static constexpr int kOffBar = kOffKV + NS * kKVBytes + (kStageInQ ? 0 : kQTiles * kQBytes);
     static constexpr int kBytes = kOffBar + static_cast<int>(sizeof(Barriers<NS, RS>));
     static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024
 };
+
+// One work item: a query block of kQTiles*kBM rows of head (b, h) and the
+// key tiles [jb, jb + nkv_t) that query tile t visits in this item's split.
+struct WorkItem {
+    int b, h, bh;
+    int q0;             // first query row of the block
+    int jb;             // first key tile of the split
+    int nkv0, nkv1;     // key tiles of query tiles 0 and 1
+    int nkv;            // max(nkv0, nkv1)
+    int split;          // split index within the block
+    bool partial;       // the block is split: write partial results
+};
+
+__device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
+    WorkItem it;
+    const int bhn = p.B * p.H;
+    const int y = w / bhn;
+    it.bh = w - y * bhn;
+    it.b = it.bh / p.H;
+    it.h = it.bh - it.b * p.H;
+    const bool causal = p.causal != 0;
+    int qb, je, nsplit;
+    if (p.kv_chunk <= 0) {
+        qb = causal ? (p.nqb - 1 - y) : y;   // causal: heaviest query blocks first
+        it.jb = 0;
+        je = 0x7fffffff;
+        nsplit = 1;
+        it.split = 0;
+    } else {
+        // the visit index i with split_begin[i] <= y < split_begin[i+1]
+        int lo = 0, hi = p.nqb;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.split_begin[mid] <= y) lo = mid;
+            else hi = mid;
+        }
+        qb = causal ? (p.nqb - 1 - lo) : lo;
+        nsplit = p.split_begin[lo + 1] - p.split_begin[lo];
+        it.split = y - p.split_begin[lo];
+        it.jb = it.split * p.kv_chunk;
+        je = it.jb + p.kv_chunk;
+    }
+    it.q0 = qb * (kQTiles * kBM);
+    it.nkv0 = max(0, min(je, key_tiles_for(it.q0, p.S, causal)) - it.jb);
+    it.nkv1 = max(0, min(je, key_tiles_for(it.q0 + kBM, p.S, causal)) - it.jb);
+    it.nkv = max(it.nkv0, it.nkv1);
+    it.partial = nsplit > 1;
+    return it;
+}
+
+// Item index of this CTA's k-th work item, or -1 past its last one.
+__device__ __forceinline__ int cta_item(int k, int items) {
+    const long long G = gridDim.x;
+    const long long c = blockIdx.x;
+    const long long w = k * G + ((k & 1) ? (G - 1 - c) : c);
+    return w < items ? static_cast<int>(w) : -1;
+}
 
 // Bounded wait on the phase of `bar` with parity `parity`.  Returns false
 // (and sets the abort flag) if the wait ran out of time, or false at once if
@@ -217,12 +295,13 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     constexpr int kMmaWarp1 = R::kMmaWarp1;
     constexpr int kTileThreads = R::kTileThreads;
     constexpr int kChunks = D / 64;   // 128-byte column chunks per row (TMA box width)
-    // Separate-P schedule (when TMEM has room: 2*kBN + 2*D + 2*64 <= 512, i.e.
-    // D = 64): P_t gets its own 64 TMEM columns, so S_t of the next key tile
-    // can be computed as soon as the softmax has read S_t into registers,
-    // while P_t V of this tile is still pending.  Otherwise P_t is written
-    // over S_t and the next S_t waits for P_t V (same thread, in order).
-    constexpr bool kSepP = (2 * kBN + 2 * D + kQTiles * (kBN / 2)) <= static_cast<int>(kTmemCols);
+    // Separate-P schedule (D = 64): P_t gets its own 64 TMEM columns, so S_t
+    // of the next key tile can be computed as soon as the softmax has read
+    // S_t into registers, while P_t V of this tile is still pending.
+    // Otherwise P_t is written over S_t and the next S_t waits for P_t V
+    // (same thread, in order).
+    constexpr bool kSepP = separate_p(D);
+    constexpr bool kStageInQ = L::kStageInQ;
     constexpr int kPCol0 = kSepP ? (2 * kBN + 2 * D) : 0;   // P_0 column
     constexpr int kPColStride = kSepP ? (kBN / 2) : kBN;     // P_1 - P_0
     // Each of the kRowSplit threads of a row writes the packed P of its
@@ -244,53 +323,16 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const int bh = blockIdx.x;
-    const int b = bh / p.H;
-    const int h = bh - b * p.H;
-    const bool causal = p.causal != 0;
-    // ---- which query block and which key tiles this CTA owns
-    int qb, jb, je, nsplit, split;
-    if (p.kv_chunk <= 0) {
-        // causal: heaviest query blocks first
-        qb = causal ? (p.nqb - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
-        jb = 0;
-        je = 0x7fffffff;
-        nsplit = 1;
-        split = 0;
-    } else {
-        // the visit index i with split_begin[i] <= y < split_begin[i+1]
-        const int y = static_cast<int>(blockIdx.y);
-        int lo = 0, hi = p.nqb;   // split_begin[lo] <= y < split_begin[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (p.split_begin[mid] <= y) lo = mid;
-            else hi = mid;
-        }
-        qb = causal ? (p.nqb - 1 - lo) : lo;
-        nsplit = p.split_begin[lo + 1] - p.split_begin[lo];
-        split = y - p.split_begin[lo];
-        jb = split * p.kv_chunk;
-        je = jb + p.kv_chunk;
-    }
-    const int q0 = qb * (kQTiles * kBM);
-    // tiles [jb, jb + nkv_t) of this CTA's key range for query tile t
-    const int nkv0 = max(0, min(je, key_tiles_for(q0, p.S, causal)) - jb);
-    const int nkv1 = max(0, min(je, key_tiles_for(q0 + kBM, p.S, causal)) - jb);
-    const int nkv = max(nkv0, nkv1);
-    const bool partial = nsplit > 1;
-    // Order of the K / V tiles through the ring.  Aliased P: K0 V0 K1 V1 ...
-    // Separate P: K0 K1 V0 K2 V1 ... K(n-1) V(n-2) V(n-1), since S_t(j+1) is
-    // issued before P_t(j) V_j.
-    auto ring_k = [&](int j) { return kSepP ? (j == 0 ? 0 : 2 * j - 1) : 2 * j; };
-    auto ring_v = [&](int j) { return kSepP ? (j == nkv - 1 ? 2 * nkv - 1 : 2 * j + 2) : 2 * j + 1; };
+    // Order of the K / V tiles of one item through the ring.  Aliased P:
+    // K0 V0 K1 V1 ...  Separate P: K0 K1 V0 K2 V1 ... K(n-1) V(n-2) V(n-1),
+    // since S_t(j+1) is issued before P_t(j) V_j.  The ring runs on across
+    // items: an item's tiles follow the previous item's.
+    auto ring_k = [](int j, int nkv) { return kSepP ? (j == 0 ? 0 : 2 * j - 1) : 2 * j; };
+    auto ring_v = [](int j, int nkv) { return kSepP ? (j == nkv - 1 ? 2 * nkv - 1 : 2 * j + 2) : 2 * j + 1; };
 
-
-    // The producer thread initialises the barriers and starts the Q loads and
-    // the first round of the K / V ring before the CTA-wide sync, so that
-    // their latency overlaps the TMEM allocation.
     const uint32_t qbar = bar_addr(&bars->q_full);
-    // ring item i -> (K or V, key tile j of this CTA's range)
-    auto load_item = [&](int i, int slot) {
+    // ring position i of item `it` -> slot `slot`
+    auto load_item = [&](const WorkItem& it, int i, int slot) {
         const uint32_t fb = bar_addr(&bars->kv_full[slot]);
         ptx::mbar_arrive_expect_tx(fb, L::kKVBytes);
         bool is_v;
@@ -301,9 +343,9 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         } else if (i == 0) {
             is_v = false;
             j = 0;
-        } else if (i == 2 * nkv - 1) {
+        } else if (i == 2 * it.nkv - 1) {
             is_v = true;
-            j = nkv - 1;
+            j = it.nkv - 1;
         } else if (i & 1) {
             is_v = false;
             j = (i + 1) >> 1;
@@ -313,14 +355,31 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         }
         const CUtensorMap* m = is_v ? &tmV : &tmK;
         for (int c = 0; c < kChunks; ++c)
-            ptx::tma_load_4d(sbase + L::kOffKV + slot * L::kKVBytes + c * (kBN * 128), m, fb, c * 64, h,
-                             (jb + j) * kBN, b);
+            ptx::tma_load_4d(sbase + L::kOffKV + slot * L::kKVBytes + c * (kBN * 128), m, fb, c * 64, it.h,
+                             (it.jb + j) * kBN, it.b);
     };
-    const int first_round = min(NS, 2 * nkv);   // ring items loaded before the sync
+    // Q tiles of item `it` (a tile with no key tile is not loaded)
+    auto load_q = [&](const WorkItem& it) {
+        uint32_t qbytes = 0;
+        for (int t = 0; t < kQTiles; ++t)
+            if ((t == 0 ? it.nkv0 : it.nkv1) > 0) qbytes += L::kQBytes;
+        ptx::mbar_arrive_expect_tx(qbar, qbytes);
+        for (int t = 0; t < kQTiles; ++t) {
+            if ((t == 0 ? it.nkv0 : it.nkv1) == 0) continue;
+            for (int c = 0; c < kChunks; ++c)
+                ptx::tma_load_4d(sbase + L::kOffQ + t * L::kQBytes + c * (kBM * 128), &tmQ, qbar, c * 64,
+                                 it.h, it.q0 + t * kBM, it.b);
+        }
+    };
 
     // ---------------------------------------------------------------- setup
+    // The producer thread initialises the barriers and starts the first
+    // item's Q loads and the first round of its K / V ring before the
+    // CTA-wide sync, so that their latency overlaps the TMEM allocation.
+    int first_round = 0;   // ring items of the first item loaded before the sync
     if (warp == kLoadWarp && lane == 0) {
-        ptx::mbar_init(bar_addr(&bars->q_full), 1);
+        ptx::mbar_init(qbar, 1);
+        ptx::mbar_init(bar_addr(&bars->q_empty), kQTiles);
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(bar_addr(&bars->kv_full[s]), 1);
             ptx::mbar_init(bar_addr(&bars->kv_empty[s]), kSepP ? kQTiles : 1);   // one per MMA issuer
@@ -338,17 +397,10 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         ptx::tma_prefetch_map(&tmK);
         ptx::tma_prefetch_map(&tmV);
         ptx::tma_prefetch_map(&tmO);
-        uint32_t qbytes = 0;
-        for (int t = 0; t < kQTiles; ++t)
-            if ((t == 0 ? nkv0 : nkv1) > 0) qbytes += L::kQBytes;
-        ptx::mbar_arrive_expect_tx(qbar, qbytes);
-        for (int t = 0; t < kQTiles; ++t) {
-            if ((t == 0 ? nkv0 : nkv1) == 0) continue;
-            for (int c = 0; c < kChunks; ++c)
-                ptx::tma_load_4d(sbase + L::kOffQ + t * L::kQBytes + c * (kBM * 128), &tmQ, qbar,
-                                 c * 64, h, q0 + t * kBM, b);
-        }
-        for (int i = 0; i < first_round; ++i) load_item(i, i);
+        const WorkItem it = decode_item(p, cta_item(0, p.items));   // the grid has <= items CTAs
+        load_q(it);
+        first_round = min(NS, 2 * it.nkv);
+        for (int i = 0; i < first_round; ++i) load_item(it, i, i);
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kTmemCols);
@@ -369,20 +421,48 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            // Q and the first round of the ring were started before the sync
-            int issued = first_round;
-            for (int i = first_round; i < 2 * nkv; ++i) {
-                const int slot = i % NS;
-                const int round = i / NS;
-                if (!wait_phase(bar_addr(&bars->kv_empty[slot]), (round - 1) & 1, abort_flag)) break;
-                load_item(i, slot);
-                issued = i + 1;
+            long long gi = 0;   // ring items issued, all items
+            int k_q = 0;        // last item whose Q was loaded
+            bool ok = true;
+            // ring item gi goes to slot gi % NS once the item NS before it released it
+            auto slot_free = [&](long long g) {
+                return g < NS || wait_phase(bar_addr(&bars->kv_empty[g % NS]),
+                                            static_cast<uint32_t>((g / NS - 1) & 1), abort_flag);
+            };
+            for (int k = 0; ok; ++k) {
+                const int w = cta_item(k, p.items);
+                if (w < 0) break;
+                const WorkItem it = decode_item(p, w);
+                const int n = 2 * it.nkv;
+                int i = 0;
+                if (k == 0) {
+                    i = first_round;   // loaded before the sync, after the Q
+                    gi = first_round;
+                } else {
+                    // With O staged in the Q buffer, the Q of this item waits
+                    // for the previous item's epilogue: load the K / V tiles
+                    // that only need free slots first.
+                    const int pre = kStageInQ ? min(NS, n) : 0;
+                    for (; i < pre; ++i, ++gi) {
+                        if (!(ok = slot_free(gi))) break;
+                        load_item(it, i, static_cast<int>(gi % NS));
+                    }
+                    if (!ok) break;
+                    if (!(ok = wait_phase(bar_addr(&bars->q_empty), (k - 1) & 1, abort_flag))) break;
+                    load_q(it);
+                    k_q = k;
+                }
+                for (; i < n; ++i, ++gi) {
+                    if (!(ok = slot_free(gi))) break;
+                    load_item(it, i, static_cast<int>(gi % NS));
+                }
             }
             if (*abort_flag) {
                 // Let every copy this thread started land before the CTA exits.
-                wait_phase(qbar, 0, abort_flag, false);
-                for (int i = max(0, issued - NS); i < issued; ++i)
-                    wait_phase(bar_addr(&bars->kv_full[i % NS]), (i / NS) & 1, abort_flag, false);
+                wait_phase(qbar, k_q & 1, abort_flag, false);
+                for (long long i = (gi > NS ? gi - NS : 0); i < gi; ++i)
+                    wait_phase(bar_addr(&bars->kv_full[i % NS]), static_cast<uint32_t>((i / NS) & 1),
+                               abort_flag, false);
             }
         }
     } else if (kSepP && (warp == kMmaWarp || warp == kMmaWarp1)) {
@@ -391,12 +471,13 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         // wait only on its own softmax.  Both issuers see every K / V tile of
         // the ring in the same order and release each slot once (a commit
         // after the products that read it, or a plain arrive once it has
-        // landed when this tile has no work on it).
+        // landed when this tile has no work on it), and each releases the Q
+        // buffer of an item once its last S_t has been computed.
         if (lane == 0) {
             const int t = (warp == kMmaWarp) ? 0 : 1;
-            const int n_t = (t == 0) ? nkv0 : nkv1;
             constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
             constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, D, BF16, true);
+            // ring positions are kept modulo 2*NS: slot and phase parity only
             auto full_bar = [&](int i) { return bar_addr(&bars->kv_full[i % NS]); };
             auto full_par = [&](int i) { return static_cast<uint32_t>((i / NS) & 1); };
             auto slot_addr = [&](int i) { return sbase + L::kOffKV + (i % NS) * L::kKVBytes; };
@@ -404,6 +485,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             const uint32_t s_free = bar_addr(&bars->s_free[t]);
             const uint32_t p_full = bar_addr(&bars->p_full[t]);
             const uint32_t o_done = bar_addr(&bars->o_done[t]);
+            const uint32_t q_empty = bar_addr(&bars->q_empty);
 
             // S_t = Q_t K^T over D in K=16 steps; both operands K-major.
             auto issue_s = [&](int ring) {
@@ -438,42 +520,54 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 return true;
             };
 
-            bool ok = (n_t == 0) || wait_phase(bar_addr(&bars->q_full), 0, abort_flag);
-            if (ok) ok = acquire(ring_k(0), n_t > 0);
-            if (ok && n_t > 0) issue_s(ring_k(0));
-            for (int j = 0; ok && j < nkv; ++j) {
-                const bool next = (j + 1) < nkv;
-                if constexpr (kSepP) {
+            int gi0 = 0;       // ring position of the item's first tile, modulo 2*NS
+            uint32_t gs = 0;   // S_t tiles issued, all items (parities only)
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int w = cta_item(k, p.items);
+                if (w < 0) break;
+                const WorkItem it = decode_item(p, w);
+                const int nkv = it.nkv;
+                const int n_t = (t == 0) ? it.nkv0 : it.nkv1;
+                const uint32_t gs0 = gs;   // S_t / P_t / P_t V index of this item's key tile 0
+                // every issuer waits for every Q load, so that its phases stay in step
+                if (!(ok = wait_phase(qbar, k & 1, abort_flag))) break;
+                if (!(ok = acquire(gi0 + ring_k(0, nkv), n_t > 0))) break;
+                if (n_t > 0) {
+                    // S_t of the previous item must have been read by the softmax
+                    if (gs > 0 && !(ok = wait_phase(s_free, (gs - 1) & 1, abort_flag))) break;
+                    ptx::tc_fence_after_sync();
+                    issue_s(gi0 + ring_k(0, nkv));
+                    ++gs;
+                }
+                // the Q buffer of tile t is free once its last S_t is complete
+                if (n_t <= 1) {
+                    if (n_t == 1) ptx::tc_commit(q_empty);
+                    else ptx::mbar_arrive(q_empty);
+                }
+                for (int j = 0; ok && j < nkv; ++j) {
                     // S_t(j+1) as soon as the softmax holds S_t(j), then P_t V(j)
-                    if (next) {
+                    if (j + 1 < nkv) {
                         const bool use = (j + 1) < n_t;
-                        if (!(ok = acquire(ring_k(j + 1), use))) break;
+                        if (!(ok = acquire(gi0 + ring_k(j + 1, nkv), use))) break;
                         if (use) {
-                            if (!(ok = wait_phase(s_free, j & 1, abort_flag))) break;
+                            if (!(ok = wait_phase(s_free, (gs - 1) & 1, abort_flag))) break;
                             ptx::tc_fence_after_sync();
-                            issue_s(ring_k(j + 1));
+                            issue_s(gi0 + ring_k(j + 1, nkv));
+                            ++gs;
+                            if (j + 2 == n_t) ptx::tc_commit(q_empty);
                         }
                     }
-                    if (!(ok = acquire(ring_v(j), j < n_t))) break;
+                    if (!(ok = acquire(gi0 + ring_v(j, nkv), j < n_t))) break;
                     if (j < n_t) {
-                        if (!(ok = wait_phase(p_full, j & 1, abort_flag))) break;
+                        // P_t(j) written; it also orders this item's first
+                        // P_t V after the previous epilogue's reads of O_t
+                        if (!(ok = wait_phase(p_full, (gs0 + j) & 1, abort_flag))) break;
                         ptx::tc_fence_after_sync();
-                        issue_pv(ring_v(j), j > 0);
-                    }
-                } else {
-                    // P_t V(j) first: S_t(j+1) overwrites P_t, which it reads
-                    if (!(ok = acquire(ring_v(j), j < n_t))) break;
-                    if (j < n_t) {
-                        if (!(ok = wait_phase(p_full, j & 1, abort_flag))) break;
-                        ptx::tc_fence_after_sync();
-                        issue_pv(ring_v(j), j > 0);
-                    }
-                    if (next) {
-                        const bool use = (j + 1) < n_t;
-                        if (!(ok = acquire(ring_k(j + 1), use))) break;
-                        if (use) issue_s(ring_k(j + 1));
+                        issue_pv(gi0 + ring_v(j, nkv), j > 0);
                     }
                 }
+                gi0 = (gi0 + 2 * nkv) % (2 * NS);
             }
             // Every MMA of this issuer must be complete before TMEM is freed.
             ptx::tc_commit(bar_addr(&bars->drain[t]));
@@ -484,7 +578,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         // One thread issues both tiles' products in the order
         //   S0(0) S1(0) | P0V(j) S0(j+1) P1V(j) S1(j+1) | ...
         // so that one tile's softmax runs while the other tile's products do;
-        // S_t(j+1) follows P_t V(j), which reads the P_t it overwrites.
+        // S_t(j+1) follows P_t V(j), which reads the P_t it overwrites.  The
+        // next item's S_t(0) follows this item's last P_t V the same way.
         if (lane == 0) {
             constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
             constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, D, BF16, true);
@@ -512,38 +607,50 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 ptx::tc_commit(bar_addr(&bars->o_done[t]));
             };
 
-            bool ok = wait_phase(bar_addr(&bars->q_full), 0, abort_flag);
-            if (ok) ok = wait_phase(full_bar(ring_k(0)), full_par(ring_k(0)), abort_flag);
-            if (ok) {
+            int gi0 = 0;                   // ring position of the item's K0, modulo 2*NS
+            uint32_t gs[kQTiles] = {0, 0};  // S_t tiles issued per query tile (parities only)
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int w = cta_item(k, p.items);
+                if (w < 0) break;
+                const WorkItem it = decode_item(p, w);
+                const int nkv = it.nkv, nkv0 = it.nkv0, nkv1 = it.nkv1;
+                const uint32_t g00 = gs[0], g10 = gs[1];
+                if (!(ok = wait_phase(qbar, k & 1, abort_flag))) break;
+                const int k0 = gi0 + ring_k(0, nkv);
+                if (!(ok = wait_phase(full_bar(k0), full_par(k0), abort_flag))) break;
                 ptx::tc_fence_after_sync();
-                if (nkv0 > 0) issue_s(0, ring_k(0));
-                if (nkv1 > 0) issue_s(1, ring_k(0));
-                ptx::tc_commit(bar_addr(&bars->kv_empty[ring_k(0) % NS]));
-            }
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int iv = ring_v(j);
-                const int ik = ring_k(j + 1);
-                const bool next = (j + 1) < nkv;
-                if (!(ok = wait_phase(full_bar(iv), full_par(iv), abort_flag))) break;
-                ptx::tc_fence_after_sync();
-                if (j < nkv0) {
-                    if (!(ok = wait_phase(bar_addr(&bars->p_full[0]), j & 1, abort_flag))) break;
+                if (nkv0 > 0) issue_s(0, k0);
+                if (nkv1 > 0) issue_s(1, k0);
+                ptx::tc_commit(bar_addr(&bars->kv_empty[k0 % NS]));
+                for (int j = 0; ok && j < nkv; ++j) {
+                    const int iv = gi0 + ring_v(j, nkv);
+                    const int ik = gi0 + ring_k(j + 1, nkv);
+                    const bool next = (j + 1) < nkv;
+                    if (!(ok = wait_phase(full_bar(iv), full_par(iv), abort_flag))) break;
                     ptx::tc_fence_after_sync();
-                    issue_pv(0, iv, j > 0);
+                    if (j < nkv0) {
+                        if (!(ok = wait_phase(bar_addr(&bars->p_full[0]), (g00 + j) & 1, abort_flag))) break;
+                        ptx::tc_fence_after_sync();
+                        issue_pv(0, iv, j > 0);
+                    }
+                    if (next) {
+                        if (!(ok = wait_phase(full_bar(ik), full_par(ik), abort_flag))) break;
+                        ptx::tc_fence_after_sync();
+                    }
+                    if (j + 1 < nkv0) issue_s(0, ik);
+                    if (j < nkv1) {
+                        if (!(ok = wait_phase(bar_addr(&bars->p_full[1]), (g10 + j) & 1, abort_flag))) break;
+                        ptx::tc_fence_after_sync();
+                        issue_pv(1, iv, j > 0);
+                    }
+                    ptx::tc_commit(bar_addr(&bars->kv_empty[iv % NS]));
+                    if (j + 1 < nkv1) issue_s(1, ik);
+                    if (next) ptx::tc_commit(bar_addr(&bars->kv_empty[ik % NS]));
                 }
-                if (next) {
-                    if (!(ok = wait_phase(full_bar(ik), full_par(ik), abort_flag))) break;
-                    ptx::tc_fence_after_sync();
-                }
-                if (j + 1 < nkv0) issue_s(0, ik);
-                if (j < nkv1) {
-                    if (!(ok = wait_phase(bar_addr(&bars->p_full[1]), j & 1, abort_flag))) break;
-                    ptx::tc_fence_after_sync();
-                    issue_pv(1, iv, j > 0);
-                }
-                ptx::tc_commit(bar_addr(&bars->kv_empty[iv % NS]));
-                if (j + 1 < nkv1) issue_s(1, ik);
-                if (next) ptx::tc_commit(bar_addr(&bars->kv_empty[ik % NS]));
+                gs[0] += nkv0;
+                gs[1] += nkv1;
+                gi0 = (gi0 + 2 * nkv) % (2 * NS);
             }
             // Every MMA must be complete before TMEM is freed.
             ptx::tc_commit(bar_addr(&bars->drain[0]));
@@ -558,9 +665,9 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         // rows 32*wq .. 32*wq+31 of the tile (wq = w % 4, the TMEM lane
         // quarter it may access).  With RS = 2 the two threads of a row swap
         // their partial maxima every key tile, so both keep the same reference
-        // max; each keeps its own partial row sum.  On an abort every warp
-        // still runs every swap barrier (with no TMEM work), so the barriers
-        // cannot hang.
+        // max; each keeps its own partial row sum.  After an abort every warp
+        // still walks every item and runs every named barrier (with no TMEM
+        // work), so the barriers cannot hang.
         constexpr int kHalf = kBN / kRowSplit;      // score columns per thread
         constexpr int kDH = D / kRowSplit;          // O columns per thread
         const int t = warp / (4 * kRowSplit);
@@ -576,143 +683,161 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                             (kSepP ? (kPCol0 + t * kPColStride + hf * (kHalf / 2)) : (t * kBN + hf * kHalf));
         const uint32_t pair_bar = 1 + t * 4 + wq;   // the RS warps sharing these rows
         const uint32_t tile_bar = 1 + 4 * kQTiles + t;
-        const int r0 = q0 + t * kBM;
-        const int row = r0 + r;
+        const bool store_thread = (r == 0 && hf == 0);   // issues this tile's O stores
         const float c = p.scale_log2;
-        const int n_tiles = (t == 0) ? nkv0 : nkv1;
-
-        float m_use = -INFINITY;   // reference max, raw (unscaled) score units
-        float l = 0.f;             // this thread's part of the row sum
-        bool ok = true;
-        // After an abort, one thread per row simply leaves the loop; with the
-        // row split, a warp keeps running its loop without TMEM stores or
+        // After an abort, one thread per row simply leaves the key loop; with
+        // the row split, a warp keeps running its loop without TMEM stores or
         // arrivals instead, so that the swap barriers stay matched.
         constexpr bool kBreakOnAbort = (kRowSplit == 1);
-        for (int j = 0; j < n_tiles; ++j) {
-            ok = (kBreakOnAbort || ok) && wait_phase(bar_addr(&bars->s_full[t]), j & 1, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (kBreakOnAbort && !ok) break;
-            ptx::tc_fence_after_sync();
-            uint32_t s[kHalf];
-            const int kv0 = (jb + j) * kBN + hf * kHalf;   // key of column 0
-            // Keys past the end and, on diagonal tiles, keys after the row are masked.
-            const bool need_mask = kv0 + kHalf > p.S || (p.causal && kv0 + kHalf - 1 > r0);
-            const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
-            constexpr int kChains = 4;
-            float mx[kChains];
-#pragma unroll
-            for (int i = 0; i < kChains; ++i) mx[i] = -INFINITY;
-            auto mask_max = [&](int k0, int k1) {
-                if (need_mask) {
-#pragma unroll
-                    for (int k = k0; k < k1; ++k)
-                        if (kv0 + k > last) s[k] = __float_as_uint(-INFINITY);
-                }
-#pragma unroll
-                for (int k = k0 / 2; k < k1 / 2; ++k)
-                    mx[k % kChains] = ptx::fmax3(mx[k % kChains], __uint_as_float(s[2 * k]),
-                                                 __uint_as_float(s[2 * k + 1]));
-            };
-#pragma unroll
-            for (int q = 0; q < kHalf / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
-            ptx::tmem_ld_wait();
-            ptx::reg_fence<kHalf>(s);
-            if (kSepP && (kBreakOnAbort || ok)) {
-                // S_t is in registers: the next S_t may overwrite it
-                ptx::tc_fence_before_sync();
-                ptx::mbar_arrive(bar_addr(&bars->s_free[t]));
-            }
-            mask_max(0, kHalf);
-            float m_tile = mx[0];
-#pragma unroll
-            for (int i = 1; i < kChains; ++i) m_tile = fmaxf(m_tile, mx[i]);
-            if constexpr (kRowSplit > 1) {
-                bars->row_max[j & 1][t][hf][r] = m_tile;
-                ptx::named_barrier_sync(pair_bar, 32 * kRowSplit);
-                m_tile = fmaxf(m_tile, bars->row_max[j & 1][t][hf ^ 1][r]);
-            }
-            const float m_new = fmaxf(m_use, m_tile);
-            // Lazy rescale: keep the old reference unless the max grew by more
-            // than kTauLog2 in log2 units (then p <= 2^kTauLog2).  The RS
-            // threads of a row see the same maxima, so they decide alike.
-            const bool rescale = (m_new - m_use) * c > kTauLog2;
-            float alpha = 1.f;
-            if (rescale) {
-                alpha = ptx::ex2_approx((m_use - m_new) * c);
-                m_use = m_new;
-            }
-            const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
+        bool ok = true;
+        uint32_t gs0 = 0;   // S_t tiles of earlier items (parities only)
 
-            // p = 2^(s*c - m*c), two columns per packed FMA / add
-            const float2 c2 = make_float2(c, c);
-            const float2 nmc2 = make_float2(-mc, -mc);
-            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-            for (int q = 0; q < kHalf / 32; ++q) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float2 x = __ffma2_rn(
-                        make_float2(__uint_as_float(s[q * 32 + 2 * k]),
-                                    __uint_as_float(s[q * 32 + 2 * k + 1])),
-                        c2, nmc2);
-                    const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
-                    sum2[k & 1] = __fadd2_rn(sum2[k & 1], pp);
-                    pk[k] = pack2<BF16>(pp.x, pp.y);
-                }
-                if (kSepP && q == 0 && j > 0 && ok) {
-                    // P_t and O_t are still read / written by P_t V of tile j-1
-                    ok = wait_phase(bar_addr(&bars->o_done[t]), (j - 1) & 1, abort_flag);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (kBreakOnAbort && !ok) break;
-                    ptx::tc_fence_after_sync();
-                }
-                if (kBreakOnAbort || ok) ptx::tmem_st_32x32b_x16(tP + q * 16, pk);
-            }
-            if (kBreakOnAbort && !ok) break;
-            const float2 sum = __fadd2_rn(sum2[0], sum2[1]);
-            l = l * alpha + (sum.x + sum.y);
+        for (int k = 0;; ++k) {
+            const int w = cta_item(k, p.items);
+            if (w < 0) break;
+            const WorkItem it = decode_item(p, w);
+            const int r0 = it.q0 + t * kBM;
+            const int row = r0 + r;
+            const int n_tiles = (t == 0) ? it.nkv0 : it.nkv1;
 
-            // O_t was last written by P V of tile j-1: with separate P its
-            // completion was awaited above; with P over S it completed before
-            // S_t of tile j (same issuing thread, in order).
-            if ((kBreakOnAbort || ok) && j > 0 && __any_sync(0xffffffffu, rescale)) {
+            float m_use = -INFINITY;   // reference max, raw (unscaled) score units
+            float l = 0.f;             // this thread's part of the row sum
+            for (int j = 0; j < n_tiles; ++j) {
+                ok = (kBreakOnAbort || ok) && wait_phase(bar_addr(&bars->s_full[t]), (gs0 + j) & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (kBreakOnAbort && !ok) break;
+                ptx::tc_fence_after_sync();
+                uint32_t s[kHalf];
+                const int kv0 = (it.jb + j) * kBN + hf * kHalf;   // key of column 0
+                // Keys past the end and, on diagonal tiles, keys after the row are masked.
+                const bool need_mask = kv0 + kHalf > p.S || (p.causal && kv0 + kHalf - 1 > r0);
+                const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
+                constexpr int kChains = 4;
+                float mx[kChains];
 #pragma unroll
-                for (int q = 0; q < kDH / 32; ++q) {
-                    uint32_t o[32];
-                    ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
-                    ptx::tmem_ld_wait();
-                    ptx::reg_fence<32>(o);
+                for (int i = 0; i < kChains; ++i) mx[i] = -INFINITY;
+                auto mask_max = [&](int k0, int k1) {
+                    if (need_mask) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                    ptx::tmem_st_32x32b_x32(tO + q * 32, o);
+                        for (int kq = k0; kq < k1; ++kq)
+                            if (kv0 + kq > last) s[kq] = __float_as_uint(-INFINITY);
+                    }
+#pragma unroll
+                    for (int kq = k0 / 2; kq < k1 / 2; ++kq)
+                        mx[kq % kChains] = ptx::fmax3(mx[kq % kChains], __uint_as_float(s[2 * kq]),
+                                                      __uint_as_float(s[2 * kq + 1]));
+                };
+#pragma unroll
+                for (int q = 0; q < kHalf / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence<kHalf>(s);
+                if (kSepP && (kBreakOnAbort || ok)) {
+                    // S_t is in registers: the next S_t may overwrite it
+                    ptx::tc_fence_before_sync();
+                    ptx::mbar_arrive(bar_addr(&bars->s_free[t]));
+                }
+                mask_max(0, kHalf);
+                float m_tile = mx[0];
+#pragma unroll
+                for (int i = 1; i < kChains; ++i) m_tile = fmaxf(m_tile, mx[i]);
+                if constexpr (kRowSplit > 1) {
+                    bars->row_max[j & 1][t][hf][r] = m_tile;
+                    ptx::named_barrier_sync(pair_bar, 32 * kRowSplit);
+                    m_tile = fmaxf(m_tile, bars->row_max[j & 1][t][hf ^ 1][r]);
+                }
+                const float m_new = fmaxf(m_use, m_tile);
+                // Lazy rescale: keep the old reference unless the max grew by more
+                // than kTauLog2 in log2 units (then p <= 2^kTauLog2).  The RS
+                // threads of a row see the same maxima, so they decide alike.
+                const bool rescale = (m_new - m_use) * c > kTauLog2;
+                float alpha = 1.f;
+                if (rescale) {
+                    alpha = ptx::ex2_approx((m_use - m_new) * c);
+                    m_use = m_new;
+                }
+                const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
+
+                // p = 2^(s*c - m*c), two columns per packed FMA / add
+                const float2 c2 = make_float2(c, c);
+                const float2 nmc2 = make_float2(-mc, -mc);
+                float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int q = 0; q < kHalf / 32; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int kq = 0; kq < 16; ++kq) {
+                        const float2 x = __ffma2_rn(
+                            make_float2(__uint_as_float(s[q * 32 + 2 * kq]),
+                                        __uint_as_float(s[q * 32 + 2 * kq + 1])),
+                            c2, nmc2);
+                        const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+                        sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
+                        pk[kq] = pack2<BF16>(pp.x, pp.y);
+                    }
+                    if (kSepP && q == 0 && j > 0 && ok) {
+                        // P_t and O_t are still read / written by P_t V of tile j-1
+                        ok = wait_phase(bar_addr(&bars->o_done[t]), (gs0 + j - 1) & 1, abort_flag);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (kBreakOnAbort && !ok) break;
+                        ptx::tc_fence_after_sync();
+                    }
+                    if (kBreakOnAbort || ok) ptx::tmem_st_32x32b_x16(tP + q * 16, pk);
+                }
+                if (kBreakOnAbort && !ok) break;
+                const float2 sum = __fadd2_rn(sum2[0], sum2[1]);
+                l = l * alpha + (sum.x + sum.y);
+
+                // O_t was last written by P V of tile j-1: with separate P its
+                // completion was awaited above; with P over S it completed before
+                // S_t of tile j (same issuing thread, in order).
+                if ((kBreakOnAbort || ok) && j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                    for (int q = 0; q < kDH / 32; ++q) {
+                        uint32_t o[32];
+                        ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence<32>(o);
+#pragma unroll
+                        for (int kq = 0; kq < 32; ++kq) o[kq] = __float_as_uint(__uint_as_float(o[kq]) * alpha);
+                        ptx::tmem_st_32x32b_x32(tO + q * 32, o);
+                    }
+                }
+                if (kBreakOnAbort || ok) {
+                    ptx::tmem_st_wait();
+                    ptx::tc_fence_before_sync();
+                    ptx::mbar_arrive(bar_addr(&bars->p_full[t]));
                 }
             }
-            if (kBreakOnAbort || ok) {
-                ptx::tmem_st_wait();
-                ptx::tc_fence_before_sync();
-                ptx::mbar_arrive(bar_addr(&bars->p_full[t]));
-            }
-        }
 
-        if (r0 < p.S) {
-            // --------------------------------------------------- epilogues
+            // ------------------------------------------------------- epilogue
+            // O_t is read out of TMEM (and waited for) before this thread's first
+            // P_t arrival of the next item, which the next item's first P_t V
+            // awaits: that orders its overwrite of O_t after these reads.
             bool eok = ok;
             if (n_tiles > 0)
-                eok = eok && wait_phase(bar_addr(&bars->o_done[t]), (n_tiles - 1) & 1, abort_flag);
+                eok = eok && wait_phase(bar_addr(&bars->o_done[t]), (gs0 + n_tiles - 1) & 1, abort_flag);
             eok = __all_sync(0xffffffffu, eok);
             // whole-row sum from the RS parts
             float l_row = l;
             if constexpr (kRowSplit > 1) {
-                bars->row_sum[t][hf][r] = l;
+                bars->row_sum[k & 1][t][hf][r] = l;
                 ptx::named_barrier_sync(pair_bar, 32 * kRowSplit);
-                l_row = l + bars->row_sum[t][hf ^ 1][r];
+                l_row = l + bars->row_sum[k & 1][t][hf ^ 1][r];
             }
-            if (partial) {
+            // With O staged in the Q buffer, this tile's store thread frees
+            // the buffer for the next item's Q.  A tile with no key tile has
+            // no product that orders its release after this item's Q load:
+            // it waits for that load first, so that the release counts for
+            // this item and not for the previous one.
+            auto release_q = [&]() {
+                if (n_tiles == 0 && !wait_phase(qbar, k & 1, abort_flag)) return;
+                ptx::mbar_arrive(bar_addr(&bars->q_empty));
+            };
+            if (it.partial && r0 < p.S) {
                 // partial result: o~ stays unnormalised (fp32), m and l go
                 // beside it; a tile that saw no key of this split records l = 0
                 const int ntq = (p.S + kBM - 1) / kBM;
-                const size_t slot = partial_slot(bh, ntq, r0 / kBM, p.max_splits, split);
+                const size_t slot = partial_slot(it.bh, ntq, r0 / kBM, p.max_splits, it.split);
                 float* ml = p.ws_ml + slot * (2 * kBM);
                 float4* po = reinterpret_cast<float4*>(p.ws_o + slot * static_cast<size_t>(kBM * D));
                 if (eok && n_tiles > 0) {
@@ -737,11 +862,16 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     ml[r] = -INFINITY;
                     ml[kBM + r] = 0.f;
                 }
+                if (kStageInQ && eok && store_thread) release_q();
             } else if (n_tiles > 0) {
-                // final result: stage O_t in this tile's Q buffer (no longer
-                // read by any MMA) as the 128-byte-swizzled TMA box, then one
-                // thread stores it; rows past S are dropped by the store
-                uint8_t* stage = smem + L::kOffQ + t * L::kQBytes;
+                // final result: stage O_t as the 128-byte-swizzled TMA box, then
+                // one thread stores it; rows past S are dropped by the store
+                uint8_t* stage = smem + L::kOffStage + t * L::kQBytes;
+                if (!kStageInQ && k > 0) {
+                    // the previous item's store must have read the staging buffer
+                    if (store_thread) ptx::bulk_wait_group_read_all();
+                    ptx::named_barrier_sync(tile_bar, kTileThreads);
+                }
                 const float inv_l = 1.f / l_row;
                 if (eok) {
                     ptx::tc_fence_after_sync();
@@ -771,20 +901,30 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     ptx::fence_proxy_async_smem();
                 }
                 const bool all_ok = ptx::named_barrier_and(tile_bar, kTileThreads, eok);
-                if (all_ok && r == 0 && hf == 0) {
+                if (all_ok && store_thread) {
                     for (int cch = 0; cch < kChunks; ++cch)
-                        ptx::tma_store_4d(&tmO, ptx::smem_addr(stage + cch * (kBM * 128)), cch * 64, h,
-                                          r0, b);
+                        ptx::tma_store_4d(&tmO, ptx::smem_addr(stage + cch * (kBM * 128)), cch * 64, it.h,
+                                          r0, it.b);
                     ptx::bulk_commit_group();
-                    ptx::bulk_wait_group_all();
+                    if (kStageInQ) {
+                        // the Q buffer may take the next item's Q once the store has read it
+                        ptx::bulk_wait_group_read_all();
+                        ptx::mbar_arrive(bar_addr(&bars->q_empty));
+                    }
                 }
                 if (all_ok && hf == 0 && p.lse != nullptr && row < p.S) {
                     // LSE = scale * m + ln l = ln2 * (m * scale * log2e + log2 l)
-                    p.lse[static_cast<size_t>(bh) * p.S + row] =
+                    p.lse[static_cast<size_t>(it.bh) * p.S + row] =
                         (m_use * c + log2f(l_row)) * 0.69314718055994530942f;
                 }
+            } else if (kStageInQ && store_thread) {
+                // no key tile for this query tile: its Q buffer was never loaded
+                release_q();
             }
+            gs0 += static_cast<uint32_t>(n_tiles);
         }
+        // every O store must be complete before the CTA exits
+        if (store_thread) ptx::bulk_wait_group_all();
     }
 
     ptx::tc_fence_before_sync();

@@ -104,6 +104,11 @@ __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
+// Wait until every committed bulk group has finished reading its shared
+// memory source (the writes to global memory may still be in flight).
+__device__ __forceinline__ void bulk_wait_group_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait_group_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }

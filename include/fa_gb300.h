@@ -34,7 +34,8 @@
  *                       an unknown dtype, or sizes whose element count
  *                       overflows 64 bits
  *   FA_ERR_UNSUPPORTED  D not in {64, 128}, a base address not 16-byte
- *                       aligned, or S / B*H beyond the launch limits
+ *                       aligned, ceil(S / 256) > 65535, or
+ *                       B * H * ceil(S / 256) > 2^31 - 1
  *   FA_ERR_CUDA         a CUDA runtime or driver call failed (the CUDA error
  *                       is left set for the caller to read)
  *   FA_ERR_TIMEOUT      reported by fa_device_status(): a device-side wait

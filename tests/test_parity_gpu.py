@@ -98,6 +98,26 @@ def test_split_kv_workspace_checks():
     assert fa.fa_splitkv_launches(4, 16, 4096, 64, True) == 1
 
 
+@pytest.mark.parametrize("B,H,S,D,dtype,causal", [
+    (2, 80, 600, 128, "bf16", True),    # ragged last block: its second query tile is empty
+    (2, 80, 600, 128, "bf16", False),
+    (2, 80, 600, 64, "f16", True),
+    (2, 100, 300, 64, "f16", False),
+    (4, 40, 512, 64, "f16", True),
+    (2, 40, 1000, 128, "f16", True),
+])
+def test_several_work_items_per_cta(B, H, S, D, dtype, causal):
+    """More query blocks than SMs: each CTA runs several items in turn, so
+    barrier phases, the K/V ring, the Q buffer and the O staging carry over
+    from one item to the next (including two ragged blocks in a row)."""
+    import attention_forward_fwd_gb300 as fa
+    import torch
+    items = B * H * ((S + 255) // 256)
+    assert items > torch.cuda.get_device_properties(0).multi_processor_count
+    assert fa.fa_splitkv_launches(B, H, S, D, causal) == 1
+    _full_case(B, H, S, D, dtype, "normal", 40 + S, causal)
+
+
 def test_many_heads_and_batches_layout():
     """[B, S, H, D] with H > 1 and B > 1: heads and batches land in place."""
     _full_case(3, 5, 200, 64, "f16", "normal", 6, False)
