@@ -180,8 +180,20 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.items = static_cast<int>(items);
     const int sms = num_sms();
     const long long ctas = (sms > 0 && items > sms) ? sms : items;
-    kern<<<dim3(static_cast<unsigned>(ctas)), fa::Roles<RS>::kThreads, kSmem, stream>>>(mq, mk, mv, mo, p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    // Programmatic dependent launch: the CTAs may start (barrier and TMEM
+    // set-up) while the previous kernel in the stream drains; the kernel
+    // waits for it before its first load.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t mcfg = {};
+    mcfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    mcfg.blockDim = dim3(fa::Roles<RS>::kThreads);
+    mcfg.dynamicSmemBytes = kSmem;
+    mcfg.stream = stream;
+    mcfg.attrs = pdl;
+    mcfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&mcfg, kern, mq, mk, mv, mo, p) != cudaSuccess) return FA_ERR_CUDA;
     if (plan.chunk == 0) return FA_OK;
 
     // merge the partials; programmatic dependent launch hides the launch gap

@@ -397,6 +397,11 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         ptx::tma_prefetch_map(&tmK);
         ptx::tma_prefetch_map(&tmV);
         ptx::tma_prefetch_map(&tmO);
+        // Launched as a programmatic dependent of the previous kernel in the
+        // stream, this CTA may have started before that kernel finished: it
+        // reads and writes global memory only after this wait (everything
+        // else in the CTA is ordered after it by the barriers and the sync).
+        ptx::grid_dependency_wait();
         const WorkItem it = decode_item(p, cta_item(0, p.items));   // the grid has <= items CTAs
         load_q(it);
         first_round = min(NS, 2 * it.nkv);
@@ -410,8 +415,9 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
-    // A dependent combine launch (split over keys) may be scheduled as soon
-    // as every CTA of this grid is running; it waits for this grid to finish.
+    // The next kernel in the stream (the combine launch of the split path, or
+    // the next call) may be scheduled as soon as every CTA of this grid is
+    // running; it waits for this grid to finish before touching memory.
     ptx::launch_dependents();
 
     // Each warpgroup changes its register budget with one instruction that
@@ -955,6 +961,9 @@ __global__ void __launch_bounds__(kCombineThreads) fa_combine_kernel(const FwdPa
     const int bh = blockIdx.y;
     const bool causal = p.causal != 0;
     const int ns = (key_tiles_for_block(qt / kQTiles, p.S, causal) + p.kv_chunk - 1) / p.kv_chunk;
+    // the next kernel in the stream may start its set-up now (it waits for
+    // this grid before touching memory)
+    ptx::launch_dependents();
     if (ns <= 1) return;   // this tile was written by the main kernel
     ptx::grid_dependency_wait();
     const int r = (blockIdx.x % kPerTile) * kRows + static_cast<int>(threadIdx.x) % kRows;
