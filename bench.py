@@ -89,8 +89,16 @@ def _traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """SM clock / clock-event-reason sampling while the timed region runs.
 
+    A thread reads NVML (libnvidia-ml through ctypes, read-only queries)
+    about every millisecond for the GPU with the CUDA device's UUID, so even a
+    region of a few milliseconds gets samples; nvidia-smi is the fallback.
+    """
+
+    # NVML clock-event reason bits
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -98,8 +106,52 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.rows = []
+        self.source = None
+        self._nvml = self._open_nvml()
+
+    def _open_nvml(self):
+        import ctypes
+        try:
+            import torch
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.gpu).uuid)
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                return None
+            get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:   # NVML_CLOCK_SM
+                return None
+            return dict(lib=lib, h=h, reasons=get_reasons, max=mx.value, c=ctypes)
+        except Exception:
+            return None
+
+    def _poll(self):
+        n = self._nvml
+        c, lib, h = n["c"], n["lib"], n["h"]
+        clk, pw, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        while not self._stop.is_set():
+            if (lib.nvmlDeviceGetClockInfo(h, 1, c.byref(clk)) == 0 and
+                    n["reasons"](h, c.byref(rs)) == 0):
+                lib.nvmlDeviceGetPowerUsage(h, c.byref(pw))
+                self.rows.append(dict(sm=float(clk.value), smax=float(n["max"]),
+                                      reasons=int(rs.value), power_w=pw.value / 1000.0))
+            time.sleep(0.001)
 
     def __enter__(self):
+        import threading
+        if self._nvml is not None:
+            self.source = "nvml"
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            time.sleep(0.005)       # a first sample before the region starts
+            return self
+        self.source = "nvidia-smi"
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
@@ -110,37 +162,47 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
+        if self.source == "nvml":
+            self._stop.set()
+            self._thread.join(timeout=5)
+            return
+        out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                out, _ = self.proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
-
-    def summary(self):
-        rows = []
-        for line in (self.out or "").splitlines():
+                out, _ = self.proc.communicate()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (out or "").splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
-                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                bits = 0
+                for name, flag in zip(names, parts[5:9]):
+                    if flag.lower() == "active":
+                        bits |= next(b for b, nm in self.REASONS.items() if nm == name)
+                self.rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), reasons=bits,
+                                      power_w=float(parts[3]) if parts[3] else 0.0))
             except ValueError:
                 continue
+
+    def summary(self):
+        rows = self.rows
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "source": self.source}
         reasons = set()
         for r in rows:
-            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
-                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
-                if r[key].lower() == "active":
+            for bit, name in self.REASONS.items():
+                if r["reasons"] & bit:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(r["sm"] for r in rows),
                 "sm_max_mhz": max(r["smax"] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power_w"] for r in rows), "source": self.source}
 
 
 def _dist_env():
