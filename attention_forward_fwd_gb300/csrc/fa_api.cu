@@ -65,6 +65,15 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int B, int S, int H, 
 #endif
 constexpr int kRowSplitD64 = FA_ROW_SPLIT_D64;
 constexpr int kRowSplitD128 = FA_ROW_SPLIT_D128;
+// K / V ring slots per head dimension
+#ifndef FA_RING_D64
+#define FA_RING_D64 6
+#endif
+#ifndef FA_RING_D128
+#define FA_RING_D128 4
+#endif
+constexpr int kRingD64 = FA_RING_D64;
+constexpr int kRingD128 = FA_RING_D128;
 
 int num_sms() {
     static int cached[64] = {0};
@@ -240,12 +249,12 @@ int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     // <head dim, bf16, K/V ring slots, softmax threads per query row>
     if (dtype == FA_F16) {
         if (D == 64)
-            return launch<64, false, 6, kRowSplitD64>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
-        return launch<128, false, 4, kRowSplitD128>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+            return launch<64, false, kRingD64, kRowSplitD64>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+        return launch<128, false, kRingD128, kRowSplitD128>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
     }
     if (D == 64)
-        return launch<64, true, 6, kRowSplitD64>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
-    return launch<128, true, 4, kRowSplitD128>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+        return launch<64, true, kRingD64, kRowSplitD64>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+    return launch<128, true, kRingD128, kRowSplitD128>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
 }
 
 }  // namespace

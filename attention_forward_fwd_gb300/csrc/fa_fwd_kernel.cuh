@@ -88,6 +88,7 @@ struct Roles : WarpLayout<RS> {
 };
 constexpr uint32_t kTmemCols = 512;
 constexpr float kTauLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
+constexpr float kMaxTileSum = 256.0f;  // 2^kTauLog2: a tile's row sum that keeps the reference
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 
 constexpr int kStatusTimeout = 4;
@@ -192,6 +193,7 @@ struct SmemLayout {
     static constexpr int kOffBar = kOffKV + NS * kKVBytes + (kStageInQ ? 0 : kQTiles * kQBytes);
     static constexpr int kBytes = kOffBar + static_cast<int>(sizeof(Barriers<NS, RS>));
     static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024
+    static_assert(kAlloc <= 232448, "shared memory beyond the 227 KiB a CTA may use");
 };
 
 // One work item: a query block of kQTiles*kBM rows of head (b, h) and the
@@ -708,6 +710,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
 
             float m_use = -INFINITY;   // reference max, raw (unscaled) score units
             float l = 0.f;             // this thread's part of the row sum
+            bool use_max_next = false; // the previous tile moved the reference
             for (int j = 0; j < n_tiles; ++j) {
                 ok = (kBreakOnAbort || ok) && wait_phase(bar_addr(&bars->s_full[t]), (gs0 + j) & 1, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
@@ -716,82 +719,192 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 uint32_t s[kHalf];
                 const int kv0 = (it.jb + j) * kBN + hf * kHalf;   // key of column 0
                 // Keys past the end and, on diagonal tiles, keys after the row are masked.
-                const bool need_mask = kv0 + kHalf > p.S || (p.causal && kv0 + kHalf - 1 > r0);
-                const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
-                constexpr int kChains = 4;
-                float mx[kChains];
+                float alpha = 1.f;
+                bool rescale = false;
+                if constexpr (kRowSplit == 1) {
+                    const bool need_mask = kv0 + kHalf > p.S || (p.causal && kv0 + kHalf - 1 > r0);
+                    const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
+                    constexpr int kChains = 4;
+                    float mx[kChains];
 #pragma unroll
-                for (int i = 0; i < kChains; ++i) mx[i] = -INFINITY;
-                auto mask_max = [&](int k0, int k1) {
+                    for (int i = 0; i < kChains; ++i) mx[i] = -INFINITY;
+                    auto mask_max = [&](int k0, int k1) {
+                        if (need_mask) {
+#pragma unroll
+                            for (int kq = k0; kq < k1; ++kq)
+                                if (kv0 + kq > last) s[kq] = __float_as_uint(-INFINITY);
+                        }
+#pragma unroll
+                        for (int kq = k0 / 2; kq < k1 / 2; ++kq)
+                            mx[kq % kChains] = ptx::fmax3(mx[kq % kChains], __uint_as_float(s[2 * kq]),
+                                                          __uint_as_float(s[2 * kq + 1]));
+                    };
+#pragma unroll
+                    for (int q = 0; q < kHalf / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence<kHalf>(s);
+                    if (kSepP && (kBreakOnAbort || ok)) {
+                        // S_t is in registers: the next S_t may overwrite it
+                        ptx::tc_fence_before_sync();
+                        ptx::mbar_arrive(bar_addr(&bars->s_free[t]));
+                    }
+                    mask_max(0, kHalf);
+                    float m_tile = mx[0];
+#pragma unroll
+                    for (int i = 1; i < kChains; ++i) m_tile = fmaxf(m_tile, mx[i]);
+                    if constexpr (kRowSplit > 1) {
+                        bars->row_max[j & 1][t][hf][r] = m_tile;
+                        ptx::named_barrier_sync(pair_bar, 32 * kRowSplit);
+                        m_tile = fmaxf(m_tile, bars->row_max[j & 1][t][hf ^ 1][r]);
+                    }
+                    const float m_new = fmaxf(m_use, m_tile);
+                    // Lazy rescale: keep the old reference unless the max grew by more
+                    // than kTauLog2 in log2 units (then p <= 2^kTauLog2).  The RS
+                    // threads of a row see the same maxima, so they decide alike.
+                    rescale = (m_new - m_use) * c > kTauLog2;
+                    if (rescale) {
+                        alpha = ptx::ex2_approx((m_use - m_new) * c);
+                        m_use = m_new;
+                    }
+                    const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
+
+                    // p = 2^(s*c - m*c), two columns per packed FMA / add
+                    const float2 c2 = make_float2(c, c);
+                    const float2 nmc2 = make_float2(-mc, -mc);
+                    float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int q = 0; q < kHalf / 32; ++q) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int kq = 0; kq < 16; ++kq) {
+                            const float2 x = __ffma2_rn(
+                                make_float2(__uint_as_float(s[q * 32 + 2 * kq]),
+                                            __uint_as_float(s[q * 32 + 2 * kq + 1])),
+                                c2, nmc2);
+                            const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+                            sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
+                            pk[kq] = pack2<BF16>(pp.x, pp.y);
+                        }
+                        if (kSepP && q == 0 && j > 0 && ok) {
+                            // P_t and O_t are still read / written by P_t V of tile j-1
+                            ok = wait_phase(bar_addr(&bars->o_done[t]), (gs0 + j - 1) & 1, abort_flag);
+                            ok = __all_sync(0xffffffffu, ok);
+                            if (kBreakOnAbort && !ok) break;
+                            ptx::tc_fence_after_sync();
+                        }
+                        if (kBreakOnAbort || ok) ptx::tmem_st_32x32b_x16(tP + q * 16, pk);
+                    }
+                    if (kBreakOnAbort && !ok) break;
+                    const float2 sum = __fadd2_rn(sum2[0], sum2[1]);
+                    l = l * alpha + (sum.x + sum.y);
+                } else {
+                    const bool need_mask = kv0 + kHalf > p.S || (p.causal && kv0 + kHalf - 1 > r0);
+                    const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
+#pragma unroll
+                    for (int q = 0; q < kHalf / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence<kHalf>(s);
+                    if (kSepP && (kBreakOnAbort || ok)) {
+                        // S_t is in registers: the next S_t may overwrite it
+                        ptx::tc_fence_before_sync();
+                        ptx::mbar_arrive(bar_addr(&bars->s_free[t]));
+                    }
                     if (need_mask) {
 #pragma unroll
-                        for (int kq = k0; kq < k1; ++kq)
+                        for (int kq = 0; kq < kHalf; ++kq)
                             if (kv0 + kq > last) s[kq] = __float_as_uint(-INFINITY);
                     }
-#pragma unroll
-                    for (int kq = k0 / 2; kq < k1 / 2; ++kq)
-                        mx[kq % kChains] = ptx::fmax3(mx[kq % kChains], __uint_as_float(s[2 * kq]),
-                                                      __uint_as_float(s[2 * kq + 1]));
-                };
-#pragma unroll
-                for (int q = 0; q < kHalf / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
-                ptx::tmem_ld_wait();
-                ptx::reg_fence<kHalf>(s);
-                if (kSepP && (kBreakOnAbort || ok)) {
-                    // S_t is in registers: the next S_t may overwrite it
-                    ptx::tc_fence_before_sync();
-                    ptx::mbar_arrive(bar_addr(&bars->s_free[t]));
-                }
-                mask_max(0, kHalf);
-                float m_tile = mx[0];
-#pragma unroll
-                for (int i = 1; i < kChains; ++i) m_tile = fmaxf(m_tile, mx[i]);
-                if constexpr (kRowSplit > 1) {
-                    bars->row_max[j & 1][t][hf][r] = m_tile;
-                    ptx::named_barrier_sync(pair_bar, 32 * kRowSplit);
-                    m_tile = fmaxf(m_tile, bars->row_max[j & 1][t][hf ^ 1][r]);
-                }
-                const float m_new = fmaxf(m_use, m_tile);
-                // Lazy rescale: keep the old reference unless the max grew by more
-                // than kTauLog2 in log2 units (then p <= 2^kTauLog2).  The RS
-                // threads of a row see the same maxima, so they decide alike.
-                const bool rescale = (m_new - m_use) * c > kTauLog2;
-                float alpha = 1.f;
-                if (rescale) {
-                    alpha = ptx::ex2_approx((m_use - m_new) * c);
-                    m_use = m_new;
-                }
-                const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
 
-                // p = 2^(s*c - m*c), two columns per packed FMA / add
-                const float2 c2 = make_float2(c, c);
-                const float2 nmc2 = make_float2(-mc, -mc);
-                float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    // One pass over this thread's columns: p = 2^(s*c - mc), two
+                    // columns per packed FMA / add, written to TMEM as packed 16-bit
+                    // P (with separate P, once P_t V of tile j-1 has released P_t).
+                    bool p_free = !(kSepP && j > 0);
+                    float sum = 0.f;
+                    auto exp_pass = [&](float mc) {
+                        const float2 c2 = make_float2(c, c);
+                        const float2 nmc2 = make_float2(-mc, -mc);
+                        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int q = 0; q < kHalf / 32; ++q) {
-                    uint32_t pk[16];
+                        for (int q = 0; q < kHalf / 32; ++q) {
+                            uint32_t pk[16];
 #pragma unroll
-                    for (int kq = 0; kq < 16; ++kq) {
-                        const float2 x = __ffma2_rn(
-                            make_float2(__uint_as_float(s[q * 32 + 2 * kq]),
-                                        __uint_as_float(s[q * 32 + 2 * kq + 1])),
-                            c2, nmc2);
-                        const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
-                        sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
-                        pk[kq] = pack2<BF16>(pp.x, pp.y);
+                            for (int kq = 0; kq < 16; ++kq) {
+                                const float2 x = __ffma2_rn(
+                                    make_float2(__uint_as_float(s[q * 32 + 2 * kq]),
+                                                __uint_as_float(s[q * 32 + 2 * kq + 1])),
+                                    c2, nmc2);
+                                const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+                                sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
+                                pk[kq] = pack2<BF16>(pp.x, pp.y);
+                            }
+                            if (!p_free && ok) {
+                                // P_t and O_t are still read / written by P_t V of tile j-1
+                                ok = wait_phase(bar_addr(&bars->o_done[t]), (gs0 + j - 1) & 1, abort_flag);
+                                ok = __all_sync(0xffffffffu, ok);
+                                if (ok) ptx::tc_fence_after_sync();
+                                p_free = true;
+                            }
+                            if (ok) ptx::tmem_st_32x32b_x16(tP + q * 16, pk);
+                        }
+                        const float2 s2 = __fadd2_rn(sum2[0], sum2[1]);
+                        sum = s2.x + s2.y;
+                    };
+
+                    // this tile's row max (the RS threads of a row swap their parts)
+                    auto tile_max = [&]() {
+                        constexpr int kChains = 4;
+                        float mx[kChains];
+#pragma unroll
+                        for (int i = 0; i < kChains; ++i) mx[i] = -INFINITY;
+#pragma unroll
+                        for (int kq = 0; kq < kHalf / 2; ++kq)
+                            mx[kq % kChains] = ptx::fmax3(mx[kq % kChains], __uint_as_float(s[2 * kq]),
+                                                          __uint_as_float(s[2 * kq + 1]));
+                        float m_tile = mx[0];
+#pragma unroll
+                        for (int i = 1; i < kChains; ++i) m_tile = fmaxf(m_tile, mx[i]);
+                        if constexpr (kRowSplit > 1) {
+                            bars->row_max[j & 1][t][hf][r] = m_tile;
+                            ptx::named_barrier_sync(pair_bar, 32 * kRowSplit);
+                            m_tile = fmaxf(m_tile, bars->row_max[j & 1][t][hf ^ 1][r]);
+                        }
+                        return m_tile;
+                    };
+                    {
+                        // With the row split the two threads of a row would swap
+                        // their maxima every tile.  Instead the exponentials are
+                        // first taken against the current reference: the lazy
+                        // rescale only has to move it when some p would exceed
+                        // 2^kTauLog2, and the row sum (p >= 0) bounds every p, so a
+                        // sum <= 2^kTauLog2 keeps the reference.  Otherwise (an
+                        // item's first tile, a failed check, or a previous tile that
+                        // moved the reference) the tile max comes first and the
+                        // reference moves up to it.  TMEM stores are warp-wide and
+                        // the two threads of a row share its reference, so the pair
+                        // of warps on these rows takes one path.
+                        bool with_max = (m_use == -INFINITY) || use_max_next;
+                        if (!with_max) {
+                            exp_pass(m_use * c);
+                            with_max = ptx::named_barrier_or(pair_bar, 32 * kRowSplit,
+                                                             !(sum <= kMaxTileSum));   // also inf / NaN
+                            if (with_max) ptx::tmem_st_wait();   // these P stores land first
+                        }
+                        if (with_max) {
+                            const float m_tile = tile_max();
+                            if (m_tile > m_use) {
+                                alpha = ptx::ex2_approx((m_use - m_tile) * c);   // 0 on the first tile
+                                m_use = m_tile;
+                                rescale = true;
+                            }
+                            exp_pass(m_use == -INFINITY ? 0.f : m_use * c);
+                        }
+                        // peaky scores keep raising the max: take it first next time
+                        // (both warps of the pair cover the same rows: same choice)
+                        use_max_next = __any_sync(0xffffffffu, rescale && j > 0);
                     }
-                    if (kSepP && q == 0 && j > 0 && ok) {
-                        // P_t and O_t are still read / written by P_t V of tile j-1
-                        ok = wait_phase(bar_addr(&bars->o_done[t]), (gs0 + j - 1) & 1, abort_flag);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (kBreakOnAbort && !ok) break;
-                        ptx::tc_fence_after_sync();
-                    }
-                    if (kBreakOnAbort || ok) ptx::tmem_st_32x32b_x16(tP + q * 16, pk);
+                    if (kBreakOnAbort && !ok) break;
+                    l = l * alpha + sum;
                 }
-                if (kBreakOnAbort && !ok) break;
-                const float2 sum = __fadd2_rn(sum2[0], sum2[1]);
-                l = l * alpha + (sum.x + sum.y);
 
                 // O_t was last written by P V of tile j-1: with separate P its
                 // completion was awaited above; with P over S it completed before

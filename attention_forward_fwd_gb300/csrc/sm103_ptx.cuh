@@ -62,6 +62,19 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier over `nthreads` threads that also returns the OR of `pred`
+// over them.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred P1, P2;\n\tsetp.ne.u32 P1, %1, 0;\n\t"
+        "bar.red.or.pred P2, %2, %3, P1;\n\tselp.u32 %0, 1, 0, P2;\n\t}"
+        : "=r"(out)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return out != 0;
+}
+
 // Named barrier over `nthreads` threads that also returns the AND of `pred`
 // over them.
 __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads, bool pred) {

@@ -68,6 +68,34 @@ def test_peaky_logits(causal, split_kv):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (128, "f16")])
+def test_peaky_logits_row_split(D, dtype, causal):
+    """Peaky scores at D = 128 (two threads per row), several work items per
+    CTA: the row sum often rules out the current reference max."""
+    _full_case(2, 100, 700, D, dtype, "stress", 6, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D,dtype", [(64, "f16"), (128, "bf16"), (128, "f16")])
+def test_rising_scores_move_the_reference(D, dtype, causal):
+    """Constant queries and keys that grow along the sequence: every key tile
+    lies a little above the previous one (about 2 log2 units per tile), so
+    each tile raises the row max by less than the lazy-rescale threshold
+    while its row sum exceeds 2^8 against the previous reference."""
+    B, H, S = 1, 3, 1024
+    rng = np.random.default_rng(12)
+    q = np.full((B, S, H, D), 0.5, dtype=np.float32)
+    ramp = (2.0 * np.arange(S) / S).astype(np.float32)
+    k = np.broadcast_to(ramp[None, :, None, None], (B, S, H, D))
+    v = rng.uniform(-1, 1, size=(B, S, H, D)).astype(np.float32)
+    qb, kb, vb = (fa_inputs.f32_to_bits(x, dtype) for x in (q, k, v))
+    scale = D ** -0.5
+    O, L = run_gpu(qb, kb, vb, dtype, causal, scale)
+    Oref, Lref = attention_reference(qb, kb, vb, dtype, causal, scale)
+    assert_close(O, L, Oref, Lref, dtype, f"rising D{D} {dtype} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("S,D,dtype", [(700, 64, "f16"), (1999, 64, "f16"), (2048, 128, "bf16"),
                                        (3000, 128, "f16"), (4096, 64, "bf16")])
 def test_split_kv_path_is_taken_and_exact(S, D, dtype, causal):
