@@ -16,7 +16,8 @@
 //                      score columns.  They also rescale O in TMEM when the
 //                      row max moves and run the epilogue of the tile.
 //   warps [4RS, 8RS)   the same for query tile 1 (rows q0+128 .. q0+255).
-//   warp  8RS          MMA issuer (one thread): S_t = Q_t K_j^T and
+//   warp  8RS          MMA issuer (the whole warp runs the loop, one
+//                      elected lane issues): S_t = Q_t K_j^T and
 //                      O_t += P_t V_j with tcgen05.mma, accumulators in TMEM;
 //                      allocates TMEM.  With separate P (below) it issues for
 //                      query tile 0 only and
@@ -422,20 +423,26 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     // running; it waits for this grid to finish before touching memory.
     ptx::launch_dependents();
 
+    // A bounded wait by every lane of a warp, with one outcome for the warp.
+    auto wait_warp = [&](uint32_t bar, uint32_t parity, bool honour_abort = true) {
+        return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, honour_abort));
+    };
+
     // Each warpgroup changes its register budget with one instruction that
     // dominates all of its role code (ptxas allocates each region for it).
     if (warp >= kMmaWarp) {
         ptx::setmaxnreg_dec<R::kControlRegs>();
         if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        // The whole warp runs the loop and the waits; lane 0 issues the copies.
+        {
             long long gi = 0;   // ring items issued, all items
             int k_q = 0;        // last item whose Q was loaded
             bool ok = true;
             // ring item gi goes to slot gi % NS once the item NS before it released it
             auto slot_free = [&](long long g) {
-                return g < NS || wait_phase(bar_addr(&bars->kv_empty[g % NS]),
-                                            static_cast<uint32_t>((g / NS - 1) & 1), abort_flag);
+                return g < NS ||
+                       wait_warp(bar_addr(&bars->kv_empty[g % NS]), static_cast<uint32_t>((g / NS - 1) & 1));
             };
             for (int k = 0; ok; ++k) {
                 const int w = cta_item(k, p.items);
@@ -444,8 +451,9 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 const int n = 2 * it.nkv;
                 int i = 0;
                 if (k == 0) {
-                    i = first_round;   // loaded before the sync, after the Q
-                    gi = first_round;
+                    // loaded before the sync, after the Q
+                    i = __shfl_sync(0xffffffffu, first_round, 0);
+                    gi = i;
                 } else {
                     // With O staged in the Q buffer, the Q of this item waits
                     // for the previous item's epilogue: load the K / V tiles
@@ -453,35 +461,35 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     const int pre = kStageInQ ? min(NS, n) : 0;
                     for (; i < pre; ++i, ++gi) {
                         if (!(ok = slot_free(gi))) break;
-                        load_item(it, i, static_cast<int>(gi % NS));
+                        if (lane == 0) load_item(it, i, static_cast<int>(gi % NS));
                     }
                     if (!ok) break;
-                    if (!(ok = wait_phase(bar_addr(&bars->q_empty), (k - 1) & 1, abort_flag))) break;
-                    load_q(it);
+                    if (!(ok = wait_warp(bar_addr(&bars->q_empty), (k - 1) & 1))) break;
+                    if (lane == 0) load_q(it);
                     k_q = k;
                 }
                 for (; i < n; ++i, ++gi) {
                     if (!(ok = slot_free(gi))) break;
-                    load_item(it, i, static_cast<int>(gi % NS));
+                    if (lane == 0) load_item(it, i, static_cast<int>(gi % NS));
                 }
             }
             if (*abort_flag) {
-                // Let every copy this thread started land before the CTA exits.
-                wait_phase(qbar, k_q & 1, abort_flag, false);
+                // Let every copy this warp started land before the CTA exits.
+                wait_warp(qbar, k_q & 1, false);
                 for (long long i = (gi > NS ? gi - NS : 0); i < gi; ++i)
-                    wait_phase(bar_addr(&bars->kv_full[i % NS]), static_cast<uint32_t>((i / NS) & 1),
-                               abort_flag, false);
+                    wait_warp(bar_addr(&bars->kv_full[i % NS]), static_cast<uint32_t>((i / NS) & 1), false);
             }
         }
     } else if (kSepP && (warp == kMmaWarp || warp == kMmaWarp1)) {
         // ------------------------------------------- MMA issuers (separate P)
-        // One issuing thread per query tile, so that each tile's products
-        // wait only on its own softmax.  Both issuers see every K / V tile of
+        // One issuing warp per query tile, so that each tile's products wait
+        // only on its own softmax; the whole warp runs the loop and one
+        // elected lane issues the MMAs and commits.  Both issuers see every K / V tile of
         // the ring in the same order and release each slot once (a commit
         // after the products that read it, or a plain arrive once it has
         // landed when this tile has no work on it), and each releases the Q
         // buffer of an item once its last S_t has been computed.
-        if (lane == 0) {
+        {
             const int t = (warp == kMmaWarp) ? 0 : 1;
             constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
             constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, D, BF16, true);
@@ -503,10 +511,10 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-                    ptx::mma_ss(tmem + t * kBN, a0 + (oa >> 4), b0 + (ob >> 4), kIdescQK, kk > 0);
+                    ptx::mma_ss_warp(tmem + t * kBN, a0 + (oa >> 4), b0 + (ob >> 4), kIdescQK, kk > 0);
                 }
-                ptx::tc_commit(s_full);
-                ptx::tc_commit(bar_addr(&bars->kv_empty[ring % NS]));
+                ptx::tc_commit_warp(s_full);
+                ptx::tc_commit_warp(bar_addr(&bars->kv_empty[ring % NS]));
             };
             // O_t (+)= P_t V over the tile's keys in K=16 steps; P from TMEM,
             // V MN-major (64-column chunks kBN*128 bytes apart).
@@ -514,17 +522,17 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), kBN * 128, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + p_col(t, kk),
-                                b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                    ptx::mma_ts_warp(tmem + 2 * kBN + t * D, tmem + p_col(t, kk),
+                                     b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
-                ptx::tc_commit(o_done);
-                ptx::tc_commit(bar_addr(&bars->kv_empty[ring % NS]));
+                ptx::tc_commit_warp(o_done);
+                ptx::tc_commit_warp(bar_addr(&bars->kv_empty[ring % NS]));
             };
             // wait for item `ring` to land; release it at once when `use` is false
             auto acquire = [&](int ring, bool use) {
-                if (!wait_phase(full_bar(ring), full_par(ring), abort_flag)) return false;
+                if (!wait_warp(full_bar(ring), full_par(ring))) return false;
                 if (use) ptx::tc_fence_after_sync();
-                else ptx::mbar_arrive(bar_addr(&bars->kv_empty[ring % NS]));
+                else ptx::mbar_arrive_warp(bar_addr(&bars->kv_empty[ring % NS]));
                 return true;
             };
 
@@ -539,19 +547,19 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 const int n_t = (t == 0) ? it.nkv0 : it.nkv1;
                 const uint32_t gs0 = gs;   // S_t / P_t / P_t V index of this item's key tile 0
                 // every issuer waits for every Q load, so that its phases stay in step
-                if (!(ok = wait_phase(qbar, k & 1, abort_flag))) break;
+                if (!(ok = wait_warp(qbar, k & 1))) break;
                 if (!(ok = acquire(gi0 + ring_k(0, nkv), n_t > 0))) break;
                 if (n_t > 0) {
                     // S_t of the previous item must have been read by the softmax
-                    if (gs > 0 && !(ok = wait_phase(s_free, (gs - 1) & 1, abort_flag))) break;
+                    if (gs > 0 && !(ok = wait_warp(s_free, (gs - 1) & 1))) break;
                     ptx::tc_fence_after_sync();
                     issue_s(gi0 + ring_k(0, nkv));
                     ++gs;
                 }
                 // the Q buffer of tile t is free once its last S_t is complete
                 if (n_t <= 1) {
-                    if (n_t == 1) ptx::tc_commit(q_empty);
-                    else ptx::mbar_arrive(q_empty);
+                    if (n_t == 1) ptx::tc_commit_warp(q_empty);
+                    else ptx::mbar_arrive_warp(q_empty);
                 }
                 for (int j = 0; ok && j < nkv; ++j) {
                     // S_t(j+1) as soon as the softmax holds S_t(j), then P_t V(j)
@@ -559,18 +567,18 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                         const bool use = (j + 1) < n_t;
                         if (!(ok = acquire(gi0 + ring_k(j + 1, nkv), use))) break;
                         if (use) {
-                            if (!(ok = wait_phase(s_free, (gs - 1) & 1, abort_flag))) break;
+                            if (!(ok = wait_warp(s_free, (gs - 1) & 1))) break;
                             ptx::tc_fence_after_sync();
                             issue_s(gi0 + ring_k(j + 1, nkv));
                             ++gs;
-                            if (j + 2 == n_t) ptx::tc_commit(q_empty);
+                            if (j + 2 == n_t) ptx::tc_commit_warp(q_empty);
                         }
                     }
                     if (!(ok = acquire(gi0 + ring_v(j, nkv), j < n_t))) break;
                     if (j < n_t) {
                         // P_t(j) written; it also orders this item's first
                         // P_t V after the previous epilogue's reads of O_t
-                        if (!(ok = wait_phase(p_full, (gs0 + j) & 1, abort_flag))) break;
+                        if (!(ok = wait_warp(p_full, (gs0 + j) & 1))) break;
                         ptx::tc_fence_after_sync();
                         issue_pv(gi0 + ring_v(j, nkv), j > 0);
                     }
@@ -578,17 +586,18 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 gi0 = (gi0 + 2 * nkv) % (2 * NS);
             }
             // Every MMA of this issuer must be complete before TMEM is freed.
-            ptx::tc_commit(bar_addr(&bars->drain[t]));
-            wait_phase(bar_addr(&bars->drain[t]), 0, abort_flag, false);
+            ptx::tc_commit_warp(bar_addr(&bars->drain[t]));
+            wait_warp(bar_addr(&bars->drain[t]), 0, false);
         }
     } else if (!kSepP && warp == kMmaWarp) {
         // ----------------------------------------------- MMA issuer (P over S)
-        // One thread issues both tiles' products in the order
+        // One warp (one elected lane issuing) runs both tiles' products in
+        // the order
         //   S0(0) S1(0) | P0V(j) S0(j+1) P1V(j) S1(j+1) | ...
         // so that one tile's softmax runs while the other tile's products do;
         // S_t(j+1) follows P_t V(j), which reads the P_t it overwrites.  The
         // next item's S_t(0) follows this item's last P_t V the same way.
-        if (lane == 0) {
+        {
             constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
             constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, D, BF16, true);
             auto full_bar = [&](int i) { return bar_addr(&bars->kv_full[i % NS]); };
@@ -601,18 +610,18 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-                    ptx::mma_ss(tmem + t * kBN, a0 + (oa >> 4), b0 + (ob >> 4), kIdescQK, kk > 0);
+                    ptx::mma_ss_warp(tmem + t * kBN, a0 + (oa >> 4), b0 + (ob >> 4), kIdescQK, kk > 0);
                 }
-                ptx::tc_commit(bar_addr(&bars->s_full[t]));
+                ptx::tc_commit_warp(bar_addr(&bars->s_full[t]));
             };
             auto issue_pv = [&](int t, int ring, bool acc) {
                 const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), kBN * 128, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + p_col(t, kk),
-                                b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                    ptx::mma_ts_warp(tmem + 2 * kBN + t * D, tmem + p_col(t, kk),
+                                     b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
-                ptx::tc_commit(bar_addr(&bars->o_done[t]));
+                ptx::tc_commit_warp(bar_addr(&bars->o_done[t]));
             };
 
             int gi0 = 0;                   // ring position of the item's K0, modulo 2*NS
@@ -624,45 +633,45 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 const WorkItem it = decode_item(p, w);
                 const int nkv = it.nkv, nkv0 = it.nkv0, nkv1 = it.nkv1;
                 const uint32_t g00 = gs[0], g10 = gs[1];
-                if (!(ok = wait_phase(qbar, k & 1, abort_flag))) break;
+                if (!(ok = wait_warp(qbar, k & 1))) break;
                 const int k0 = gi0 + ring_k(0, nkv);
-                if (!(ok = wait_phase(full_bar(k0), full_par(k0), abort_flag))) break;
+                if (!(ok = wait_warp(full_bar(k0), full_par(k0)))) break;
                 ptx::tc_fence_after_sync();
                 if (nkv0 > 0) issue_s(0, k0);
                 if (nkv1 > 0) issue_s(1, k0);
-                ptx::tc_commit(bar_addr(&bars->kv_empty[k0 % NS]));
+                ptx::tc_commit_warp(bar_addr(&bars->kv_empty[k0 % NS]));
                 for (int j = 0; ok && j < nkv; ++j) {
                     const int iv = gi0 + ring_v(j, nkv);
                     const int ik = gi0 + ring_k(j + 1, nkv);
                     const bool next = (j + 1) < nkv;
-                    if (!(ok = wait_phase(full_bar(iv), full_par(iv), abort_flag))) break;
+                    if (!(ok = wait_warp(full_bar(iv), full_par(iv)))) break;
                     ptx::tc_fence_after_sync();
                     if (j < nkv0) {
-                        if (!(ok = wait_phase(bar_addr(&bars->p_full[0]), (g00 + j) & 1, abort_flag))) break;
+                        if (!(ok = wait_warp(bar_addr(&bars->p_full[0]), (g00 + j) & 1))) break;
                         ptx::tc_fence_after_sync();
                         issue_pv(0, iv, j > 0);
                     }
                     if (next) {
-                        if (!(ok = wait_phase(full_bar(ik), full_par(ik), abort_flag))) break;
+                        if (!(ok = wait_warp(full_bar(ik), full_par(ik)))) break;
                         ptx::tc_fence_after_sync();
                     }
                     if (j + 1 < nkv0) issue_s(0, ik);
                     if (j < nkv1) {
-                        if (!(ok = wait_phase(bar_addr(&bars->p_full[1]), (g10 + j) & 1, abort_flag))) break;
+                        if (!(ok = wait_warp(bar_addr(&bars->p_full[1]), (g10 + j) & 1))) break;
                         ptx::tc_fence_after_sync();
                         issue_pv(1, iv, j > 0);
                     }
-                    ptx::tc_commit(bar_addr(&bars->kv_empty[iv % NS]));
+                    ptx::tc_commit_warp(bar_addr(&bars->kv_empty[iv % NS]));
                     if (j + 1 < nkv1) issue_s(1, ik);
-                    if (next) ptx::tc_commit(bar_addr(&bars->kv_empty[ik % NS]));
+                    if (next) ptx::tc_commit_warp(bar_addr(&bars->kv_empty[ik % NS]));
                 }
                 gs[0] += nkv0;
                 gs[1] += nkv1;
                 gi0 = (gi0 + 2 * nkv) % (2 * NS);
             }
             // Every MMA must be complete before TMEM is freed.
-            ptx::tc_commit(bar_addr(&bars->drain[0]));
-            wait_phase(bar_addr(&bars->drain[0]), 0, abort_flag, false);
+            ptx::tc_commit_warp(bar_addr(&bars->drain[0]));
+            wait_warp(bar_addr(&bars->drain[0]), 0, false);
         }
     }
     } else {

@@ -256,6 +256,47 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// Issue forms for a whole converged warp: every lane runs the issuing code
+// (so that descriptors and loop state are warp-uniform), one lane elected by
+// elect.sync issues the instruction.  With all 32 lanes active the elected
+// lane is the same every time, so its commits track the MMAs it issued.
+// (Issuing from a loop that only lane 0 runs was measured to slow the tensor
+// pipe to 88-123 cycles per M128 N128 K16 MMA when the SM sub-partition also
+// runs busy warps, against 64 cycles from a converged warp.)
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred E, P1;\n\telect.sync _|E, 0xffffffff;\n\t"
+        "setp.ne.b32 P1, %4, 0;\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, P1;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred E, P1;\n\telect.sync _|E, 0xffffffff;\n\t"
+        "setp.ne.b32 P1, %4, 0;\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, P1;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred E;\n\telect.sync _|E, 0xffffffff;\n\t"
+        "@E tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred E;\n\telect.sync _|E, 0xffffffff;\n\t"
+        "@E mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem], one K=16 step (A read from tensor memory).
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
