@@ -168,6 +168,7 @@ struct Barriers {
     uint64_t s_full[kQTiles];
     uint64_t s_free[kQTiles];   // S_t read into registers (separate-P schedule)
     uint64_t p_full[kQTiles];
+    uint64_t p_half[kQTiles];   // separate P: the first half of P_t (keys 0..63) is stored
     uint64_t o_done[kQTiles];
     uint64_t drain[kQTiles];
     uint32_t tmem_base;
@@ -391,6 +392,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             ptx::mbar_init(bar_addr(&bars->s_full[t]), 1);
             ptx::mbar_init(bar_addr(&bars->s_free[t]), kTileThreads);
             ptx::mbar_init(bar_addr(&bars->p_full[t]), kTileThreads);
+            ptx::mbar_init(bar_addr(&bars->p_half[t]), kTileThreads);
             ptx::mbar_init(bar_addr(&bars->o_done[t]), 1);
             ptx::mbar_init(bar_addr(&bars->drain[t]), 1);
         }
@@ -516,17 +518,16 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 ptx::tc_commit_warp(s_full);
                 ptx::tc_commit_warp(bar_addr(&bars->kv_empty[ring % NS]));
             };
-            // O_t (+)= P_t V over the tile's keys in K=16 steps; P from TMEM,
-            // V MN-major (64-column chunks kBN*128 bytes apart).
-            auto issue_pv = [&](int ring, bool acc) {
+            // O_t (+)= P_t V over the keys [kk0*16, kk1*16) of the tile in
+            // K=16 steps; P from TMEM, V MN-major (64-column chunks kBN*128
+            // bytes apart).
+            auto issue_pv = [&](int ring, bool acc, int kk0, int kk1) {
                 const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), kBN * 128, 1024);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
+                for (int kk = kk0; kk < kk1; ++kk) {
                     ptx::mma_ts_warp(tmem + 2 * kBN + t * D, tmem + p_col(t, kk),
                                      b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
-                ptx::tc_commit_warp(o_done);
-                ptx::tc_commit_warp(bar_addr(&bars->kv_empty[ring % NS]));
             };
             // wait for item `ring` to land; release it at once when `use` is false
             auto acquire = [&](int ring, bool use) {
@@ -576,11 +577,20 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     }
                     if (!(ok = acquire(gi0 + ring_v(j, nkv), j < n_t))) break;
                     if (j < n_t) {
-                        // P_t(j) written; it also orders this item's first
-                        // P_t V after the previous epilogue's reads of O_t
+                        // P_t V(j) in two halves: the first 64 keys as soon as
+                        // the softmax has stored their P (and rescaled O_t if it
+                        // had to), the rest once all of P_t(j) is written.  This
+                        // also orders the item's first P_t V after the previous
+                        // epilogue's reads of O_t.
+                        const int ring = gi0 + ring_v(j, nkv);
+                        if (!(ok = wait_warp(bar_addr(&bars->p_half[t]), (gs0 + j) & 1))) break;
+                        ptx::tc_fence_after_sync();
+                        issue_pv(ring, j > 0, 0, kBN / 32);
                         if (!(ok = wait_warp(p_full, (gs0 + j) & 1))) break;
                         ptx::tc_fence_after_sync();
-                        issue_pv(gi0 + ring_v(j, nkv), j > 0);
+                        issue_pv(ring, true, kBN / 32, kBN / 16);
+                        ptx::tc_commit_warp(o_done);
+                        ptx::tc_commit_warp(bar_addr(&bars->kv_empty[ring % NS]));
                     }
                 }
                 gi0 = (gi0 + 2 * nkv) % (2 * NS);
@@ -800,8 +810,28 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                             ok = __all_sync(0xffffffffu, ok);
                             if (kBreakOnAbort && !ok) break;
                             ptx::tc_fence_after_sync();
+                            // O_t is rescaled before any of P_t V(j) can start
+                            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                                for (int q2 = 0; q2 < kDH / 32; ++q2) {
+                                    uint32_t o[32];
+                                    ptx::tmem_ld_32x32b_x32(tO + q2 * 32, o);
+                                    ptx::tmem_ld_wait();
+                                    ptx::reg_fence<32>(o);
+#pragma unroll
+                                    for (int u = 0; u < 32; ++u)
+                                        o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+                                    ptx::tmem_st_32x32b_x32(tO + q2 * 32, o);
+                                }
+                            }
                         }
                         if (kBreakOnAbort || ok) ptx::tmem_st_32x32b_x16(tP + q * 16, pk);
+                        if (kSepP && q == (kHalf / 32) / 2 - 1 && (kBreakOnAbort || ok)) {
+                            // the first half of P_t(j) may be read
+                            ptx::tmem_st_wait();
+                            ptx::tc_fence_before_sync();
+                            ptx::mbar_arrive(bar_addr(&bars->p_half[t]));
+                        }
                     }
                     if (kBreakOnAbort && !ok) break;
                     const float2 sum = __fadd2_rn(sum2[0], sum2[1]);
@@ -918,7 +948,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 // O_t was last written by P V of tile j-1: with separate P its
                 // completion was awaited above; with P over S it completed before
                 // S_t of tile j (same issuing thread, in order).
-                if ((kBreakOnAbort || ok) && j > 0 && __any_sync(0xffffffffu, rescale)) {
+                if ((kBreakOnAbort || ok) && j > 0 && !(kSepP && kRowSplit == 1) &&
+                    __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
                     for (int q = 0; q < kDH / 32; ++q) {
                         uint32_t o[32];
@@ -933,6 +964,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 if (kBreakOnAbort || ok) {
                     ptx::tmem_st_wait();
                     ptx::tc_fence_before_sync();
+                    // with the row split all of P_t is released at once
+                    if (kSepP && kRowSplit > 1) ptx::mbar_arrive(bar_addr(&bars->p_half[t]));
                     ptx::mbar_arrive(bar_addr(&bars->p_full[t]));
                 }
             }
