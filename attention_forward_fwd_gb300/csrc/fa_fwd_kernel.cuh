@@ -1134,17 +1134,24 @@ __global__ void __launch_bounds__(kCombineThreads) fa_combine_kernel(const FwdPa
     constexpr size_t kSlotMl = 2 * kBM;
     constexpr size_t kSlotO = static_cast<size_t>(kBM) * D / 4;   // float4 per slot
 
-    float M = -INFINITY;
+    // The loads of every split's (m, l) and o~ chunk are independent of one
+    // another: issue them all before any of the arithmetic (one L2 round trip).
+    const float4* pa = po0 + (2 * cchunk) * kBM + r;
     float msp[kCombineMaxSplits], lsp[kCombineMaxSplits];
+    float4 xo[kCombineMaxSplits], yo[kCombineMaxSplits];
 #pragma unroll
     for (int s = 0; s < kCombineMaxSplits; ++s) {
         msp[s] = -INFINITY;
         lsp[s] = 0.f;
+        xo[s] = yo[s] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (s < ns) {
             msp[s] = ml0[s * kSlotMl + r];
             lsp[s] = ml0[s * kSlotMl + kBM + r];
+            xo[s] = pa[s * kSlotO];
+            yo[s] = pa[s * kSlotO + kBM];
         }
     }
+    float M = -INFINITY;
     for (int s = kCombineMaxSplits; s < ns; ++s)
         if (ml0[s * kSlotMl + kBM + r] > 0.f) M = fmaxf(M, ml0[s * kSlotMl + r]);
 #pragma unroll
@@ -1163,14 +1170,13 @@ __global__ void __launch_bounds__(kCombineThreads) fa_combine_kernel(const FwdPa
     }
     const float inv_l = 1.f / Lsum;
 
+    // a split that saw no key wrote no o~ (its chunk is not read into the sum)
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const float4* pa = po0 + (2 * cchunk) * kBM + r;
 #pragma unroll
     for (int s = 0; s < kCombineMaxSplits; ++s) {
-        if (s < ns && msp[s] > 0.f) {
-            const float4 x = pa[s * kSlotO];
-            const float4 y = pa[s * kSlotO + kBM];
+        if (msp[s] > 0.f) {
             const float w = msp[s];
+            const float4 x = xo[s], y = yo[s];
             acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
             acc[4] += w * y.x; acc[5] += w * y.y; acc[6] += w * y.z; acc[7] += w * y.w;
         }
