@@ -84,23 +84,25 @@ def f32_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
 
 def make_qkv(B: int, H: int, S: int, D: int, dtype: str = "f16",
              dist: str = "normal", seed: int = 0,
-             identical_key_head: tuple = ()):
+             identical_key_head: tuple = (), h_kv: int | None = None):
     """Draw Q, K, V as uint16 bit arrays of shape [B, S, H, D].
 
     dist="normal": Q, K, V iid N(0, 1).
     dist="stress": Q, K = 4 * N(0, 1) (peaky softmax), V ~ U[-1, 1].
     identical_key_head=(b, h): every key row of that head is set to its row 0.
+    h_kv: K and V get h_kv heads ([B, S, h_kv, D]) instead of H.
     """
     rng = np.random.default_rng(seed)
     shape = (B, S, H, D)
+    kv_shape = shape if h_kv is None else (B, S, h_kv, D)
     q = rng.standard_normal(shape, dtype=np.float32)
-    k = rng.standard_normal(shape, dtype=np.float32)
+    k = rng.standard_normal(kv_shape, dtype=np.float32)
     if dist == "normal":
-        v = rng.standard_normal(shape, dtype=np.float32)
+        v = rng.standard_normal(kv_shape, dtype=np.float32)
     elif dist == "stress":
         q *= 4.0
         k *= 4.0
-        v = rng.uniform(-1.0, 1.0, size=shape).astype(np.float32)
+        v = rng.uniform(-1.0, 1.0, size=kv_shape).astype(np.float32)
     else:
         raise ValueError(f"unknown dist {dist!r}")
     if identical_key_head:

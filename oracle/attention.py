@@ -44,6 +44,10 @@ Readings where the pages are silent
 * layout: [B, S, H, D] for Q, K, V, O; LSE is [B, H, S].
 * padded keys (j >= S) do not exist in the definition; every row has at least
   one visible key (j = 0), so no row is empty.
+* grouped K/V heads (not on the pages; the production extension listed with
+  the contract): K and V may have H_kv heads with H_kv dividing H; query head
+  h then uses K/V head h // (H / H_kv), consecutive query heads sharing one
+  K/V head (H_kv = 1: one K/V head for all).
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (closed forms, invariants, library routines, brute force and hand-derived
@@ -117,9 +121,16 @@ def _rows_one_head(q, k, v, rows, causal, scale):
     return o, lse
 
 
+def _kv_group(H: int, H_kv: int) -> int:
+    """Query heads per K/V head (H_kv must divide H)."""
+    if H_kv < 1 or H % H_kv != 0:
+        raise ValueError(f"{H_kv} K/V heads do not divide {H} query heads")
+    return H // H_kv
+
+
 def attention_reference_f64(q, k, v, causal: bool, scale: float,
                             row_block: int = 512):
-    """Definition on float64 arrays q, k, v of shape [B, S, H, D].
+    """Definition on float64 arrays q [B, S, H, D] and k, v [B, S, H_kv, D].
 
     Returns (O [B, S, H, D] float64, LSE [B, H, S] float64).
     """
@@ -127,11 +138,13 @@ def attention_reference_f64(q, k, v, causal: bool, scale: float,
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     B, S, H, D = q.shape
+    group = _kv_group(H, k.shape[2])
     O = np.empty((B, S, H, v.shape[3]), dtype=np.float64)
     LSE = np.empty((B, H, S), dtype=np.float64)
     for b in range(B):
         for h in range(H):
-            qh, kh, vh = q[b, :, h, :], k[b, :, h, :], v[b, :, h, :]
+            hk = h // group                              # the K/V head of query head h
+            qh, kh, vh = q[b, :, h, :], k[b, :, hk, :], v[b, :, hk, :]
             for r0 in range(0, S, row_block):
                 rows = np.arange(r0, min(S, r0 + row_block))
                 o, lse = _rows_one_head(qh, kh, vh, rows, causal, scale)
@@ -153,9 +166,10 @@ def attention_rows(qb, kb, vb, dtype: str, causal: bool, scale: float,
     Returns (O [len(rows), D], LSE [len(rows)]) in float64.
     """
     rows = np.asarray(rows, dtype=np.int64)
+    hk = h // _kv_group(qb.shape[2], kb.shape[2])
     qh = decode(qb[b, :, h, :], dtype)
-    kh = decode(kb[b, :, h, :], dtype)
-    vh = decode(vb[b, :, h, :], dtype)
+    kh = decode(kb[b, :, hk, :], dtype)
+    vh = decode(vb[b, :, hk, :], dtype)
     return _rows_one_head(qh, kh, vh, rows, causal, scale)
 
 

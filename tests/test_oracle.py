@@ -435,3 +435,56 @@ def test_pins_catch_planted_mistakes(kind):
 @pytest.mark.parametrize("kind", ["o_not_rescaled", "l_not_rescaled"])
 def test_pins_catch_planted_recurrence_mistakes(kind):
     assert _fails_some_pin(_online_mutant(kind)), kind
+
+
+# ------------------------------------------------------ grouped K/V heads
+# Reading (not on the pages): with H_kv K/V heads, query head h uses K/V head
+# h // (H / H_kv).  The pins below fix that grouping and reduce the grouped
+# call to the single-head definition pinned above.
+
+def test_grouped_heads_constant_values_pick_the_group():
+    """V constant per K/V head (head j holds (j + 1) / 4 everywhere): every
+    output of query head h equals the constant of its group's K/V head, which
+    distinguishes h // group from any other assignment (h mod H_kv, ...)."""
+    B, H, H_kv, S, D = 1, 6, 3, 37, 64
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((B, S, H, D))
+    k = rng.standard_normal((B, S, H_kv, D))
+    v = np.empty((B, S, H_kv, D))
+    for j in range(H_kv):
+        v[:, :, j, :] = (j + 1) / 4.0
+    for causal in (False, True):
+        O, _ = attention_reference_f64(q, k, v, causal, 0.125)
+        for h in range(H):
+            want = (h // (H // H_kv) + 1) / 4.0
+            assert np.abs(O[:, :, h, :] - want).max() < 1e-12, (h, causal)
+
+
+@pytest.mark.parametrize("H,H_kv", [(4, 4), (4, 2), (6, 1), (8, 2)])
+def test_grouped_heads_equal_single_head_calls(H, H_kv):
+    """Each query head of a grouped call equals the single-head definition
+    called on that head and its K/V head (MQA when H_kv = 1, MHA when equal)."""
+    qb, kb, vb = fa_inputs.make_qkv(2, H, 45, 64, "f16", "normal", 22, h_kv=H_kv)
+    for causal in (False, True):
+        O, L = attention_reference(qb, kb, vb, "f16", causal, 0.125)
+        for h in range(H):
+            hk = h * H_kv // H
+            o1, l1 = attention_reference(qb[:, :, h:h + 1], kb[:, :, hk:hk + 1], vb[:, :, hk:hk + 1],
+                                         "f16", causal, 0.125)
+            assert np.array_equal(O[:, :, h:h + 1], o1) and np.array_equal(L[:, h:h + 1], l1)
+
+
+def test_grouped_heads_rows_match_full_reference():
+    qb, kb, vb = fa_inputs.make_qkv(1, 8, 70, 64, "bf16", "stress", 23, h_kv=2)
+    O, L = attention_reference(qb, kb, vb, "bf16", True, 0.125)
+    rows = [0, 1, 33, 69]
+    for h in (0, 3, 4, 7):
+        o, l = attention_rows(qb, kb, vb, "bf16", True, 0.125, 0, h, rows)
+        assert np.allclose(o, O[0, rows, h, :], rtol=0, atol=1e-13)
+        assert np.allclose(l, L[0, h, rows], rtol=0, atol=1e-13)
+
+
+def test_grouped_heads_must_divide():
+    qb, kb, vb = fa_inputs.make_qkv(1, 4, 16, 64, "f16", "normal", 24, h_kv=3)
+    with pytest.raises(ValueError):
+        attention_reference(qb, kb, vb, "f16", False, 0.125)
