@@ -16,6 +16,7 @@ from .build import LIB_PATH, build  # noqa: F401
 __all__ = ["fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
            "fa_device_status", "fa_kernels_per_call", "attention_forward",
            "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_launches",
+           "fa_fwd_gqa", "fa_fwd_gqa_splitkv",
            "FaError", "library", "EXPORTED_SYMBOLS", "FA_F16", "FA_BF16"]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
@@ -23,7 +24,7 @@ FA_F16, FA_BF16 = 0, 1
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
                     "fa_device_status", "fa_kernels_per_call", "fa_splitkv_workspace_size",
-                    "fa_splitkv_launches", "fa_fwd_splitkv")
+                    "fa_splitkv_launches", "fa_fwd_splitkv", "fa_fwd_gqa", "fa_fwd_gqa_splitkv")
 
 _LIB = None
 
@@ -61,6 +62,11 @@ def library() -> ctypes.CDLL:
         lib.fa_splitkv_launches.restype = i
         lib.fa_fwd_splitkv.argtypes = sig + [i, vp, ctypes.c_size_t, vp]
         lib.fa_fwd_splitkv.restype = i
+        gsig = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i]   # ..., B, H, H_kv, S, D, causal, scale, dtype
+        lib.fa_fwd_gqa.argtypes = gsig + [vp]
+        lib.fa_fwd_gqa.restype = i
+        lib.fa_fwd_gqa_splitkv.argtypes = gsig + [vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_gqa_splitkv.restype = i
         _LIB = lib
     return _LIB
 
@@ -115,6 +121,20 @@ def fa_fwd_splitkv(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype, workspace,
                                         workspace, int(workspace_bytes), stream))
 
 
+def fa_fwd_gqa(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype, stream) -> int:
+    """Raw C-ABI call with H_kv K/V heads; returns the status."""
+    return int(library().fa_fwd_gqa(Q, K, V, O, LSE, int(B), int(H), int(H_kv), int(S), int(D),
+                                    int(bool(causal)), float(scale), int(dtype), stream))
+
+
+def fa_fwd_gqa_splitkv(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype, workspace,
+                       workspace_bytes, stream) -> int:
+    """Raw C-ABI call with H_kv K/V heads, keys split when SMs would idle."""
+    return int(library().fa_fwd_gqa_splitkv(Q, K, V, O, LSE, int(B), int(H), int(H_kv), int(S),
+                                            int(D), int(bool(causal)), float(scale), int(dtype),
+                                            workspace, int(workspace_bytes), stream))
+
+
 # workspace buffers of the split path, one per (device, stream): calls on one
 # stream are ordered, so they may share it
 _WORKSPACES = {}
@@ -133,9 +153,10 @@ def _workspace(device, stream_handle: int, nbytes: int):
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
                       out=None, lse=None, with_lse: bool = True, stream=None,
                       split_kv: bool = True):
-    """O, LSE for torch CUDA tensors q, k, v of shape [B, S, H, D].
+    """O, LSE for torch CUDA tensors q [B, S, H, D] and k, v [B, S, H_kv, D].
 
-    q, k, v must be contiguous fp16 or bf16 tensors on the same CUDA device.
+    q, k, v must be contiguous fp16 or bf16 tensors on the same CUDA device;
+    H_kv must divide H (query head h uses K/V head h // (H / H_kv)).
     ``out`` / ``lse`` may be preallocated ([B, S, H, D] same dtype; [B, H, S]
     fp32).  Work is enqueued on ``stream`` (default: the current stream) and
     not waited for.  ``split_kv`` lets the library split the keys of each
@@ -149,11 +170,15 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         raise ValueError(f"unsupported dtype {q.dtype}")
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("q, k, v must have the same dtype")
-    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must all be [B, S, H, D] with the same shape")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B, S, H, D] and k, v [B, S, H_kv, D]")
+    if k.shape[0] != q.shape[0] or k.shape[1] != q.shape[1] or k.shape[3] != q.shape[3] or \
+            k.shape[2] < 1 or q.shape[2] % k.shape[2] != 0:
+        raise ValueError("k, v must match q in B, S, D, with H_kv dividing H")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
     B, S, H, D = q.shape
+    H_kv = k.shape[2]
     if scale is None:
         scale = D ** -0.5
     if out is None:
@@ -172,12 +197,12 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         nbytes = fa_splitkv_workspace_size(B, H, S, D, causal) if split_kv else 0
         if nbytes > 0:
             ws = _workspace(q.device, st, nbytes)
-            rc = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                lse_ptr, B, H, S, D, causal, scale, dtype, ws.data_ptr(),
-                                ws.numel(), st)
+            rc = fa_fwd_gqa_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse_ptr, B, H, H_kv, S, D, causal, scale, dtype, ws.data_ptr(),
+                                    ws.numel(), st)
         else:
-            rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
-                        B, H, S, D, causal, scale, dtype, st)
+            rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                            B, H, H_kv, S, D, causal, scale, dtype, st)
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
     return out, lse

@@ -137,8 +137,8 @@ size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D) {
 }
 
 template <int D, bool BF16, int NS, int RS>
-int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int S,
-           int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace) {
+int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
+           int S, int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace) {
     auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS>;
     constexpr int kSmem = fa::SmemLayout<D, NS, RS>::kAlloc;
     // The dynamic shared-memory opt-in is per device; remember it per device.
@@ -153,8 +153,8 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     if (attr_err[dev] != cudaSuccess) return FA_ERR_CUDA;
 
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, Q, BF16, B, S, H, D, fa::kBM) || !make_map(&mk, K, BF16, B, S, H, D, fa::kBN) ||
-        !make_map(&mv, V, BF16, B, S, H, D, fa::kBN) || !make_map(&mo, O, BF16, B, S, H, D, fa::kBM))
+    if (!make_map(&mq, Q, BF16, B, S, H, D, fa::kBM) || !make_map(&mk, K, BF16, B, S, Hkv, D, fa::kBN) ||
+        !make_map(&mv, V, BF16, B, S, Hkv, D, fa::kBN) || !make_map(&mo, O, BF16, B, S, H, D, fa::kBM))
         return FA_ERR_CUDA;
 
     fa::FwdParams p;
@@ -162,6 +162,7 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.H = H;
     p.S = S;
     p.causal = causal ? 1 : 0;
+    p.kv_group = H / Hkv;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.lse = LSE;
     const int rows_per_cta = fa::kQTiles * fa::kBM;
@@ -243,18 +244,18 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
     return FA_OK;
 }
 
-int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int S,
-             int D, int causal, float scale, int dtype, cudaStream_t st, const SplitPlan& plan,
+int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
+             int S, int D, int causal, float scale, int dtype, cudaStream_t st, const SplitPlan& plan,
              void* ws) {
     // <head dim, bf16, K/V ring slots, softmax threads per query row>
     if (dtype == FA_F16) {
         if (D == 64)
-            return launch<64, false, kRingD64, kRowSplitD64>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
-        return launch<128, false, kRingD128, kRowSplitD128>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+            return launch<64, false, kRingD64, kRowSplitD64>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, plan, ws);
+        return launch<128, false, kRingD128, kRowSplitD128>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, plan, ws);
     }
     if (D == 64)
-        return launch<64, true, kRingD64, kRowSplitD64>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
-    return launch<128, true, kRingD128, kRowSplitD128>(Q, K, V, O, LSE, B, H, S, causal, scale, st, plan, ws);
+        return launch<64, true, kRingD64, kRowSplitD64>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, plan, ws);
+    return launch<128, true, kRingD128, kRowSplitD128>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, plan, ws);
 }
 
 }  // namespace
@@ -265,7 +266,16 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
            int D, int causal, float scale, int dtype, fa_stream_t stream) {
     const int v = validate(Q, K, V, O, LSE, B, H, S, D, scale, dtype);
     if (v != FA_OK) return v;
-    return dispatch(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype,
+    return dispatch(Q, K, V, O, LSE, B, H, H, S, D, causal, scale, dtype,
+                    reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr);
+}
+
+int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+               int H_kv, int S, int D, int causal, float scale, int dtype, fa_stream_t stream) {
+    const int v = validate(Q, K, V, O, LSE, B, H, S, D, scale, dtype);
+    if (v != FA_OK) return v;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    return dispatch(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype,
                     reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr);
 }
 
@@ -283,19 +293,27 @@ int fa_splitkv_launches(int B, int H, int S, int D, int causal) {
     return plan_split(B, H, S, causal != 0, num_sms()).chunk ? 2 : 1;
 }
 
-int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
-                   int S, int D, int causal, float scale, int dtype, void* workspace,
-                   size_t workspace_bytes, fa_stream_t stream) {
+int fa_fwd_gqa_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                       int H, int H_kv, int S, int D, int causal, float scale, int dtype,
+                       void* workspace, size_t workspace_bytes, fa_stream_t stream) {
     const int v = validate(Q, K, V, O, LSE, B, H, S, D, scale, dtype);
     if (v != FA_OK) return v;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     const int sms = num_sms();
     if (sms <= 0) return FA_ERR_CUDA;
     const SplitPlan plan = plan_split(B, H, S, causal != 0, sms);
     const size_t need = workspace_bytes_for(plan, B, H, S, D);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FA_ERR_INVALID_ARG;
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 15u)) return FA_ERR_UNSUPPORTED;
-    return dispatch(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype,
+    return dispatch(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype,
                     reinterpret_cast<cudaStream_t>(stream), plan, workspace);
+}
+
+int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                   int S, int D, int causal, float scale, int dtype, void* workspace,
+                   size_t workspace_bytes, fa_stream_t stream) {
+    return fa_fwd_gqa_splitkv(Q, K, V, O, LSE, B, H, H, S, D, causal, scale, dtype, workspace,
+                              workspace_bytes, stream);
 }
 
 int fa_fwd_f16(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
@@ -396,6 +414,6 @@ extern "C" int fa_fwd_splitkv_static(const void* Q, const void* K, const void* V
         ws = static_workspace_address(&status);
         if (ws == nullptr) return status;
     }
-    return dispatch(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype,
+    return dispatch(Q, K, V, O, LSE, B, H, H, S, D, causal, scale, dtype,
                     reinterpret_cast<cudaStream_t>(stream), plan, ws);
 }

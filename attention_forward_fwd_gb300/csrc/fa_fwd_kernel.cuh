@@ -103,6 +103,7 @@ constexpr int kMaxSplitBlocks = 128;
 struct FwdParams {
     int B, H, S;
     int causal;
+    int kv_group;       // query heads per K/V head (K, V have H / kv_group heads)
     // Work items: the (query block, split) pairs of every head, numbered
     // w = y * (B*H) + b*H + h with y the block's visit index (heaviest first
     // when causal).  Each CTA runs items blockIdx.x, 2G-1-blockIdx.x,
@@ -202,6 +203,7 @@ struct SmemLayout {
 // key tiles [jb, jb + nkv_t) that query tile t visits in this item's split.
 struct WorkItem {
     int b, h, bh;
+    int hkv;            // the K/V head of query head h
     int q0;             // first query row of the block
     int jb;             // first key tile of the split
     int nkv0, nkv1;     // key tiles of query tiles 0 and 1
@@ -217,6 +219,7 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
     it.bh = w - y * bhn;
     it.b = it.bh / p.H;
     it.h = it.bh - it.b * p.H;
+    it.hkv = it.h / p.kv_group;
     const bool causal = p.causal != 0;
     int qb, je, nsplit;
     if (p.kv_chunk <= 0) {
@@ -359,7 +362,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         }
         const CUtensorMap* m = is_v ? &tmV : &tmK;
         for (int c = 0; c < kChunks; ++c)
-            ptx::tma_load_4d(sbase + L::kOffKV + slot * L::kKVBytes + c * (kBN * 128), m, fb, c * 64, it.h,
+            ptx::tma_load_4d(sbase + L::kOffKV + slot * L::kKVBytes + c * (kBN * 128), m, fb, c * 64, it.hkv,
                              (it.jb + j) * kBN, it.b);
     };
     // Q tiles of item `it` (a tile with no key tile is not loaded)

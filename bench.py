@@ -346,10 +346,11 @@ def run_ours(args, w):
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def call(qp, kp, vp, o, lse, causal):
-        rc = lib.fa_fwd_splitkv(qp, kp, vp, o.data_ptr(), lse.data_ptr(), w.B, w.H, w.S, w.D,
+        rc = lib.fa_fwd_gqa_splitkv(qp, kp, vp, o.data_ptr(), lse.data_ptr(), w.B, w.H, w.kv_heads,
+                                    w.S, w.D,
                                 int(causal), w.scale, dtype_code, ws.data_ptr(), ws.numel(), sp)
         if rc != 0:
-            raise fa.FaError(rc, "fa_fwd_splitkv")
+            raise fa.FaError(rc, "fa_fwd_gqa_splitkv")
 
     def step():
         for causal, o, lse in zip(modes, outs, lses):
@@ -450,14 +451,16 @@ def end_to_end(args, w, lib, fa, dev, stream, tq, tk, tv, modes, dtype_code, ws,
     """
     import torch
     n_in = tq.numel()
+    n_kv = tk.numel()       # K and V (fewer heads than Q when grouped)
     elt = tq.element_size()
-    h_in = torch.empty(3 * n_in, dtype=tq.dtype).pin_memory()
-    for i, t in enumerate((tq, tk, tv)):
-        h_in[i * n_in:(i + 1) * n_in].copy_(t.reshape(-1))
+    n_all = n_in + 2 * n_kv
+    h_in = torch.empty(n_all, dtype=tq.dtype).pin_memory()
+    for off, t in ((0, tq), (n_in, tk), (n_in + n_kv, tv)):
+        h_in[off:off + t.numel()].copy_(t.reshape(-1))
     o_bytes = n_in * elt
     l_bytes = (w.B * w.H * w.S * 4 + 255) // 256 * 256   # keeps the next O 16-byte aligned
     out_bytes = len(modes) * (o_bytes + l_bytes)
-    d_in = [torch.empty(3 * n_in, dtype=tq.dtype, device=dev) for _ in range(2)]
+    d_in = [torch.empty(n_all, dtype=tq.dtype, device=dev) for _ in range(2)]
     d_out = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
     h_out = [torch.empty(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
 
@@ -466,11 +469,12 @@ def end_to_end(args, w, lib, fa, dev, stream, tq, tk, tv, modes, dtype_code, ws,
         base_out = d_out[slot].data_ptr()
         for m, causal in enumerate(modes):
             o_ptr = base_out + m * (o_bytes + l_bytes)
-            rc = lib.fa_fwd_splitkv(base_in, base_in + n_in * elt, base_in + 2 * n_in * elt, o_ptr,
-                                    o_ptr + o_bytes, w.B, w.H, w.S, w.D, int(causal), w.scale,
+            rc = lib.fa_fwd_gqa_splitkv(base_in, base_in + n_in * elt, base_in + (n_in + n_kv) * elt,
+                                        o_ptr, o_ptr + o_bytes, w.B, w.H, w.kv_heads, w.S, w.D,
+                                        int(causal), w.scale,
                                     dtype_code, ws.data_ptr(), ws.numel(), st.cuda_stream)
             if rc != 0:
-                raise fa.FaError(rc, "fa_fwd_splitkv")
+                raise fa.FaError(rc, "fa_fwd_gqa_splitkv")
 
     # copies, event records and stream waits go straight to the CUDA driver
     # (a few hundred ns each; the torch wrappers cost microseconds per call)
@@ -481,7 +485,7 @@ def end_to_end(args, w, lib, fa, dev, stream, tq, tk, tv, modes, dtype_code, ws,
     uploaded = [drv.event() for _ in range(2)]
     computed = [drv.event() for _ in range(2)]
     downloaded = [drv.event() for _ in range(2)]
-    in_bytes = 3 * n_in * elt
+    in_bytes = n_all * elt
 
     def pipelined_step(i):
         sl = i % 2
@@ -525,7 +529,7 @@ def end_to_end(args, w, lib, fa, dev, stream, tq, tk, tv, modes, dtype_code, ws,
     if not torch.isfinite(got.float()).all():
         raise RuntimeError("end-to-end output is not finite")
     return {"value": world * flops_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-            "h2d_bytes_per_step": 3 * n_in * elt, "d2h_bytes_per_step": out_bytes,
+            "h2d_bytes_per_step": n_all * elt, "d2h_bytes_per_step": out_bytes,
             "ms_per_step": ms, "steps": n,
             "copies": "one packed upload and one packed download per step on their own "
                       "streams, two buffer slots (overlapping the neighbouring steps' kernels)",
@@ -555,8 +559,9 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
-                    rc = lib.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                            o.data_ptr(), lse.data_ptr(), w.B, w.H, w.S, w.D,
+                    rc = lib.fa_fwd_gqa_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                o.data_ptr(), lse.data_ptr(), w.B, w.H, w.kv_heads,
+                                                w.S, w.D,
                                             int(causal), w.scale, code, ws.data_ptr(),
                                             ws.numel(), stream.cuda_stream)
                     e1.record(stream)

@@ -27,7 +27,9 @@ stress     B=3,H=8,S=1999,D=64 fp16, Q,K = 4*N(0,1), V ~ U[-1,1], scale 1/8,
            both masks; head (b=2,h=7) has every key equal to key 0
 =========  ==================================================================
 
-Seeds are ``1000 + index`` (index 1..5 in the order above).
+Seeds are ``1000 + index`` (index 1..5 in the order above).  A sixth workload,
+b4h32kv8d128 (B=4, 32 query heads over 8 K/V heads, S=4096, D=128 bf16,
+causal, seed 1006), measures grouped K/V heads.
 """
 from __future__ import annotations
 
@@ -53,6 +55,11 @@ class Workload:
     modes: tuple          # causal flags the workload is run with
     seed: int
     identical_key_head: tuple = field(default=())   # (b, h) or ()
+    h_kv: int | None = None   # K/V heads when grouped (query heads share them)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.h_kv is None else self.h_kv
 
 
 WORKLOADS = {
@@ -66,6 +73,10 @@ WORKLOADS = {
                           1.0 / math.sqrt(128.0), (True, False), 1004),
     "stress": Workload("stress", 3, 8, 1999, 64, "f16", "stress", 1.0 / 8.0,
                        (True, False), 1005, identical_key_head=(2, 7)),
+    # grouped K/V heads (GQA): 32 query heads sharing 8 K/V heads, the
+    # production extension beyond the five configurations
+    "b4h32kv8d128": Workload("b4h32kv8d128", 4, 32, 4096, 128, "bf16", "normal",
+                             1.0 / math.sqrt(128.0), (True,), 1006, h_kv=8),
 }
 
 
@@ -113,7 +124,7 @@ def make_qkv(B: int, H: int, S: int, D: int, dtype: str = "f16",
 
 def make_qkv_for(w: Workload):
     return make_qkv(w.B, w.H, w.S, w.D, w.dtype, w.dist, w.seed,
-                    w.identical_key_head)
+                    w.identical_key_head, h_kv=w.h_kv)
 
 
 def to_torch(bits: np.ndarray, dtype: str):

@@ -112,6 +112,30 @@ int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* 
                    void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * Grouped K/V heads (GQA; MQA when H_kv = 1).  The page "CuTe 详解：以
+ * FlashAttention-2 拆解 Layout、TiledCopy 与 TiledMMA" lists GQA/MQA among
+ * what a production FA2 forward also handles (section 哪些结论可以迁移，哪些只是
+ * 本例特例); it gives no formula, and the reading here is the usual one:
+ * K and V have H_kv heads, H_kv divides H, and query head h attends with
+ * K/V head h / (H / H_kv) (consecutive query heads share a K/V head).
+ *
+ *   Q, O  [B, S, H, D] 16-bit, device       LSE [B, H, S] fp32 or NULL
+ *   K, V  [B, S, H_kv, D] 16-bit, device    everything else as fa_fwd
+ *
+ * fa_fwd_gqa_splitkv splits the keys like fa_fwd_splitkv; its workspace size
+ * is fa_splitkv_workspace_size(B, H, S, D, causal) (it does not depend on
+ * H_kv).  Errors: as fa_fwd; FA_ERR_INVALID_ARG also when H_kv < 1 or H_kv
+ * does not divide H.  fa_fwd(...) is fa_fwd_gqa(..., H_kv = H, ...).
+ */
+int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
+               int B, int H, int H_kv, int S, int D, int causal, float scale, int dtype,
+               fa_stream_t stream);
+int fa_fwd_gqa_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                       int B, int H, int H_kv, int S, int D, int causal, float scale,
+                       int dtype, void* workspace, size_t workspace_bytes,
+                       fa_stream_t stream);
+
+/*
  * fa_fwd_splitkv without a workspace argument, for callers that cannot
  * allocate device memory (for example a latency-critical loop that must not
  * pay for cudaMalloc's implicit device synchronisation, or a program whose

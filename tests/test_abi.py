@@ -106,3 +106,31 @@ def test_splitkv_entry_points_validate_before_cuda(lib):
     bad = fa.fa_fwd_splitkv(16, 16, 16, 16, None, 1, 1, 128, 96, 0, 0.125, fa.FA_F16,
                             None, 0, None)
     assert bad == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("H,H_kv", [(4, 0), (4, -1), (4, 3), (6, 4), (1, 2)])
+def test_gqa_entry_points_reject_bad_group_before_cuda(lib, H, H_kv):
+    """H_kv must be >= 1 and divide H; checked before anything is launched."""
+    args = (16, 16, 16, 16, None, 1, H, H_kv, 128, 64, 0, 0.125, fa.FA_F16)
+    assert fa.fa_fwd_gqa(*args, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_gqa_splitkv(*args, None, 0, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_gqa_entry_points_validate_like_fa_fwd(lib):
+    assert fa.fa_fwd_gqa(None, 16, 16, 16, None, 1, 4, 2, 128, 64, 0, 0.125, fa.FA_F16, None) \
+        == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_gqa(16, 16, 16, 16, None, 1, 4, 2, 128, 96, 0, 0.125, fa.FA_F16, None) \
+        == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_gqa(16, 16, 24, 16, None, 1, 4, 2, 128, 64, 0, 0.125, fa.FA_F16, None) \
+        == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.gpu
+def test_binding_rejects_mismatched_kv_heads():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs CUDA tensors to get past the device check")
+    q = torch.zeros(1, 8, 4, 64, dtype=torch.float16, device="cuda")
+    k = torch.zeros(1, 8, 3, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(ValueError):
+        fa.attention_forward(q, k, k)

@@ -146,6 +146,35 @@ def test_several_work_items_per_cta(B, H, S, D, dtype, causal):
     _full_case(B, H, S, D, dtype, "normal", 40 + S, causal)
 
 
+@pytest.mark.parametrize("split_kv", [False, True], ids=["one-cta-per-block", "split-kv"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,H_kv,S,D,dtype", [
+    (2, 8, 2, 300, 64, "f16"),     # GQA, ragged
+    (1, 8, 1, 513, 64, "bf16"),    # MQA
+    (2, 16, 4, 640, 128, "bf16"),
+    (1, 6, 3, 257, 128, "f16"),
+    (3, 40, 8, 512, 64, "f16"),    # several work items per CTA
+])
+def test_grouped_kv_heads(B, H, H_kv, S, D, dtype, causal, split_kv):
+    """K/V with H_kv heads shared by groups of H / H_kv query heads, every
+    element against the oracle (one CTA per block and the key split)."""
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dtype, "normal", 50 + S + H_kv, h_kv=H_kv)
+    scale = D ** -0.5
+    O, L = run_gpu(qb, kb, vb, dtype, causal, scale, split_kv=split_kv)
+    Oref, Lref = attention_reference(qb, kb, vb, dtype, causal, scale)
+    assert_close(O, L, Oref, Lref, dtype, f"B{B} H{H}/{H_kv} S{S} D{D} {dtype} causal={causal}")
+
+
+def test_grouped_kv_heads_split_path_is_taken():
+    """One query head group on a long sequence: the keys are split and merged."""
+    import attention_forward_fwd_gb300 as fa
+    assert fa.fa_splitkv_launches(1, 2, 3000, 64, True) == 2
+    qb, kb, vb = fa_inputs.make_qkv(1, 2, 3000, 64, "f16", "stress", 77, h_kv=1)
+    O, L = run_gpu(qb, kb, vb, "f16", True, 0.125, split_kv=True)
+    Oref, Lref = attention_reference(qb, kb, vb, "f16", True, 0.125)
+    assert_close(O, L, Oref, Lref, "f16", "MQA split")
+
+
 def test_many_heads_and_batches_layout():
     """[B, S, H, D] with H > 1 and B > 1: heads and batches land in place."""
     _full_case(3, 5, 200, 64, "f16", "normal", 6, False)
@@ -194,7 +223,7 @@ def _sampled_rows(S, rng, n=24):
 
 
 @pytest.mark.parametrize("name,causal", [("b4h16", True), ("b2h16d128", True),
-                                         ("b2h16d128", False)])
+                                         ("b2h16d128", False), ("b4h32kv8d128", True)])
 def test_workload_full_size_sampled(name, causal):
     """Full-size workloads in the launch configuration the bench times;
     sampled rows of several heads against the oracle row by row."""
