@@ -39,7 +39,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "make_qkv", "make_qkv_for", "to_torch",
-           "f32_to_bits", "attention_flops"]
+           "f32_to_bits", "attention_flops", "make_varlen", "varlen_lengths"]
 
 
 @dataclass(frozen=True)
@@ -120,6 +120,24 @@ def make_qkv(B: int, H: int, S: int, D: int, dtype: str = "f16",
         b, h = identical_key_head
         k[b, :, h, :] = k[b, 0, h, :]
     return (f32_to_bits(q, dtype), f32_to_bits(k, dtype), f32_to_bits(v, dtype))
+
+
+def make_varlen(seqlens, H: int, D: int, dtype: str = "f16", dist: str = "normal",
+                seed: int = 0, h_kv: int | None = None):
+    """Packed variable-length batch: Q [total, H, D] and K, V [total, h_kv, D]
+    as uint16 bit arrays (sequence b is rows cu[b] .. cu[b+1]-1), and the
+    int32 offsets cu = [0, S_0, S_0 + S_1, ...] (length B + 1)."""
+    seqlens = np.asarray(seqlens, dtype=np.int64)
+    cu = np.zeros(len(seqlens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(seqlens)
+    total = int(cu[-1])
+    q, k, v = make_qkv(1, H, total, D, dtype, dist, seed, h_kv=h_kv)
+    return q[0], k[0], v[0], cu
+
+
+def varlen_lengths(B: int, lo: int, hi: int, seed: int) -> np.ndarray:
+    """B sequence lengths drawn uniformly from [lo, hi] (a mixed-length batch)."""
+    return np.random.default_rng(seed).integers(lo, hi + 1, size=B)
 
 
 def make_qkv_for(w: Workload):

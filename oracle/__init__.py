@@ -6,5 +6,5 @@ and reference legs may import this package.  The CUDA path never does.
 from .attention import (  # noqa: F401
     decode, decode_bf16, decode_f16,
     attention_reference, attention_reference_f64, attention_rows,
-    softmax_probabilities, online_softmax_attention,
+    softmax_probabilities, online_softmax_attention, attention_reference_varlen,
 )

@@ -48,6 +48,11 @@ Readings where the pages are silent
   the contract): K and V may have H_kv heads with H_kv dividing H; query head
   h then uses K/V head h // (H / H_kv), consecutive query heads sharing one
   K/V head (H_kv = 1: one K/V head for all).
+* variable-length batches (not on the pages; "变长序列" is listed with the
+  production FA2's other needs): sequences packed along the token axis,
+  Q [total, H, D], K and V [total, H_kv, D], offsets cu[0..B] with cu[0] = 0;
+  sequence b is rows cu[b] .. cu[b+1]-1 and attends only within itself (the
+  causal mask counts positions from the sequence start); LSE is [H, total].
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (closed forms, invariants, library routines, brute force and hand-derived
@@ -62,7 +67,7 @@ import numpy as np
 __all__ = [
     "decode_f16", "decode_bf16", "decode",
     "attention_reference", "attention_reference_f64", "attention_rows",
-    "softmax_probabilities", "online_softmax_attention",
+    "softmax_probabilities", "online_softmax_attention", "attention_reference_varlen",
 ]
 
 
@@ -171,6 +176,29 @@ def attention_rows(qb, kb, vb, dtype: str, causal: bool, scale: float,
     kh = decode(kb[b, :, hk, :], dtype)
     vh = decode(vb[b, :, hk, :], dtype)
     return _rows_one_head(qh, kh, vh, rows, causal, scale)
+
+
+def attention_reference_varlen(qb, kb, vb, cu_seqlens, dtype: str, causal: bool, scale: float):
+    """Definition on a packed variable-length batch of 16-bit bit arrays:
+    each sequence is its own single-batch call of the definition.
+
+    qb [total, H, D], kb / vb [total, H_kv, D], cu_seqlens [B + 1].
+    Returns (O [total, H, D], LSE [H, total]) in float64.
+    """
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    total, H, D = qb.shape
+    if cu[0] != 0 or cu[-1] != total or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must start at 0, end at the token count and not decrease")
+    O = np.zeros((total, H, vb.shape[2]), dtype=np.float64)
+    LSE = np.zeros((H, total), dtype=np.float64)
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        if e == a:
+            continue                                   # an empty sequence has no rows
+        o, lse = attention_reference(qb[None, a:e], kb[None, a:e], vb[None, a:e], dtype, causal, scale)
+        O[a:e] = o[0]
+        LSE[:, a:e] = lse[0]
+    return O, LSE
 
 
 def softmax_probabilities(q, k, causal: bool, scale: float, b: int, h: int):

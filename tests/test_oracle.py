@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import fa_inputs
-from oracle import (attention_reference, attention_reference_f64,
+from oracle import (attention_reference, attention_reference_f64, attention_reference_varlen,
                     attention_rows, decode_bf16, decode_f16,
                     online_softmax_attention, softmax_probabilities)
 
@@ -488,3 +488,47 @@ def test_grouped_heads_must_divide():
     qb, kb, vb = fa_inputs.make_qkv(1, 4, 16, 64, "f16", "normal", 24, h_kv=3)
     with pytest.raises(ValueError):
         attention_reference(qb, kb, vb, "f16", False, 0.125)
+
+
+# ------------------------------------------------------ variable length
+# Reading (not on the pages): packed sequences, offsets cu, each sequence
+# attends within itself; LSE is [H, total].
+
+def test_varlen_equal_lengths_equal_the_batched_definition():
+    """B sequences of one length packed back to back give the batched result
+    (the [B, S, H, D] layout is the same memory with cu = 0, S, 2S, ...)."""
+    B, S, H, D = 3, 70, 4, 64
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, "f16", "normal", 31, h_kv=2)
+    cu = np.arange(B + 1, dtype=np.int32) * S
+    for causal in (False, True):
+        O, L = attention_reference(qb, kb, vb, "f16", causal, 0.125)
+        Ov, Lv = attention_reference_varlen(qb.reshape(B * S, H, D), kb.reshape(B * S, 2, D),
+                                            vb.reshape(B * S, 2, D), cu, "f16", causal, 0.125)
+        assert np.array_equal(Ov, O.reshape(B * S, H, D))
+        assert np.array_equal(Lv, L.transpose(1, 0, 2).reshape(H, B * S))
+
+
+def test_varlen_sequences_do_not_see_each_other():
+    """Changing every token of the other sequences leaves a sequence's output
+    unchanged; the first row of a causal sequence equals its own V row 0."""
+    lens = [5, 130, 1, 77]
+    qb, kb, vb, cu = fa_inputs.make_varlen(lens, 2, 64, "bf16", "normal", 32)
+    O, L = attention_reference_varlen(qb, kb, vb, cu, "bf16", True, 0.125)
+    a, e = int(cu[1]), int(cu[2])
+    q2, k2, v2, _ = fa_inputs.make_varlen(lens, 2, 64, "bf16", "normal", 33)
+    for x, y in ((q2, qb), (k2, kb), (v2, vb)):
+        x[a:e] = y[a:e]
+    O2, L2 = attention_reference_varlen(q2, k2, v2, cu, "bf16", True, 0.125)
+    assert np.array_equal(O2[a:e], O[a:e]) and np.array_equal(L2[:, a:e], L[:, a:e])
+    assert not np.array_equal(O2[:a], O[:a])
+    for b in range(len(lens)):
+        r = int(cu[b])
+        assert np.allclose(O[r], decode_bf16(vb[r]), rtol=0, atol=1e-12)   # causal row 0 = V[0]
+
+
+def test_varlen_empty_sequences_and_bad_offsets():
+    qb, kb, vb, cu = fa_inputs.make_varlen([0, 9, 0, 4], 1, 64, "f16", "normal", 34)
+    O, L = attention_reference_varlen(qb, kb, vb, cu, "f16", False, 0.125)
+    assert O.shape == (13, 1, 64) and np.all(np.isfinite(L))
+    with pytest.raises(ValueError):
+        attention_reference_varlen(qb, kb, vb, np.array([0, 9, 4, 13]), "f16", False, 0.125)
