@@ -16,15 +16,17 @@ from .build import LIB_PATH, build  # noqa: F401
 __all__ = ["fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
            "fa_device_status", "fa_kernels_per_call", "attention_forward",
            "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_launches",
-           "fa_fwd_gqa", "fa_fwd_gqa_splitkv",
+           "fa_fwd_gqa", "fa_fwd_gqa_splitkv", "fa_fwd_varlen", "attention_forward_varlen",
            "FaError", "library", "EXPORTED_SYMBOLS", "FA_F16", "FA_BF16"]
 
-FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+(FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT,
+ FA_ERR_BAD_SEQLENS) = range(6)
 FA_F16, FA_BF16 = 0, 1
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
                     "fa_device_status", "fa_kernels_per_call", "fa_splitkv_workspace_size",
-                    "fa_splitkv_launches", "fa_fwd_splitkv", "fa_fwd_gqa", "fa_fwd_gqa_splitkv")
+                    "fa_splitkv_launches", "fa_fwd_splitkv", "fa_fwd_gqa", "fa_fwd_gqa_splitkv",
+                    "fa_fwd_varlen")
 
 _LIB = None
 
@@ -67,6 +69,9 @@ def library() -> ctypes.CDLL:
         lib.fa_fwd_gqa.restype = i
         lib.fa_fwd_gqa_splitkv.argtypes = gsig + [vp, ctypes.c_size_t, vp]
         lib.fa_fwd_gqa_splitkv.restype = i
+        # Q, K, V, O, LSE, cu_seqlens, B, max_seqlen, total, H, H_kv, D, causal, scale, dtype, stream
+        lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_varlen.restype = i
         _LIB = lib
     return _LIB
 
@@ -133,6 +138,14 @@ def fa_fwd_gqa_splitkv(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype, 
     return int(library().fa_fwd_gqa_splitkv(Q, K, V, O, LSE, int(B), int(H), int(H_kv), int(S),
                                             int(D), int(bool(causal)), float(scale), int(dtype),
                                             workspace, int(workspace_bytes), stream))
+
+
+def fa_fwd_varlen(Q, K, V, O, LSE, cu_seqlens, B, max_seqlen, total, H, H_kv, D, causal, scale,
+                  dtype, stream) -> int:
+    """Raw C-ABI call on a packed variable-length batch; returns the status."""
+    return int(library().fa_fwd_varlen(Q, K, V, O, LSE, cu_seqlens, int(B), int(max_seqlen),
+                                       int(total), int(H), int(H_kv), int(D), int(bool(causal)),
+                                       float(scale), int(dtype), stream))
 
 
 # workspace buffers of the split path, one per (device, stream): calls on one
@@ -205,4 +218,54 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
                             B, H, H_kv, S, D, causal, scale, dtype, st)
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
+    return out, lse
+
+
+def attention_forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
+                             scale: float | None = None, out=None, lse=None,
+                             with_lse: bool = True, stream=None):
+    """O, LSE of a packed variable-length batch of torch CUDA tensors.
+
+    q [total, H, D], k, v [total, H_kv, D] (contiguous fp16 / bf16, H_kv
+    dividing H), cu_seqlens an int32 CUDA tensor [B + 1] of sequence offsets
+    (cu_seqlens[0] = 0), max_seqlen the longest sequence.  Returns
+    out [total, H, D] and lse [H, total] (fp32).  Work is enqueued on
+    ``stream`` (default: the current stream) and not waited for; offsets that
+    are out of range are reported by ``fa_device_status()``.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens", cu_seqlens)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must be fp16 or bf16 of one dtype")
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be an int32 tensor [B + 1]")
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape or k.shape[0] != q.shape[0] \
+            or k.shape[2] != q.shape[2] or q.shape[1] % k.shape[1] != 0:
+        raise ValueError("q must be [total, H, D] and k, v [total, H_kv, D], H_kv dividing H")
+    total, H, D = q.shape
+    H_kv = k.shape[1]
+    B = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse is None and with_lse:
+        lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.shape != (H, total) or lse.dtype != torch.float32
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [H, total] tensor")
+    dtype = FA_F16 if q.dtype == torch.float16 else FA_BF16
+    with torch.cuda.device(q.device):
+        st = torch.cuda.current_stream().cuda_stream if stream is None else int(stream)
+        rc = fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, cu_seqlens.data_ptr(),
+                           B, max_seqlen, total, H, H_kv, D, causal, scale, dtype, st)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_varlen")
     return out, lse

@@ -136,10 +136,11 @@ size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D) {
     return slots * (static_cast<size_t>(fa::kBM) * D + 2 * fa::kBM) * sizeof(float);
 }
 
-template <int D, bool BF16, int NS, int RS>
+template <int D, bool BF16, int NS, int RS, bool VARLEN>
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
-           int S, int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace) {
-    auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS>;
+           int S, int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace,
+           const int* cu_seqlens, int total) {
+    auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS, VARLEN>;
     constexpr int kSmem = fa::SmemLayout<D, NS, RS>::kAlloc;
     // The dynamic shared-memory opt-in is per device; remember it per device.
     static std::once_flag once[64];
@@ -152,9 +153,12 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     });
     if (attr_err[dev] != cudaSuccess) return FA_ERR_CUDA;
 
+    // packed variable-length tensors are one batch of `total` rows
+    const int mb = cu_seqlens ? 1 : B;
+    const int ms = cu_seqlens ? total : S;
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, Q, BF16, B, S, H, D, fa::kBM) || !make_map(&mk, K, BF16, B, S, Hkv, D, fa::kBN) ||
-        !make_map(&mv, V, BF16, B, S, Hkv, D, fa::kBN) || !make_map(&mo, O, BF16, B, S, H, D, fa::kBM))
+    if (!make_map(&mq, Q, BF16, mb, ms, H, D, fa::kBM) || !make_map(&mk, K, BF16, mb, ms, Hkv, D, fa::kBN) ||
+        !make_map(&mv, V, BF16, mb, ms, Hkv, D, fa::kBN) || !make_map(&mo, O, BF16, mb, ms, H, D, fa::kBM))
         return FA_ERR_CUDA;
 
     fa::FwdParams p;
@@ -163,6 +167,9 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.S = S;
     p.causal = causal ? 1 : 0;
     p.kv_group = H / Hkv;
+    p.cu_seqlens = cu_seqlens;
+    p.total = total;
+    p.o_ptr = O;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.lse = LSE;
     const int rows_per_cta = fa::kQTiles * fa::kBM;
@@ -246,16 +253,21 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
 
 int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
              int S, int D, int causal, float scale, int dtype, cudaStream_t st, const SplitPlan& plan,
-             void* ws) {
-    // <head dim, bf16, K/V ring slots, softmax threads per query row>
+             void* ws, const int* cu_seqlens = nullptr, int total = 0) {
+    // <head dim, bf16, K/V ring slots, softmax threads per query row, packed>
+    const bool packed = cu_seqlens != nullptr;
+#define FA_LAUNCH(D_, BF16_, NS_, RS_)                                                              \
+    (packed ? launch<D_, BF16_, NS_, RS_, true>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st,  \
+                                                plan, ws, cu_seqlens, total)                        \
+            : launch<D_, BF16_, NS_, RS_, false>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, \
+                                                 plan, ws, cu_seqlens, total))
     if (dtype == FA_F16) {
-        if (D == 64)
-            return launch<64, false, kRingD64, kRowSplitD64>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, plan, ws);
-        return launch<128, false, kRingD128, kRowSplitD128>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, plan, ws);
+        if (D == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);
+        return FA_LAUNCH(128, false, kRingD128, kRowSplitD128);
     }
-    if (D == 64)
-        return launch<64, true, kRingD64, kRowSplitD64>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, plan, ws);
-    return launch<128, true, kRingD128, kRowSplitD128>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, plan, ws);
+    if (D == 64) return FA_LAUNCH(64, true, kRingD64, kRowSplitD64);
+    return FA_LAUNCH(128, true, kRingD128, kRowSplitD128);
+#undef FA_LAUNCH
 }
 
 }  // namespace
@@ -277,6 +289,22 @@ int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
     if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     return dispatch(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype,
                     reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr);
+}
+
+int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                  const int* cu_seqlens, int B, int max_seqlen, int total, int H, int H_kv, int D,
+                  int causal, float scale, int dtype, fa_stream_t stream) {
+    // the shape checks of the batched call, on one batch of `total` rows
+    const int v = validate(Q, K, V, O, LSE, 1, H, total, D, scale, dtype);
+    if (v != FA_OK) return v;
+    if (cu_seqlens == nullptr || B < 1 || max_seqlen < 1 || max_seqlen > total) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) return FA_ERR_UNSUPPORTED;
+    const long long nqb = (static_cast<long long>(max_seqlen) + 255) / 256;
+    if (static_cast<long long>(B) * H * nqb > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    return dispatch(Q, K, V, O, LSE, B, H, H_kv, max_seqlen, D, causal, scale, dtype,
+                    reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, static_cast<int>(nqb)},
+                    nullptr, cu_seqlens, total);
 }
 
 int fa_splitkv_workspace_size(int B, int H, int S, int D, int causal, size_t* bytes) {
@@ -333,6 +361,7 @@ const char* fa_status_string(int status) {
         case FA_ERR_UNSUPPORTED: return "unsupported shape, head dimension or alignment";
         case FA_ERR_CUDA: return "CUDA runtime or driver error";
         case FA_ERR_TIMEOUT: return "a device-side wait timed out";
+        case FA_ERR_BAD_SEQLENS: return "a sequence offset was out of range (that sequence was skipped)";
         default: return "unknown status";
     }
 }

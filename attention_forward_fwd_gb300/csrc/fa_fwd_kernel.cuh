@@ -93,6 +93,7 @@ constexpr float kMaxTileSum = 256.0f;  // 2^kTauLog2: a tile's row sum that keep
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 
 constexpr int kStatusTimeout = 4;
+constexpr int kStatusBadSeqlens = 5;   // a sequence offset was out of range (sequence skipped)
 
 // Device status word: 0, or the status of the first wait that ran out.
 __device__ int g_fa_device_status;
@@ -104,6 +105,13 @@ struct FwdParams {
     int B, H, S;
     int causal;
     int kv_group;       // query heads per K/V head (K, V have H / kv_group heads)
+    // Variable-length batch (cu_seqlens != nullptr): Q, K, V, O are packed
+    // [total, heads, D], sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1
+    // (at most S rows), LSE is [H, total].  Work items of query blocks past a
+    // sequence's end are empty and skipped.
+    const int* cu_seqlens;
+    int total;
+    void* o_ptr;        // O, for the row-by-row stores of a sequence's last tile
     // Work items: the (query block, split) pairs of every head, numbered
     // w = y * (B*H) + b*H + h with y the block's visit index (heaviest first
     // when causal).  Each CTA runs items blockIdx.x, 2G-1-blockIdx.x,
@@ -204,6 +212,10 @@ struct SmemLayout {
 struct WorkItem {
     int b, h, bh;
     int hkv;            // the K/V head of query head h
+    int S;              // rows of this item's sequence
+    int base;           // first row of the sequence in the (packed) tensors
+    int tb;             // batch coordinate of the tensor maps (0 when packed)
+    bool bad;           // its sequence offsets were out of range
     int q0;             // first query row of the block
     int jb;             // first key tile of the split
     int nkv0, nkv1;     // key tiles of query tiles 0 and 1
@@ -212,6 +224,7 @@ struct WorkItem {
     bool partial;       // the block is split: write partial results
 };
 
+template <bool VARLEN>
 __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
     WorkItem it;
     const int bhn = p.B * p.H;
@@ -220,6 +233,20 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
     it.b = it.bh / p.H;
     it.h = it.bh - it.b * p.H;
     it.hkv = it.h / p.kv_group;
+    it.S = p.S;
+    it.base = 0;
+    it.tb = it.b;
+    it.bad = false;
+    if constexpr (VARLEN) {
+        const int a = p.cu_seqlens[it.b];
+        const int e = p.cu_seqlens[it.b + 1];
+        // offsets outside [0, total], decreasing, or a sequence longer than S:
+        // nothing of it is read or written
+        it.bad = !(a >= 0 && e >= a && e <= p.total && e - a <= p.S);
+        it.S = it.bad ? 0 : e - a;
+        it.base = it.bad ? 0 : a;
+        it.tb = 0;
+    }
     const bool causal = p.causal != 0;
     int qb, je, nsplit;
     if (p.kv_chunk <= 0) {
@@ -243,8 +270,8 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
         je = it.jb + p.kv_chunk;
     }
     it.q0 = qb * (kQTiles * kBM);
-    it.nkv0 = max(0, min(je, key_tiles_for(it.q0, p.S, causal)) - it.jb);
-    it.nkv1 = max(0, min(je, key_tiles_for(it.q0 + kBM, p.S, causal)) - it.jb);
+    it.nkv0 = max(0, min(je, key_tiles_for(it.q0, it.S, causal)) - it.jb);
+    it.nkv1 = max(0, min(je, key_tiles_for(it.q0 + kBM, it.S, causal)) - it.jb);
     it.nkv = max(it.nkv0, it.nkv1);
     it.partial = nsplit > 1;
     return it;
@@ -289,7 +316,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-template <int D, bool BF16, int NS, int RS>
+template <int D, bool BF16, int NS, int RS, bool VARLEN>
 __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -363,7 +390,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         const CUtensorMap* m = is_v ? &tmV : &tmK;
         for (int c = 0; c < kChunks; ++c)
             ptx::tma_load_4d(sbase + L::kOffKV + slot * L::kKVBytes + c * (kBN * 128), m, fb, c * 64, it.hkv,
-                             (it.jb + j) * kBN, it.b);
+                             it.base + (it.jb + j) * kBN, it.tb);
     };
     // Q tiles of item `it` (a tile with no key tile is not loaded)
     auto load_q = [&](const WorkItem& it) {
@@ -375,7 +402,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             if ((t == 0 ? it.nkv0 : it.nkv1) == 0) continue;
             for (int c = 0; c < kChunks; ++c)
                 ptx::tma_load_4d(sbase + L::kOffQ + t * L::kQBytes + c * (kBM * 128), &tmQ, qbar, c * 64,
-                                 it.h, it.q0 + t * kBM, it.b);
+                                 it.h, it.base + it.q0 + t * kBM, it.tb);
         }
     };
 
@@ -410,10 +437,18 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         // reads and writes global memory only after this wait (everything
         // else in the CTA is ordered after it by the barriers and the sync).
         ptx::grid_dependency_wait();
-        const WorkItem it = decode_item(p, cta_item(0, p.items));   // the grid has <= items CTAs
-        load_q(it);
-        first_round = min(NS, 2 * it.nkv);
-        for (int i = 0; i < first_round; ++i) load_item(it, i, i);
+        // this CTA's first item with key tiles (items of query blocks past the
+        // end of a variable-length sequence have none)
+        for (int k = 0;; ++k) {
+            const int w = cta_item(k, p.items);
+            if (w < 0) break;
+            const WorkItem it = decode_item<VARLEN>(p, w);
+            if (VARLEN && it.nkv == 0) continue;
+            load_q(it);
+            first_round = min(NS, 2 * it.nkv);
+            for (int i = 0; i < first_round; ++i) load_item(it, i, i);
+            break;
+        }
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kTmemCols);
@@ -449,13 +484,16 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 return g < NS ||
                        wait_warp(bar_addr(&bars->kv_empty[g % NS]), static_cast<uint32_t>((g / NS - 1) & 1));
             };
+            int ki = 0;   // items with key tiles so far (the barrier phases count these)
             for (int k = 0; ok; ++k) {
                 const int w = cta_item(k, p.items);
                 if (w < 0) break;
-                const WorkItem it = decode_item(p, w);
+                const WorkItem it = decode_item<VARLEN>(p, w);
+                if (VARLEN && it.bad && lane == 0) atomicCAS(&g_fa_device_status, 0, kStatusBadSeqlens);
+                if (VARLEN && it.nkv == 0) continue;
                 const int n = 2 * it.nkv;
                 int i = 0;
-                if (k == 0) {
+                if (ki == 0) {
                     // loaded before the sync, after the Q
                     i = __shfl_sync(0xffffffffu, first_round, 0);
                     gi = i;
@@ -469,14 +507,15 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                         if (lane == 0) load_item(it, i, static_cast<int>(gi % NS));
                     }
                     if (!ok) break;
-                    if (!(ok = wait_warp(bar_addr(&bars->q_empty), (k - 1) & 1))) break;
+                    if (!(ok = wait_warp(bar_addr(&bars->q_empty), (ki - 1) & 1))) break;
                     if (lane == 0) load_q(it);
-                    k_q = k;
+                    k_q = ki;
                 }
                 for (; i < n; ++i, ++gi) {
                     if (!(ok = slot_free(gi))) break;
                     if (lane == 0) load_item(it, i, static_cast<int>(gi % NS));
                 }
+                ++ki;
             }
             if (*abort_flag) {
                 // Let every copy this warp started land before the CTA exits.
@@ -543,15 +582,18 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             int gi0 = 0;       // ring position of the item's first tile, modulo 2*NS
             uint32_t gs = 0;   // S_t tiles issued, all items (parities only)
             bool ok = true;
+            int ki = 0;   // items with key tiles so far
             for (int k = 0; ok; ++k) {
                 const int w = cta_item(k, p.items);
                 if (w < 0) break;
-                const WorkItem it = decode_item(p, w);
+                const WorkItem it = decode_item<VARLEN>(p, w);
+                if (VARLEN && it.nkv == 0) continue;
                 const int nkv = it.nkv;
                 const int n_t = (t == 0) ? it.nkv0 : it.nkv1;
                 const uint32_t gs0 = gs;   // S_t / P_t / P_t V index of this item's key tile 0
                 // every issuer waits for every Q load, so that its phases stay in step
-                if (!(ok = wait_warp(qbar, k & 1))) break;
+                if (!(ok = wait_warp(qbar, ki & 1))) break;
+                ++ki;
                 if (!(ok = acquire(gi0 + ring_k(0, nkv), n_t > 0))) break;
                 if (n_t > 0) {
                     // S_t of the previous item must have been read by the softmax
@@ -640,13 +682,16 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             int gi0 = 0;                   // ring position of the item's K0, modulo 2*NS
             uint32_t gs[kQTiles] = {0, 0};  // S_t tiles issued per query tile (parities only)
             bool ok = true;
+            int ki = 0;   // items with key tiles so far
             for (int k = 0; ok; ++k) {
                 const int w = cta_item(k, p.items);
                 if (w < 0) break;
-                const WorkItem it = decode_item(p, w);
+                const WorkItem it = decode_item<VARLEN>(p, w);
+                if (VARLEN && it.nkv == 0) continue;
                 const int nkv = it.nkv, nkv0 = it.nkv0, nkv1 = it.nkv1;
                 const uint32_t g00 = gs[0], g10 = gs[1];
-                if (!(ok = wait_warp(qbar, k & 1))) break;
+                if (!(ok = wait_warp(qbar, ki & 1))) break;
+                ++ki;
                 const int k0 = gi0 + ring_k(0, nkv);
                 if (!(ok = wait_warp(full_bar(k0), full_par(k0)))) break;
                 ptx::tc_fence_after_sync();
@@ -722,10 +767,12 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         bool ok = true;
         uint32_t gs0 = 0;   // S_t tiles of earlier items (parities only)
 
+        int ki = 0;   // items with key tiles so far (the barrier phases count these)
         for (int k = 0;; ++k) {
             const int w = cta_item(k, p.items);
             if (w < 0) break;
-            const WorkItem it = decode_item(p, w);
+            const WorkItem it = decode_item<VARLEN>(p, w);
+            if (VARLEN && it.nkv == 0) continue;
             const int r0 = it.q0 + t * kBM;
             const int row = r0 + r;
             const int n_tiles = (t == 0) ? it.nkv0 : it.nkv1;
@@ -744,8 +791,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 float alpha = 1.f;
                 bool rescale = false;
                 if constexpr (kRowSplit == 1) {
-                    const bool need_mask = kv0 + kHalf > p.S || (p.causal && kv0 + kHalf - 1 > r0);
-                    const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
+                    const bool need_mask = kv0 + kHalf > it.S || (p.causal && kv0 + kHalf - 1 > r0);
+                    const int last = p.causal ? min(it.S - 1, row) : (it.S - 1);
                     constexpr int kChains = 4;
                     float mx[kChains];
 #pragma unroll
@@ -840,8 +887,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     const float2 sum = __fadd2_rn(sum2[0], sum2[1]);
                     l = l * alpha + (sum.x + sum.y);
                 } else {
-                    const bool need_mask = kv0 + kHalf > p.S || (p.causal && kv0 + kHalf - 1 > r0);
-                    const int last = p.causal ? min(p.S - 1, row) : (p.S - 1);
+                    const bool need_mask = kv0 + kHalf > it.S || (p.causal && kv0 + kHalf - 1 > r0);
+                    const int last = p.causal ? min(it.S - 1, row) : (it.S - 1);
 #pragma unroll
                     for (int q = 0; q < kHalf / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
                     ptx::tmem_ld_wait();
@@ -984,9 +1031,9 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             // whole-row sum from the RS parts
             float l_row = l;
             if constexpr (kRowSplit > 1) {
-                bars->row_sum[k & 1][t][hf][r] = l;
+                bars->row_sum[ki & 1][t][hf][r] = l;
                 ptx::named_barrier_sync(pair_bar, 32 * kRowSplit);
-                l_row = l + bars->row_sum[k & 1][t][hf ^ 1][r];
+                l_row = l + bars->row_sum[ki & 1][t][hf ^ 1][r];
             }
             // With O staged in the Q buffer, this tile's store thread frees
             // the buffer for the next item's Q.  A tile with no key tile has
@@ -994,10 +1041,10 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             // it waits for that load first, so that the release counts for
             // this item and not for the previous one.
             auto release_q = [&]() {
-                if (n_tiles == 0 && !wait_phase(qbar, k & 1, abort_flag)) return;
+                if (n_tiles == 0 && !wait_phase(qbar, ki & 1, abort_flag)) return;
                 ptx::mbar_arrive(bar_addr(&bars->q_empty));
             };
-            if (it.partial && r0 < p.S) {
+            if (it.partial && r0 < it.S) {
                 // partial result: o~ stays unnormalised (fp32), m and l go
                 // beside it; a tile that saw no key of this split records l = 0
                 const int ntq = (p.S + kBM - 1) / kBM;
@@ -1029,14 +1076,19 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 if (kStageInQ && eok && store_thread) release_q();
             } else if (n_tiles > 0) {
                 // final result: stage O_t as the 128-byte-swizzled TMA box, then
-                // one thread stores it; rows past S are dropped by the store
+                // one thread stores it; rows past S are dropped by the store.
+                // The last tile of a packed sequence is stored row by row
+                // instead (the rows after it belong to the next sequence).
+                const bool direct = VARLEN && r0 + kBM > it.S;
                 uint8_t* stage = smem + L::kOffStage + t * L::kQBytes;
-                if (!kStageInQ && k > 0) {
+                if (!kStageInQ && !direct && ki > 0) {
                     // the previous item's store must have read the staging buffer
                     if (store_thread) ptx::bulk_wait_group_read_all();
                     ptx::named_barrier_sync(tile_bar, kTileThreads);
                 }
                 const float inv_l = 1.f / l_row;
+                uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +
+                                 (static_cast<size_t>(it.base + row) * p.H + it.h) * D;
                 if (eok) {
                     ptx::tc_fence_after_sync();
 #pragma unroll
@@ -1048,8 +1100,6 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {   // four 16-byte chunks of 8 values
                             const int cc = hf * (kDH / 8) + q * 4 + u;   // chunk along the row
-                            const int box = cc >> 3;
-                            const int phys = (cc & 7) ^ (r & 7);
                             uint4 v;
                             v.x = pack2<BF16>(__uint_as_float(o[u * 8 + 0]) * inv_l,
                                               __uint_as_float(o[u * 8 + 1]) * inv_l);
@@ -1059,33 +1109,44 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                                               __uint_as_float(o[u * 8 + 5]) * inv_l);
                             v.w = pack2<BF16>(__uint_as_float(o[u * 8 + 6]) * inv_l,
                                               __uint_as_float(o[u * 8 + 7]) * inv_l);
-                            *reinterpret_cast<uint4*>(stage + box * (kBM * 128) + r * 128 + phys * 16) = v;
+                            if (direct) {
+                                if (row < it.S) *reinterpret_cast<uint4*>(orow + cc * 8) = v;
+                            } else {
+                                const int box = cc >> 3;
+                                const int phys = (cc & 7) ^ (r & 7);
+                                *reinterpret_cast<uint4*>(stage + box * (kBM * 128) + r * 128 + phys * 16) = v;
+                            }
                         }
                     }
-                    ptx::fence_proxy_async_smem();
+                    if (!direct) ptx::fence_proxy_async_smem();
                 }
-                const bool all_ok = ptx::named_barrier_and(tile_bar, kTileThreads, eok);
-                if (all_ok && store_thread) {
-                    for (int cch = 0; cch < kChunks; ++cch)
-                        ptx::tma_store_4d(&tmO, ptx::smem_addr(stage + cch * (kBM * 128)), cch * 64, it.h,
-                                          r0, it.b);
-                    ptx::bulk_commit_group();
-                    if (kStageInQ) {
-                        // the Q buffer may take the next item's Q once the store has read it
-                        ptx::bulk_wait_group_read_all();
-                        ptx::mbar_arrive(bar_addr(&bars->q_empty));
+                bool all_ok = eok;
+                if (!direct) {
+                    all_ok = ptx::named_barrier_and(tile_bar, kTileThreads, eok);
+                    if (all_ok && store_thread) {
+                        for (int cch = 0; cch < kChunks; ++cch)
+                            ptx::tma_store_4d(&tmO, ptx::smem_addr(stage + cch * (kBM * 128)), cch * 64, it.h,
+                                              it.base + r0, it.tb);
+                        ptx::bulk_commit_group();
                     }
                 }
-                if (all_ok && hf == 0 && p.lse != nullptr && row < p.S) {
+                if (kStageInQ && all_ok && store_thread) {
+                    // the Q buffer may take the next item's Q once the store has read it
+                    if (!direct) ptx::bulk_wait_group_read_all();
+                    ptx::mbar_arrive(bar_addr(&bars->q_empty));
+                }
+                if (eok && hf == 0 && p.lse != nullptr && row < it.S) {
                     // LSE = scale * m + ln l = ln2 * (m * scale * log2e + log2 l)
-                    p.lse[static_cast<size_t>(it.bh) * p.S + row] =
-                        (m_use * c + log2f(l_row)) * 0.69314718055994530942f;
+                    const size_t li = VARLEN ? static_cast<size_t>(it.h) * p.total + it.base + row
+                                             : static_cast<size_t>(it.bh) * p.S + row;
+                    p.lse[li] = (m_use * c + log2f(l_row)) * 0.69314718055994530942f;
                 }
             } else if (kStageInQ && store_thread) {
                 // no key tile for this query tile: its Q buffer was never loaded
                 release_q();
             }
             gs0 += static_cast<uint32_t>(n_tiles);
+            ++ki;
         }
         // every O store must be complete before the CTA exits
         if (store_thread) ptx::bulk_wait_group_all();

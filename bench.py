@@ -561,9 +561,8 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
                     e0.record(stream)
                     rc = lib.fa_fwd_gqa_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                                 o.data_ptr(), lse.data_ptr(), w.B, w.H, w.kv_heads,
-                                                w.S, w.D,
-                                            int(causal), w.scale, code, ws.data_ptr(),
-                                            ws.numel(), stream.cuda_stream)
+                                                w.S, w.D, int(causal), w.scale, code, ws.data_ptr(),
+                                                ws.numel(), stream.cuda_stream)
                     e1.record(stream)
                     assert rc == 0
                     if i >= 3:
@@ -575,7 +574,49 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
                 "ms": t, "tflops": tf, "pct_of_peak": 100.0 * tf / peak,
                 "launches": fa.fa_splitkv_launches(w.B, w.H, w.S, w.D, causal)}
         del q, k, v, o, lse, ws
+    res.update(varlen_workload(lib, fa, dev, stream, flush, peak))
     return res
+
+
+# Packed variable-length batch: 16 sequences of 256..8192 tokens (uniform,
+# seed 1007), 16 heads, D = 128 bf16, causal; FLOPs 2*H*S_b^2*D per sequence.
+VARLEN = dict(B=16, lo=256, hi=8192, seed=1007, H=16, D=128, dtype="bf16")
+
+
+def varlen_workload(lib, fa, dev, stream, flush, peak):
+    """Kernel-timed TFLOP/s of the packed variable-length batch (informational)."""
+    import numpy as np
+    import torch
+    c = VARLEN
+    lens = fa_inputs.varlen_lengths(c["B"], c["lo"], c["hi"], c["seed"])
+    qb, kb, vb, cu = fa_inputs.make_varlen(lens, c["H"], c["D"], c["dtype"], "normal", c["seed"])
+    q, k, v = (fa_inputs.to_torch(x, c["dtype"]).to(dev) for x in (qb, kb, vb))
+    cu_t = torch.from_numpy(cu).to(dev)
+    o = torch.empty_like(q)
+    total = q.shape[0]
+    lse = torch.empty((c["H"], total), dtype=torch.float32, device=dev)
+    scale = c["D"] ** -0.5
+    ms = []
+    with torch.cuda.stream(stream):
+        for i in range(13):
+            flush.fill_(float(i))
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            rc = lib.fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), cu_t.data_ptr(), c["B"], int(lens.max()), total,
+                                   c["H"], c["H"], c["D"], 1, scale, fa.FA_BF16, stream.cuda_stream)
+            e1.record(stream)
+            assert rc == 0
+            if i >= 3:
+                ms.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    t = statistics.median(a.elapsed_time(b) for a, b in ms)
+    flops = sum(fa_inputs.attention_flops(1, c["H"], int(s_), c["D"], True) for s_ in lens)
+    tf = flops / (t * 1e-3) / 1e12
+    name = f"varlen{c['B']}x{c['lo']}-{c['hi']}h{c['H']}d{c['D']}/causal"
+    return {name: {"ms": t, "tflops": tf, "pct_of_peak": 100.0 * tf / peak, "launches": 1,
+                   "tokens": int(total)}}
 
 
 def main(argv=None):

@@ -41,6 +41,10 @@
  *   FA_ERR_TIMEOUT      reported by fa_device_status(): a device-side wait
  *                       exceeded its time limit and the kernel returned early
  *                       (the outputs of that call are undefined)
+ *   FA_ERR_BAD_SEQLENS  reported by fa_device_status(): fa_fwd_varlen found a
+ *                       sequence offset out of range; nothing of that
+ *                       sequence was read or written (its O / LSE rows are
+ *                       left as they were)
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -60,7 +64,8 @@ typedef enum {
     FA_ERR_INVALID_ARG = 1,
     FA_ERR_UNSUPPORTED = 2,
     FA_ERR_CUDA = 3,
-    FA_ERR_TIMEOUT = 4
+    FA_ERR_TIMEOUT = 4,
+    FA_ERR_BAD_SEQLENS = 5
 } fa_status_t;
 
 typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype_t;
@@ -134,6 +139,33 @@ int fa_fwd_gqa_splitkv(const void* Q, const void* K, const void* V, void* O, flo
                        int B, int H, int H_kv, int S, int D, int causal, float scale,
                        int dtype, void* workspace, size_t workspace_bytes,
                        fa_stream_t stream);
+
+/*
+ * Variable-length batch: B sequences packed along the token axis.  The page
+ * "CuTe 详解：以 FlashAttention-2 拆解 Layout、TiledCopy 与 TiledMMA" lists
+ * variable-length sequences (变长序列) among what a production FA2 forward
+ * also handles (section 哪些结论可以迁移，哪些只是本例特例) without a formula;
+ * the reading here is the usual one: sequence b is rows
+ * cu_seqlens[b] .. cu_seqlens[b+1]-1 of the packed tensors and attends only
+ * within itself (causal positions count from the sequence start).
+ *
+ *   Q, O        [total, H, D] 16-bit, device
+ *   K, V        [total, H_kv, D] 16-bit, device (H_kv divides H)
+ *   LSE         [H, total] fp32, device, or NULL
+ *   cu_seqlens  [B + 1] int32, device: cu_seqlens[0] = 0, non-decreasing,
+ *               cu_seqlens[B] <= total, every length <= max_seqlen; read by
+ *               the kernel (a sequence that breaks this is skipped and
+ *               reported as FA_ERR_BAD_SEQLENS by fa_device_status())
+ *   max_seqlen  the longest sequence (sizes the grid), 1 <= max_seqlen <= total
+ *
+ * Errors before launch: as fa_fwd (on one batch of `total` rows), and
+ * FA_ERR_INVALID_ARG for a NULL cu_seqlens, B < 1, max_seqlen out of range
+ * or H_kv not dividing H; FA_ERR_UNSUPPORTED for a cu_seqlens pointer that is
+ * not 4-byte aligned.  The keys are not split over CTAs.
+ */
+int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                  const int* cu_seqlens, int B, int max_seqlen, int total, int H, int H_kv,
+                  int D, int causal, float scale, int dtype, fa_stream_t stream);
 
 /*
  * fa_fwd_splitkv without a workspace argument, for callers that cannot
