@@ -53,6 +53,10 @@ Readings where the pages are silent
   Q [total, H, D], K and V [total, H_kv, D], offsets cu[0..B] with cu[0] = 0;
   sequence b is rows cu[b] .. cu[b+1]-1 and attends only within itself (the
   causal mask counts positions from the sequence start); LSE is [H, total].
+* local (sliding-window) attention (not on the pages beyond "causal/local
+  mask" among the production needs): a window (left, right) keeps key j for
+  query i iff i - left <= j <= i + right, a negative bound meaning no bound on
+  that side; with the causal mask the right bound is 0.
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (closed forms, invariants, library routines, brute force and hand-derived
@@ -100,22 +104,28 @@ def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # the plain definition
 
-def _visible(S: int, rows: np.ndarray, causal: bool) -> np.ndarray:
+def _visible(S: int, rows: np.ndarray, causal: bool, window=(-1, -1)) -> np.ndarray:
     """Boolean mask [len(rows), S]: key j visible to query row i."""
     keys = np.arange(S)[None, :]
+    vis = np.ones((len(rows), S), dtype=bool)
     if causal:
-        return keys <= rows[:, None]
-    return np.ones((len(rows), S), dtype=bool)
+        vis &= keys <= rows[:, None]
+    left, right = window
+    if left >= 0:
+        vis &= keys >= rows[:, None] - left
+    if right >= 0:
+        vis &= keys <= rows[:, None] + right
+    return vis
 
 
-def _rows_one_head(q, k, v, rows, causal, scale):
+def _rows_one_head(q, k, v, rows, causal, scale, window=(-1, -1)):
     """Definition for query rows ``rows`` of one head.
 
     q: [S, D], k: [S, D], v: [S, Dv] float64.  Returns (O [n, Dv], LSE [n]).
     """
     S = k.shape[0]
     z = scale * (q[rows] @ k.T)                      # z_ij, fp64
-    vis = _visible(S, rows, causal)
+    vis = _visible(S, rows, causal, window)
     z = np.where(vis, z, -np.inf)                   # j outside N_i
     m = z.max(axis=1)                               # M_i
     e = np.exp(z - m[:, None])                      # exp(z_ij - M_i), 0 off N_i
@@ -134,7 +144,7 @@ def _kv_group(H: int, H_kv: int) -> int:
 
 
 def attention_reference_f64(q, k, v, causal: bool, scale: float,
-                            row_block: int = 512):
+                            row_block: int = 512, window=(-1, -1)):
     """Definition on float64 arrays q [B, S, H, D] and k, v [B, S, H_kv, D].
 
     Returns (O [B, S, H, D] float64, LSE [B, H, S] float64).
@@ -152,20 +162,22 @@ def attention_reference_f64(q, k, v, causal: bool, scale: float,
             qh, kh, vh = q[b, :, h, :], k[b, :, hk, :], v[b, :, hk, :]
             for r0 in range(0, S, row_block):
                 rows = np.arange(r0, min(S, r0 + row_block))
-                o, lse = _rows_one_head(qh, kh, vh, rows, causal, scale)
+                o, lse = _rows_one_head(qh, kh, vh, rows, causal, scale, window)
                 O[b, rows, h, :] = o
                 LSE[b, h, rows] = lse
     return O, LSE
 
 
-def attention_reference(qb, kb, vb, dtype: str, causal: bool, scale: float):
-    """Definition on 16-bit bit arrays [B, S, H, D] (decoded exactly)."""
+def attention_reference(qb, kb, vb, dtype: str, causal: bool, scale: float,
+                        window=(-1, -1)):
+    """Definition on 16-bit bit arrays [B, S, H, D] (decoded exactly);
+    ``window`` = (left, right) keeps keys i - left .. i + right (-1: no bound)."""
     return attention_reference_f64(decode(qb, dtype), decode(kb, dtype),
-                                   decode(vb, dtype), causal, scale)
+                                   decode(vb, dtype), causal, scale, window=window)
 
 
 def attention_rows(qb, kb, vb, dtype: str, causal: bool, scale: float,
-                   b: int, h: int, rows):
+                   b: int, h: int, rows, window=(-1, -1)):
     """Definition for a few query rows of one head (full-size sampling).
 
     Returns (O [len(rows), D], LSE [len(rows)]) in float64.
@@ -175,7 +187,7 @@ def attention_rows(qb, kb, vb, dtype: str, causal: bool, scale: float,
     qh = decode(qb[b, :, h, :], dtype)
     kh = decode(kb[b, :, hk, :], dtype)
     vh = decode(vb[b, :, hk, :], dtype)
-    return _rows_one_head(qh, kh, vh, rows, causal, scale)
+    return _rows_one_head(qh, kh, vh, rows, causal, scale, window)
 
 
 def attention_reference_varlen(qb, kb, vb, cu_seqlens, dtype: str, causal: bool, scale: float):

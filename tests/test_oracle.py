@@ -532,3 +532,58 @@ def test_varlen_empty_sequences_and_bad_offsets():
     assert O.shape == (13, 1, 64) and np.all(np.isfinite(L))
     with pytest.raises(ValueError):
         attention_reference_varlen(qb, kb, vb, np.array([0, 9, 4, 13]), "f16", False, 0.125)
+
+
+# ------------------------------------------------------ local (sliding window)
+# Reading (not on the pages beyond "causal/local mask"): window (left, right)
+# keeps key j for query i iff i - left <= j <= i + right (-1: no bound).
+
+def _f64(bits, dtype="f16"):
+    return decode_f16(bits) if dtype == "f16" else decode_bf16(bits)
+
+
+def test_window_zero_width_returns_own_value():
+    """(0, 0): every row sees only its own key, so O = V row by row and
+    LSE = scale * q_i . k_i."""
+    qb, kb, vb = fa_inputs.make_qkv(2, 3, 50, 64, "f16", "normal", 41)
+    for causal in (False, True):
+        O, L = attention_reference(qb, kb, vb, "f16", causal, 0.125, window=(0, 0))
+        assert np.array_equal(O, _f64(vb))
+        z = 0.125 * np.einsum("bshd,bshd->bhs", _f64(qb), _f64(kb))
+        assert np.allclose(L, z, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal,window", [(True, (1, -1)), (False, (1, 0)), (False, (1, 1))])
+def test_window_of_two_or_three_keys_closed_form(causal, window):
+    """Left bound 1 (causal, or right bound 0): keys {i-1, i}; window (1, 1):
+    keys {i-1, i, i+1} -- a softmax over two or three logits written out."""
+    qb, kb, vb = fa_inputs.make_qkv(1, 2, 40, 64, "bf16", "stress", 42)
+    q, k, v = _f64(qb, "bf16"), _f64(kb, "bf16"), _f64(vb, "bf16")
+    O, L = attention_reference(qb, kb, vb, "bf16", causal, 0.125, window=window)
+    S = 40
+    right = 0 if (causal or window[1] == 0) else window[1]
+    for h in range(2):
+        for i in range(S):
+            keys = [j for j in (i - 1, i, i + 1) if 0 <= j < S and i - 1 <= j <= i + right]
+            z = np.array([0.125 * q[0, i, h] @ k[0, j, h] for j in keys])
+            w = np.exp(z - z.max())
+            o = sum(wj * v[0, j, h] for wj, j in zip(w, keys)) / w.sum()
+            assert np.allclose(O[0, i, h], o, rtol=0, atol=1e-12)
+            assert abs(L[0, h, i] - (z.max() + math.log(w.sum()))) < 1e-12
+
+
+def test_unbounded_or_covering_window_is_the_plain_definition():
+    qb, kb, vb = fa_inputs.make_qkv(1, 2, 70, 64, "f16", "normal", 43)
+    for causal in (False, True):
+        O, L = attention_reference(qb, kb, vb, "f16", causal, 0.125)
+        for window in ((-1, -1), (69, 69), (1000, -1), (-1, 1000)):
+            Ow, Lw = attention_reference(qb, kb, vb, "f16", causal, 0.125, window=window)
+            assert np.array_equal(Ow, O) and np.array_equal(Lw, L), (causal, window)
+
+
+def test_window_rows_match_full_reference():
+    qb, kb, vb = fa_inputs.make_qkv(1, 4, 300, 64, "f16", "normal", 44, h_kv=2)
+    O, L = attention_reference(qb, kb, vb, "f16", True, 0.125, window=(37, -1))
+    rows = [0, 5, 36, 37, 38, 299]
+    o, l = attention_rows(qb, kb, vb, "f16", True, 0.125, 0, 3, rows, window=(37, -1))
+    assert np.array_equal(o, O[0, rows, 3]) and np.array_equal(l, L[0, 3, rows])
