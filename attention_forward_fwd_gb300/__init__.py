@@ -17,6 +17,7 @@ __all__ = ["fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
            "fa_device_status", "fa_kernels_per_call", "attention_forward",
            "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_launches",
            "fa_fwd_gqa", "fa_fwd_gqa_splitkv", "fa_fwd_varlen", "attention_forward_varlen",
+           "fa_fwd_local",
            "FaError", "library", "EXPORTED_SYMBOLS", "FA_F16", "FA_BF16"]
 
 (FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT,
@@ -26,7 +27,7 @@ FA_F16, FA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
                     "fa_device_status", "fa_kernels_per_call", "fa_splitkv_workspace_size",
                     "fa_splitkv_launches", "fa_fwd_splitkv", "fa_fwd_gqa", "fa_fwd_gqa_splitkv",
-                    "fa_fwd_varlen")
+                    "fa_fwd_varlen", "fa_fwd_local")
 
 _LIB = None
 
@@ -72,6 +73,9 @@ def library() -> ctypes.CDLL:
         # Q, K, V, O, LSE, cu_seqlens, B, max_seqlen, total, H, H_kv, D, causal, scale, dtype, stream
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_varlen.restype = i
+        # ..., B, H, H_kv, S, D, causal, window_left, window_right, scale, dtype, stream
+        lib.fa_fwd_local.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_local.restype = i
         _LIB = lib
     return _LIB
 
@@ -140,6 +144,14 @@ def fa_fwd_gqa_splitkv(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype, 
                                             workspace, int(workspace_bytes), stream))
 
 
+def fa_fwd_local(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, window_left, window_right, scale,
+                 dtype, stream) -> int:
+    """Raw C-ABI call with a sliding window (keys i - left .. i + right)."""
+    return int(library().fa_fwd_local(Q, K, V, O, LSE, int(B), int(H), int(H_kv), int(S), int(D),
+                                      int(bool(causal)), int(window_left), int(window_right),
+                                      float(scale), int(dtype), stream))
+
+
 def fa_fwd_varlen(Q, K, V, O, LSE, cu_seqlens, B, max_seqlen, total, H, H_kv, D, causal, scale,
                   dtype, stream) -> int:
     """Raw C-ABI call on a packed variable-length batch; returns the status."""
@@ -165,7 +177,7 @@ def _workspace(device, stream_handle: int, nbytes: int):
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
                       out=None, lse=None, with_lse: bool = True, stream=None,
-                      split_kv: bool = True):
+                      split_kv: bool = True, window=None):
     """O, LSE for torch CUDA tensors q [B, S, H, D] and k, v [B, S, H_kv, D].
 
     q, k, v must be contiguous fp16 or bf16 tensors on the same CUDA device;
@@ -175,6 +187,8 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     not waited for.  ``split_kv`` lets the library split the keys of each
     query block over several CTAs when the shape leaves SMs idle (the
     workspace is allocated with torch and cached per device and stream).
+    ``window = (left, right)`` restricts query i to keys i - left .. i + right
+    (-1: no bound on that side); windowed calls are not split.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -207,8 +221,12 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     with torch.cuda.device(q.device):
         st = torch.cuda.current_stream().cuda_stream if stream is None else int(stream)
         lse_ptr = lse.data_ptr() if lse is not None else None
-        nbytes = fa_splitkv_workspace_size(B, H, S, D, causal) if split_kv else 0
-        if nbytes > 0:
+        nbytes = fa_splitkv_workspace_size(B, H, S, D, causal) if split_kv and window is None else 0
+        if window is not None:
+            rc = fa_fwd_local(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                              B, H, H_kv, S, D, causal, int(window[0]), int(window[1]), scale,
+                              dtype, st)
+        elif nbytes > 0:
             ws = _workspace(q.device, st, nbytes)
             rc = fa_fwd_gqa_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                     lse_ptr, B, H, H_kv, S, D, causal, scale, dtype, ws.data_ptr(),

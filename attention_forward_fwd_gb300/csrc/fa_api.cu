@@ -136,11 +136,11 @@ size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D) {
     return slots * (static_cast<size_t>(fa::kBM) * D + 2 * fa::kBM) * sizeof(float);
 }
 
-template <int D, bool BF16, int NS, int RS, bool VARLEN>
+template <int D, bool BF16, int NS, int RS, bool GENERAL>
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
            int S, int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace,
-           const int* cu_seqlens, int total) {
-    auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS, VARLEN>;
+           const int* cu_seqlens, int total, int win_left, int win_right) {
+    auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS, GENERAL>;
     constexpr int kSmem = fa::SmemLayout<D, NS, RS>::kAlloc;
     // The dynamic shared-memory opt-in is per device; remember it per device.
     static std::once_flag once[64];
@@ -168,6 +168,8 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.causal = causal ? 1 : 0;
     p.kv_group = H / Hkv;
     p.cu_seqlens = cu_seqlens;
+    p.win_left = win_left;
+    p.win_right = win_right;
     p.total = total;
     p.o_ptr = O;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
@@ -253,14 +255,17 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
 
 int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
              int S, int D, int causal, float scale, int dtype, cudaStream_t st, const SplitPlan& plan,
-             void* ws, const int* cu_seqlens = nullptr, int total = 0) {
-    // <head dim, bf16, K/V ring slots, softmax threads per query row, packed>
-    const bool packed = cu_seqlens != nullptr;
+             void* ws, const int* cu_seqlens = nullptr, int total = 0, int win_left = -1,
+             int win_right = -1) {
+    // <head dim, bf16, K/V ring slots, softmax threads per query row, general>:
+    // packed variable-length batches and local windows take the general
+    // variant; the plain one compiles neither
+    const bool general = cu_seqlens != nullptr || win_left >= 0 || win_right >= 0;
 #define FA_LAUNCH(D_, BF16_, NS_, RS_)                                                              \
-    (packed ? launch<D_, BF16_, NS_, RS_, true>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st,  \
-                                                plan, ws, cu_seqlens, total)                        \
+    (general ? launch<D_, BF16_, NS_, RS_, true>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st,  \
+                                                plan, ws, cu_seqlens, total, win_left, win_right)                        \
             : launch<D_, BF16_, NS_, RS_, false>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, \
-                                                 plan, ws, cu_seqlens, total))
+                                                 plan, ws, cu_seqlens, total, win_left, win_right))
     if (dtype == FA_F16) {
         if (D == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);
         return FA_LAUNCH(128, false, kRingD128, kRowSplitD128);
@@ -289,6 +294,18 @@ int fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
     if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     return dispatch(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype,
                     reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr);
+}
+
+int fa_fwd_local(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                 int H_kv, int S, int D, int causal, int window_left, int window_right, float scale,
+                 int dtype, fa_stream_t stream) {
+    const int v = validate(Q, K, V, O, LSE, B, H, S, D, scale, dtype);
+    if (v != FA_OK) return v;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+    return dispatch(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype,
+                    reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr,
+                    nullptr, 0, window_left, window_right);
 }
 
 int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,

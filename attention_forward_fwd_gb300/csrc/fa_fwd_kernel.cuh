@@ -105,6 +105,10 @@ struct FwdParams {
     int B, H, S;
     int causal;
     int kv_group;       // query heads per K/V head (K, V have H / kv_group heads)
+    // Local attention: key j is kept for query i iff i - win_left <= j <= i +
+    // win_right (-1: no bound on that side; the causal mask caps the right
+    // bound at 0).  Windowed calls are not split over keys.
+    int win_left, win_right;
     // Variable-length batch (cu_seqlens != nullptr): Q, K, V, O are packed
     // [total, heads, D], sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1
     // (at most S rows), LSE is [H, total].  Work items of query blocks past a
@@ -218,13 +222,16 @@ struct WorkItem {
     bool bad;           // its sequence offsets were out of range
     int q0;             // first query row of the block
     int jb;             // first key tile of the split
-    int nkv0, nkv1;     // key tiles of query tiles 0 and 1
-    int nkv;            // max(nkv0, nkv1)
+    // query tile t uses key tiles [s_t, nkv_t) of the item's range (counted
+    // from jb); s_t > 0 only with a left window bound
+    int s0, s1;
+    int nkv0, nkv1;
+    int nkv;            // max(nkv0, nkv1): the item's key tiles through the ring
     int split;          // split index within the block
     bool partial;       // the block is split: write partial results
 };
 
-template <bool VARLEN>
+template <bool GENERAL>
 __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
     WorkItem it;
     const int bhn = p.B * p.H;
@@ -237,7 +244,7 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
     it.base = 0;
     it.tb = it.b;
     it.bad = false;
-    if constexpr (VARLEN) {
+    if (GENERAL && p.cu_seqlens != nullptr) {
         const int a = p.cu_seqlens[it.b];
         const int e = p.cu_seqlens[it.b + 1];
         // offsets outside [0, total], decreasing, or a sequence longer than S:
@@ -272,6 +279,24 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
     it.q0 = qb * (kQTiles * kBM);
     it.nkv0 = max(0, min(je, key_tiles_for(it.q0, it.S, causal)) - it.jb);
     it.nkv1 = max(0, min(je, key_tiles_for(it.q0 + kBM, it.S, causal)) - it.jb);
+    it.s0 = it.s1 = 0;
+    if (GENERAL && (p.win_left >= 0 || p.win_right >= 0)) {
+        // key tiles [lo_t, hi_t) that query tile t's rows reach (jb is 0 here)
+        int lo[kQTiles], hi[kQTiles];
+        for (int t = 0; t < kQTiles; ++t) {
+            const int r0 = it.q0 + t * kBM;
+            const int e = t == 0 ? it.nkv0 : it.nkv1;
+            lo[t] = p.win_left < 0 ? 0 : max(0, r0 - p.win_left) / kBN;
+            hi[t] = p.win_right < 0 ? e : min(e, (r0 + kBM - 1 + p.win_right) / kBN + 1);
+            if (hi[t] <= lo[t]) lo[t] = hi[t] = 0;   // no key for this tile
+        }
+        const int first = hi[0] > 0 ? lo[0] : lo[1];
+        it.jb = first;
+        it.s0 = hi[0] > 0 ? lo[0] - first : 0;
+        it.nkv0 = hi[0] > 0 ? hi[0] - first : 0;
+        it.s1 = hi[1] > 0 ? lo[1] - first : 0;
+        it.nkv1 = hi[1] > 0 ? hi[1] - first : 0;
+    }
     it.nkv = max(it.nkv0, it.nkv1);
     it.partial = nsplit > 1;
     return it;
@@ -316,7 +341,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-template <int D, bool BF16, int NS, int RS, bool VARLEN>
+template <int D, bool BF16, int NS, int RS, bool GENERAL>
 __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -396,10 +421,10 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     auto load_q = [&](const WorkItem& it) {
         uint32_t qbytes = 0;
         for (int t = 0; t < kQTiles; ++t)
-            if ((t == 0 ? it.nkv0 : it.nkv1) > 0) qbytes += L::kQBytes;
+            if ((t == 0 ? it.nkv0 - it.s0 : it.nkv1 - it.s1) > 0) qbytes += L::kQBytes;
         ptx::mbar_arrive_expect_tx(qbar, qbytes);
         for (int t = 0; t < kQTiles; ++t) {
-            if ((t == 0 ? it.nkv0 : it.nkv1) == 0) continue;
+            if ((t == 0 ? it.nkv0 - it.s0 : it.nkv1 - it.s1) <= 0) continue;
             for (int c = 0; c < kChunks; ++c)
                 ptx::tma_load_4d(sbase + L::kOffQ + t * L::kQBytes + c * (kBM * 128), &tmQ, qbar, c * 64,
                                  it.h, it.base + it.q0 + t * kBM, it.tb);
@@ -442,8 +467,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         for (int k = 0;; ++k) {
             const int w = cta_item(k, p.items);
             if (w < 0) break;
-            const WorkItem it = decode_item<VARLEN>(p, w);
-            if (VARLEN && it.nkv == 0) continue;
+            const WorkItem it = decode_item<GENERAL>(p, w);
+            if (GENERAL && it.nkv == 0) continue;
             load_q(it);
             first_round = min(NS, 2 * it.nkv);
             for (int i = 0; i < first_round; ++i) load_item(it, i, i);
@@ -488,9 +513,9 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             for (int k = 0; ok; ++k) {
                 const int w = cta_item(k, p.items);
                 if (w < 0) break;
-                const WorkItem it = decode_item<VARLEN>(p, w);
-                if (VARLEN && it.bad && lane == 0) atomicCAS(&g_fa_device_status, 0, kStatusBadSeqlens);
-                if (VARLEN && it.nkv == 0) continue;
+                const WorkItem it = decode_item<GENERAL>(p, w);
+                if (GENERAL && it.bad && lane == 0) atomicCAS(&g_fa_device_status, 0, kStatusBadSeqlens);
+                if (GENERAL && it.nkv == 0) continue;
                 const int n = 2 * it.nkv;
                 int i = 0;
                 if (ki == 0) {
@@ -586,16 +611,18 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             for (int k = 0; ok; ++k) {
                 const int w = cta_item(k, p.items);
                 if (w < 0) break;
-                const WorkItem it = decode_item<VARLEN>(p, w);
-                if (VARLEN && it.nkv == 0) continue;
+                const WorkItem it = decode_item<GENERAL>(p, w);
+                if (GENERAL && it.nkv == 0) continue;
                 const int nkv = it.nkv;
+                const int s_t = !GENERAL ? 0 : (t == 0) ? it.s0 : it.s1;    // key tiles [s_t, n_t)
                 const int n_t = (t == 0) ? it.nkv0 : it.nkv1;
-                const uint32_t gs0 = gs;   // S_t / P_t / P_t V index of this item's key tile 0
+                auto used = [&](int j) { return j >= s_t && j < n_t; };
+                const uint32_t gs0 = gs;   // S_t / P_t / P_t V index of this tile's first key tile
                 // every issuer waits for every Q load, so that its phases stay in step
                 if (!(ok = wait_warp(qbar, ki & 1))) break;
                 ++ki;
-                if (!(ok = acquire(gi0 + ring_k(0, nkv), n_t > 0))) break;
-                if (n_t > 0) {
+                if (!(ok = acquire(gi0 + ring_k(0, nkv), used(0)))) break;
+                if (used(0)) {
                     // S_t of the previous item must have been read by the softmax
                     if (gs > 0 && !(ok = wait_warp(s_free, (gs - 1) & 1))) break;
                     ptx::tc_fence_after_sync();
@@ -603,35 +630,34 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     ++gs;
                 }
                 // the Q buffer of tile t is free once its last S_t is complete
-                if (n_t <= 1) {
-                    if (n_t == 1) ptx::tc_commit_warp(q_empty);
-                    else ptx::mbar_arrive_warp(q_empty);
-                }
+                if (n_t <= s_t) ptx::mbar_arrive_warp(q_empty);
+                else if (n_t == 1) ptx::tc_commit_warp(q_empty);
                 for (int j = 0; ok && j < nkv; ++j) {
                     // S_t(j+1) as soon as the softmax holds S_t(j), then P_t V(j)
                     if (j + 1 < nkv) {
-                        const bool use = (j + 1) < n_t;
+                        const bool use = used(j + 1);
                         if (!(ok = acquire(gi0 + ring_k(j + 1, nkv), use))) break;
                         if (use) {
-                            if (!(ok = wait_warp(s_free, (gs - 1) & 1))) break;
+                            if (gs > 0 && !(ok = wait_warp(s_free, (gs - 1) & 1))) break;
                             ptx::tc_fence_after_sync();
                             issue_s(gi0 + ring_k(j + 1, nkv));
                             ++gs;
                             if (j + 2 == n_t) ptx::tc_commit_warp(q_empty);
                         }
                     }
-                    if (!(ok = acquire(gi0 + ring_v(j, nkv), j < n_t))) break;
-                    if (j < n_t) {
+                    if (!(ok = acquire(gi0 + ring_v(j, nkv), used(j)))) break;
+                    if (used(j)) {
                         // P_t V(j) in two halves: the first 64 keys as soon as
                         // the softmax has stored their P (and rescaled O_t if it
                         // had to), the rest once all of P_t(j) is written.  This
                         // also orders the item's first P_t V after the previous
                         // epilogue's reads of O_t.
                         const int ring = gi0 + ring_v(j, nkv);
-                        if (!(ok = wait_warp(bar_addr(&bars->p_half[t]), (gs0 + j) & 1))) break;
+                        const uint32_t g = gs0 + static_cast<uint32_t>(j - s_t);
+                        if (!(ok = wait_warp(bar_addr(&bars->p_half[t]), g & 1))) break;
                         ptx::tc_fence_after_sync();
-                        issue_pv(ring, j > 0, 0, kBN / 32);
-                        if (!(ok = wait_warp(p_full, (gs0 + j) & 1))) break;
+                        issue_pv(ring, j > s_t, 0, kBN / 32);
+                        if (!(ok = wait_warp(p_full, g & 1))) break;
                         ptx::tc_fence_after_sync();
                         issue_pv(ring, true, kBN / 32, kBN / 16);
                         ptx::tc_commit_warp(o_done);
@@ -686,17 +712,18 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             for (int k = 0; ok; ++k) {
                 const int w = cta_item(k, p.items);
                 if (w < 0) break;
-                const WorkItem it = decode_item<VARLEN>(p, w);
-                if (VARLEN && it.nkv == 0) continue;
+                const WorkItem it = decode_item<GENERAL>(p, w);
+                if (GENERAL && it.nkv == 0) continue;
                 const int nkv = it.nkv, nkv0 = it.nkv0, nkv1 = it.nkv1;
+                const int s0 = GENERAL ? it.s0 : 0, s1 = GENERAL ? it.s1 : 0;
                 const uint32_t g00 = gs[0], g10 = gs[1];
                 if (!(ok = wait_warp(qbar, ki & 1))) break;
                 ++ki;
                 const int k0 = gi0 + ring_k(0, nkv);
                 if (!(ok = wait_warp(full_bar(k0), full_par(k0)))) break;
                 ptx::tc_fence_after_sync();
-                if (nkv0 > 0) issue_s(0, k0);
-                if (nkv1 > 0) issue_s(1, k0);
+                if (s0 == 0 && nkv0 > 0) issue_s(0, k0);
+                if (s1 == 0 && nkv1 > 0) issue_s(1, k0);
                 ptx::tc_commit_warp(bar_addr(&bars->kv_empty[k0 % NS]));
                 for (int j = 0; ok && j < nkv; ++j) {
                     const int iv = gi0 + ring_v(j, nkv);
@@ -704,27 +731,27 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     const bool next = (j + 1) < nkv;
                     if (!(ok = wait_warp(full_bar(iv), full_par(iv)))) break;
                     ptx::tc_fence_after_sync();
-                    if (j < nkv0) {
-                        if (!(ok = wait_warp(bar_addr(&bars->p_full[0]), (g00 + j) & 1))) break;
+                    if (j >= s0 && j < nkv0) {
+                        if (!(ok = wait_warp(bar_addr(&bars->p_full[0]), (g00 + j - s0) & 1))) break;
                         ptx::tc_fence_after_sync();
-                        issue_pv(0, iv, j > 0);
+                        issue_pv(0, iv, j > s0);
                     }
                     if (next) {
                         if (!(ok = wait_warp(full_bar(ik), full_par(ik)))) break;
                         ptx::tc_fence_after_sync();
                     }
-                    if (j + 1 < nkv0) issue_s(0, ik);
-                    if (j < nkv1) {
-                        if (!(ok = wait_warp(bar_addr(&bars->p_full[1]), (g10 + j) & 1))) break;
+                    if (j + 1 >= s0 && j + 1 < nkv0) issue_s(0, ik);
+                    if (j >= s1 && j < nkv1) {
+                        if (!(ok = wait_warp(bar_addr(&bars->p_full[1]), (g10 + j - s1) & 1))) break;
                         ptx::tc_fence_after_sync();
-                        issue_pv(1, iv, j > 0);
+                        issue_pv(1, iv, j > s1);
                     }
                     ptx::tc_commit_warp(bar_addr(&bars->kv_empty[iv % NS]));
-                    if (j + 1 < nkv1) issue_s(1, ik);
+                    if (j + 1 >= s1 && j + 1 < nkv1) issue_s(1, ik);
                     if (next) ptx::tc_commit_warp(bar_addr(&bars->kv_empty[ik % NS]));
                 }
-                gs[0] += nkv0;
-                gs[1] += nkv1;
+                gs[0] += max(0, nkv0 - s0);
+                gs[1] += max(0, nkv1 - s1);
                 gi0 = (gi0 + 2 * nkv) % (2 * NS);
             }
             // Every MMA must be complete before TMEM is freed.
@@ -771,11 +798,12 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         for (int k = 0;; ++k) {
             const int w = cta_item(k, p.items);
             if (w < 0) break;
-            const WorkItem it = decode_item<VARLEN>(p, w);
-            if (VARLEN && it.nkv == 0) continue;
+            const WorkItem it = decode_item<GENERAL>(p, w);
+            if (GENERAL && it.nkv == 0) continue;
             const int r0 = it.q0 + t * kBM;
             const int row = r0 + r;
-            const int n_tiles = (t == 0) ? it.nkv0 : it.nkv1;
+            const int s_t = !GENERAL ? 0 : (t == 0) ? it.s0 : it.s1;
+            const int n_tiles = max(0, ((t == 0) ? it.nkv0 : it.nkv1) - s_t);   // key tiles of this tile
 
             float m_use = -INFINITY;   // reference max, raw (unscaled) score units
             float l = 0.f;             // this thread's part of the row sum
@@ -786,13 +814,19 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 if (kBreakOnAbort && !ok) break;
                 ptx::tc_fence_after_sync();
                 uint32_t s[kHalf];
-                const int kv0 = (it.jb + j) * kBN + hf * kHalf;   // key of column 0
+                const int kv0 = (it.jb + s_t + j) * kBN + hf * kHalf;   // key of column 0
                 // Keys past the end and, on diagonal tiles, keys after the row are masked.
                 float alpha = 1.f;
                 bool rescale = false;
                 if constexpr (kRowSplit == 1) {
-                    const bool need_mask = kv0 + kHalf > it.S || (p.causal && kv0 + kHalf - 1 > r0);
-                    const int last = p.causal ? min(it.S - 1, row) : (it.S - 1);
+                    // keys outside [first, last] are masked: past the sequence,
+                    // after the row (causal) or outside the window
+                    const bool need_mask = kv0 + kHalf > it.S || (p.causal && kv0 + kHalf - 1 > r0) ||
+                                           (GENERAL && p.win_left >= 0 && kv0 < r0 + kBM - 1 - p.win_left) ||
+                                           (GENERAL && p.win_right >= 0 && kv0 + kHalf - 1 > r0 + p.win_right);
+                    int last = p.causal ? min(it.S - 1, row) : (it.S - 1);
+                    if (GENERAL && p.win_right >= 0) last = min(last, row + p.win_right);
+                    const int first = (GENERAL && p.win_left >= 0) ? row - p.win_left : -1;
                     constexpr int kChains = 4;
                     float mx[kChains];
 #pragma unroll
@@ -801,7 +835,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                         if (need_mask) {
 #pragma unroll
                             for (int kq = k0; kq < k1; ++kq)
-                                if (kv0 + kq > last) s[kq] = __float_as_uint(-INFINITY);
+                                if (kv0 + kq > last || (GENERAL && kv0 + kq < first)) s[kq] = __float_as_uint(-INFINITY);
                         }
 #pragma unroll
                         for (int kq = k0 / 2; kq < k1 / 2; ++kq)
@@ -887,8 +921,14 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     const float2 sum = __fadd2_rn(sum2[0], sum2[1]);
                     l = l * alpha + (sum.x + sum.y);
                 } else {
-                    const bool need_mask = kv0 + kHalf > it.S || (p.causal && kv0 + kHalf - 1 > r0);
-                    const int last = p.causal ? min(it.S - 1, row) : (it.S - 1);
+                    // keys outside [first, last] are masked: past the sequence,
+                    // after the row (causal) or outside the window
+                    const bool need_mask = kv0 + kHalf > it.S || (p.causal && kv0 + kHalf - 1 > r0) ||
+                                           (GENERAL && p.win_left >= 0 && kv0 < r0 + kBM - 1 - p.win_left) ||
+                                           (GENERAL && p.win_right >= 0 && kv0 + kHalf - 1 > r0 + p.win_right);
+                    int last = p.causal ? min(it.S - 1, row) : (it.S - 1);
+                    if (GENERAL && p.win_right >= 0) last = min(last, row + p.win_right);
+                    const int first = (GENERAL && p.win_left >= 0) ? row - p.win_left : -1;
 #pragma unroll
                     for (int q = 0; q < kHalf / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
                     ptx::tmem_ld_wait();
@@ -901,7 +941,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     if (need_mask) {
 #pragma unroll
                         for (int kq = 0; kq < kHalf; ++kq)
-                            if (kv0 + kq > last) s[kq] = __float_as_uint(-INFINITY);
+                            if (kv0 + kq > last || (GENERAL && kv0 + kq < first)) s[kq] = __float_as_uint(-INFINITY);
                     }
 
                     // One pass over this thread's columns: p = 2^(s*c - mc), two
@@ -971,7 +1011,11 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                         // reference moves up to it.  TMEM stores are warp-wide and
                         // the two threads of a row share its reference, so the pair
                         // of warps on these rows takes one path.
-                        bool with_max = (m_use == -INFINITY) || use_max_next;
+                        // (a row with no key yet -- the first tile, or a window
+                        // that has not reached its keys -- has no reference: a
+                        // warp-wide choice, like everything that feeds the named
+                        // barriers and TMEM stores below)
+                        bool with_max = __any_sync(0xffffffffu, m_use == -INFINITY) || use_max_next;
                         if (!with_max) {
                             exp_pass(m_use * c);
                             with_max = ptx::named_barrier_or(pair_bar, 32 * kRowSplit,
@@ -1079,7 +1123,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 // one thread stores it; rows past S are dropped by the store.
                 // The last tile of a packed sequence is stored row by row
                 // instead (the rows after it belong to the next sequence).
-                const bool direct = VARLEN && r0 + kBM > it.S;
+                const bool direct = GENERAL && p.cu_seqlens != nullptr && r0 + kBM > it.S;
                 uint8_t* stage = smem + L::kOffStage + t * L::kQBytes;
                 if (!kStageInQ && !direct && ki > 0) {
                     // the previous item's store must have read the staging buffer
@@ -1137,8 +1181,9 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 }
                 if (eok && hf == 0 && p.lse != nullptr && row < it.S) {
                     // LSE = scale * m + ln l = ln2 * (m * scale * log2e + log2 l)
-                    const size_t li = VARLEN ? static_cast<size_t>(it.h) * p.total + it.base + row
-                                             : static_cast<size_t>(it.bh) * p.S + row;
+                    const size_t li = (GENERAL && p.cu_seqlens != nullptr)
+                                          ? static_cast<size_t>(it.h) * p.total + it.base + row
+                                          : static_cast<size_t>(it.bh) * p.S + row;
                     p.lse[li] = (m_use * c + log2f(l_row)) * 0.69314718055994530942f;
                 }
             } else if (kStageInQ && store_thread) {

@@ -575,7 +575,45 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
                 "launches": fa.fa_splitkv_launches(w.B, w.H, w.S, w.D, causal)}
         del q, k, v, o, lse, ws
     res.update(varlen_workload(lib, fa, dev, stream, flush, peak))
+    res.update(window_workload(lib, fa, dev, stream, flush, peak))
     return res
+
+
+# Local attention: B2 H16 S16384 D128 bf16, causal, each query sees the 2048
+# keys before it and itself; FLOPs 4*D per visible (query, key) pair.
+WINDOW = dict(B=2, H=16, S=16384, D=128, left=2048, seed=1008)
+
+
+def window_workload(lib, fa, dev, stream, flush, peak):
+    """Kernel-timed TFLOP/s of the sliding-window workload (informational)."""
+    import torch
+    c = WINDOW
+    qb, kb, vb = fa_inputs.make_qkv(c["B"], c["H"], c["S"], c["D"], "bf16", "normal", c["seed"])
+    q, k, v = (fa_inputs.to_torch(x, "bf16").to(dev) for x in (qb, kb, vb))
+    o = torch.empty_like(q)
+    lse = torch.empty((c["B"], c["H"], c["S"]), dtype=torch.float32, device=dev)
+    ms = []
+    with torch.cuda.stream(stream):
+        for i in range(13):
+            flush.fill_(float(i))
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            rc = lib.fa_fwd_local(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), c["B"], c["H"], c["H"], c["S"], c["D"], 1,
+                                  c["left"], -1, c["D"] ** -0.5, fa.FA_BF16, stream.cuda_stream)
+            e1.record(stream)
+            assert rc == 0
+            if i >= 3:
+                ms.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    t = statistics.median(a.elapsed_time(b) for a, b in ms)
+    S, L = c["S"], c["left"]
+    pairs = sum(min(i, L) + 1 for i in range(S))          # visible keys per head
+    flops = 4.0 * c["D"] * pairs * c["B"] * c["H"]
+    tf = flops / (t * 1e-3) / 1e12
+    name = f"window{L}_b{c['B']}h{c['H']}s{S}d{c['D']}/causal"
+    return {name: {"ms": t, "tflops": tf, "pct_of_peak": 100.0 * tf / peak, "launches": 1}}
 
 
 # Packed variable-length batch: 16 sequences of 256..8192 tokens (uniform,

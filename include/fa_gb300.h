@@ -141,6 +141,22 @@ int fa_fwd_gqa_splitkv(const void* Q, const void* K, const void* V, void* O, flo
                        fa_stream_t stream);
 
 /*
+ * Local (sliding-window) attention.  The page "CuTe 详解：以 FlashAttention-2
+ * 拆解 Layout、TiledCopy 与 TiledMMA" names a "causal/local mask" among what a
+ * production FA2 forward also handles (section 哪些结论可以迁移，哪些只是本例
+ * 特例) without a formula; the reading here is the usual one: key j is kept
+ * for query i iff i - window_left <= j <= i + window_right, -1 meaning no
+ * bound on that side, and the causal mask caps the right bound at 0.  Key
+ * tiles outside every row's window of a query tile are neither loaded nor
+ * multiplied.  Arguments and layout as fa_fwd_gqa; the keys are not split
+ * over CTAs.  Errors: as fa_fwd_gqa, and FA_ERR_INVALID_ARG for a window
+ * bound below -1.
+ */
+int fa_fwd_local(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                 int B, int H, int H_kv, int S, int D, int causal, int window_left,
+                 int window_right, float scale, int dtype, fa_stream_t stream);
+
+/*
  * Variable-length batch: B sequences packed along the token axis.  The page
  * "CuTe 详解：以 FlashAttention-2 拆解 Layout、TiledCopy 与 TiledMMA" lists
  * variable-length sequences (变长序列) among what a production FA2 forward
