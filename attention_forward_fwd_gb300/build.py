@@ -51,7 +51,7 @@ KERNEL_LAUNCH_REGS = {1: 168, 2: 96}
 
 
 def _expected_regs(mangled: str) -> int:
-    m = re.search(r"fa_fwd_kernelILi\d+ELb[01]ELi\d+ELi(\d+)(?:ELb[01])?EE", mangled)
+    m = re.search(r"fa_fwd_kernelILi\d+ELb[01]ELi\d+ELi(\d+)(?:ELb[01]|ELi\d+)?EE", mangled)
     if not m:
         raise RuntimeError(f"cannot read the template arguments of {mangled}")
     return KERNEL_LAUNCH_REGS[int(m.group(1))]

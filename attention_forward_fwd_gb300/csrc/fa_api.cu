@@ -136,11 +136,11 @@ size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D) {
     return slots * (static_cast<size_t>(fa::kBM) * D + 2 * fa::kBM) * sizeof(float);
 }
 
-template <int D, bool BF16, int NS, int RS, bool GENERAL>
+template <int D, bool BF16, int NS, int RS, int FEAT>
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
            int S, int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace,
            const int* cu_seqlens, int total, int win_left, int win_right) {
-    auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS, GENERAL>;
+    auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS, FEAT>;
     constexpr int kSmem = fa::SmemLayout<D, NS, RS>::kAlloc;
     // The dynamic shared-memory opt-in is per device; remember it per device.
     static std::once_flag once[64];
@@ -257,15 +257,18 @@ int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, i
              int S, int D, int causal, float scale, int dtype, cudaStream_t st, const SplitPlan& plan,
              void* ws, const int* cu_seqlens = nullptr, int total = 0, int win_left = -1,
              int win_right = -1) {
-    // <head dim, bf16, K/V ring slots, softmax threads per query row, general>:
-    // packed variable-length batches and local windows take the general
-    // variant; the plain one compiles neither
-    const bool general = cu_seqlens != nullptr || win_left >= 0 || win_right >= 0;
-#define FA_LAUNCH(D_, BF16_, NS_, RS_)                                                              \
-    (general ? launch<D_, BF16_, NS_, RS_, true>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st,  \
-                                                plan, ws, cu_seqlens, total, win_left, win_right)                        \
-            : launch<D_, BF16_, NS_, RS_, false>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, \
-                                                 plan, ws, cu_seqlens, total, win_left, win_right))
+    // <head dim, bf16, K/V ring slots, softmax threads per query row, feature>:
+    // packed variable-length batches and local windows have kernel variants of
+    // their own; the plain one compiles neither
+    const int feat = cu_seqlens != nullptr ? fa::kPacked
+                     : (win_left >= 0 || win_right >= 0) ? fa::kLocal : fa::kPlain;
+#define FA_LAUNCH(D_, BF16_, NS_, RS_)                                                                 \
+    (feat == fa::kPacked  ? launch<D_, BF16_, NS_, RS_, fa::kPacked>(Q, K, V, O, LSE, B, H, Hkv, S,  \
+                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right) \
+     : feat == fa::kLocal ? launch<D_, BF16_, NS_, RS_, fa::kLocal>(Q, K, V, O, LSE, B, H, Hkv, S,   \
+                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right) \
+                          : launch<D_, BF16_, NS_, RS_, fa::kPlain>(Q, K, V, O, LSE, B, H, Hkv, S,   \
+                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right))
     if (dtype == FA_F16) {
         if (D == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);
         return FA_LAUNCH(128, false, kRingD128, kRowSplitD128);

@@ -231,7 +231,11 @@ struct WorkItem {
     bool partial;       // the block is split: write partial results
 };
 
-template <bool GENERAL>
+// Kernel variants: the plain batched call, packed variable-length batches,
+// and local (sliding-window) attention; each compiles only its own extras.
+enum Feature : int { kPlain = 0, kPacked = 1, kLocal = 2 };
+
+template <int FEAT>
 __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
     WorkItem it;
     const int bhn = p.B * p.H;
@@ -244,7 +248,7 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
     it.base = 0;
     it.tb = it.b;
     it.bad = false;
-    if (GENERAL && p.cu_seqlens != nullptr) {
+    if constexpr (FEAT == kPacked) {
         const int a = p.cu_seqlens[it.b];
         const int e = p.cu_seqlens[it.b + 1];
         // offsets outside [0, total], decreasing, or a sequence longer than S:
@@ -280,7 +284,7 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
     it.nkv0 = max(0, min(je, key_tiles_for(it.q0, it.S, causal)) - it.jb);
     it.nkv1 = max(0, min(je, key_tiles_for(it.q0 + kBM, it.S, causal)) - it.jb);
     it.s0 = it.s1 = 0;
-    if (GENERAL && (p.win_left >= 0 || p.win_right >= 0)) {
+    if constexpr (FEAT == kLocal) {
         // key tiles [lo_t, hi_t) that query tile t's rows reach (jb is 0 here)
         int lo[kQTiles], hi[kQTiles];
         for (int t = 0; t < kQTiles; ++t) {
@@ -341,7 +345,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-template <int D, bool BF16, int NS, int RS, bool GENERAL>
+template <int D, bool BF16, int NS, int RS, int FEAT>
 __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -467,8 +471,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         for (int k = 0;; ++k) {
             const int w = cta_item(k, p.items);
             if (w < 0) break;
-            const WorkItem it = decode_item<GENERAL>(p, w);
-            if (GENERAL && it.nkv == 0) continue;
+            const WorkItem it = decode_item<FEAT>(p, w);
+            if (FEAT == kPacked && it.nkv == 0) continue;
             load_q(it);
             first_round = min(NS, 2 * it.nkv);
             for (int i = 0; i < first_round; ++i) load_item(it, i, i);
@@ -513,9 +517,9 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             for (int k = 0; ok; ++k) {
                 const int w = cta_item(k, p.items);
                 if (w < 0) break;
-                const WorkItem it = decode_item<GENERAL>(p, w);
-                if (GENERAL && it.bad && lane == 0) atomicCAS(&g_fa_device_status, 0, kStatusBadSeqlens);
-                if (GENERAL && it.nkv == 0) continue;
+                const WorkItem it = decode_item<FEAT>(p, w);
+                if (FEAT == kPacked && it.bad && lane == 0) atomicCAS(&g_fa_device_status, 0, kStatusBadSeqlens);
+                if (FEAT == kPacked && it.nkv == 0) continue;
                 const int n = 2 * it.nkv;
                 int i = 0;
                 if (ki == 0) {
@@ -611,10 +615,10 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             for (int k = 0; ok; ++k) {
                 const int w = cta_item(k, p.items);
                 if (w < 0) break;
-                const WorkItem it = decode_item<GENERAL>(p, w);
-                if (GENERAL && it.nkv == 0) continue;
+                const WorkItem it = decode_item<FEAT>(p, w);
+                if (FEAT == kPacked && it.nkv == 0) continue;
                 const int nkv = it.nkv;
-                const int s_t = !GENERAL ? 0 : (t == 0) ? it.s0 : it.s1;    // key tiles [s_t, n_t)
+                const int s_t = FEAT != kLocal ? 0 : (t == 0) ? it.s0 : it.s1;    // key tiles [s_t, n_t)
                 const int n_t = (t == 0) ? it.nkv0 : it.nkv1;
                 auto used = [&](int j) { return j >= s_t && j < n_t; };
                 const uint32_t gs0 = gs;   // S_t / P_t / P_t V index of this tile's first key tile
@@ -712,10 +716,10 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             for (int k = 0; ok; ++k) {
                 const int w = cta_item(k, p.items);
                 if (w < 0) break;
-                const WorkItem it = decode_item<GENERAL>(p, w);
-                if (GENERAL && it.nkv == 0) continue;
+                const WorkItem it = decode_item<FEAT>(p, w);
+                if (FEAT == kPacked && it.nkv == 0) continue;
                 const int nkv = it.nkv, nkv0 = it.nkv0, nkv1 = it.nkv1;
-                const int s0 = GENERAL ? it.s0 : 0, s1 = GENERAL ? it.s1 : 0;
+                const int s0 = FEAT == kLocal ? it.s0 : 0, s1 = FEAT == kLocal ? it.s1 : 0;
                 const uint32_t g00 = gs[0], g10 = gs[1];
                 if (!(ok = wait_warp(qbar, ki & 1))) break;
                 ++ki;
@@ -798,11 +802,11 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         for (int k = 0;; ++k) {
             const int w = cta_item(k, p.items);
             if (w < 0) break;
-            const WorkItem it = decode_item<GENERAL>(p, w);
-            if (GENERAL && it.nkv == 0) continue;
+            const WorkItem it = decode_item<FEAT>(p, w);
+            if (FEAT == kPacked && it.nkv == 0) continue;
             const int r0 = it.q0 + t * kBM;
             const int row = r0 + r;
-            const int s_t = !GENERAL ? 0 : (t == 0) ? it.s0 : it.s1;
+            const int s_t = FEAT != kLocal ? 0 : (t == 0) ? it.s0 : it.s1;
             const int n_tiles = max(0, ((t == 0) ? it.nkv0 : it.nkv1) - s_t);   // key tiles of this tile
 
             float m_use = -INFINITY;   // reference max, raw (unscaled) score units
@@ -822,11 +826,11 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     // keys outside [first, last] are masked: past the sequence,
                     // after the row (causal) or outside the window
                     const bool need_mask = kv0 + kHalf > it.S || (p.causal && kv0 + kHalf - 1 > r0) ||
-                                           (GENERAL && p.win_left >= 0 && kv0 < r0 + kBM - 1 - p.win_left) ||
-                                           (GENERAL && p.win_right >= 0 && kv0 + kHalf - 1 > r0 + p.win_right);
+                                           (FEAT == kLocal && p.win_left >= 0 && kv0 < r0 + kBM - 1 - p.win_left) ||
+                                           (FEAT == kLocal && p.win_right >= 0 && kv0 + kHalf - 1 > r0 + p.win_right);
                     int last = p.causal ? min(it.S - 1, row) : (it.S - 1);
-                    if (GENERAL && p.win_right >= 0) last = min(last, row + p.win_right);
-                    const int first = (GENERAL && p.win_left >= 0) ? row - p.win_left : -1;
+                    if (FEAT == kLocal && p.win_right >= 0) last = min(last, row + p.win_right);
+                    const int first = (FEAT == kLocal && p.win_left >= 0) ? row - p.win_left : -1;
                     constexpr int kChains = 4;
                     float mx[kChains];
 #pragma unroll
@@ -835,7 +839,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                         if (need_mask) {
 #pragma unroll
                             for (int kq = k0; kq < k1; ++kq)
-                                if (kv0 + kq > last || (GENERAL && kv0 + kq < first)) s[kq] = __float_as_uint(-INFINITY);
+                                if (kv0 + kq > last || (FEAT == kLocal && kv0 + kq < first)) s[kq] = __float_as_uint(-INFINITY);
                         }
 #pragma unroll
                         for (int kq = k0 / 2; kq < k1 / 2; ++kq)
@@ -924,11 +928,11 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     // keys outside [first, last] are masked: past the sequence,
                     // after the row (causal) or outside the window
                     const bool need_mask = kv0 + kHalf > it.S || (p.causal && kv0 + kHalf - 1 > r0) ||
-                                           (GENERAL && p.win_left >= 0 && kv0 < r0 + kBM - 1 - p.win_left) ||
-                                           (GENERAL && p.win_right >= 0 && kv0 + kHalf - 1 > r0 + p.win_right);
+                                           (FEAT == kLocal && p.win_left >= 0 && kv0 < r0 + kBM - 1 - p.win_left) ||
+                                           (FEAT == kLocal && p.win_right >= 0 && kv0 + kHalf - 1 > r0 + p.win_right);
                     int last = p.causal ? min(it.S - 1, row) : (it.S - 1);
-                    if (GENERAL && p.win_right >= 0) last = min(last, row + p.win_right);
-                    const int first = (GENERAL && p.win_left >= 0) ? row - p.win_left : -1;
+                    if (FEAT == kLocal && p.win_right >= 0) last = min(last, row + p.win_right);
+                    const int first = (FEAT == kLocal && p.win_left >= 0) ? row - p.win_left : -1;
 #pragma unroll
                     for (int q = 0; q < kHalf / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
                     ptx::tmem_ld_wait();
@@ -941,7 +945,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     if (need_mask) {
 #pragma unroll
                         for (int kq = 0; kq < kHalf; ++kq)
-                            if (kv0 + kq > last || (GENERAL && kv0 + kq < first)) s[kq] = __float_as_uint(-INFINITY);
+                            if (kv0 + kq > last || (FEAT == kLocal && kv0 + kq < first)) s[kq] = __float_as_uint(-INFINITY);
                     }
 
                     // One pass over this thread's columns: p = 2^(s*c - mc), two
@@ -1123,7 +1127,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 // one thread stores it; rows past S are dropped by the store.
                 // The last tile of a packed sequence is stored row by row
                 // instead (the rows after it belong to the next sequence).
-                const bool direct = GENERAL && p.cu_seqlens != nullptr && r0 + kBM > it.S;
+                const bool direct = FEAT == kPacked && r0 + kBM > it.S;
                 uint8_t* stage = smem + L::kOffStage + t * L::kQBytes;
                 if (!kStageInQ && !direct && ki > 0) {
                     // the previous item's store must have read the staging buffer
@@ -1181,7 +1185,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 }
                 if (eok && hf == 0 && p.lse != nullptr && row < it.S) {
                     // LSE = scale * m + ln l = ln2 * (m * scale * log2e + log2 l)
-                    const size_t li = (GENERAL && p.cu_seqlens != nullptr)
+                    const size_t li = FEAT == kPacked
                                           ? static_cast<size_t>(it.h) * p.total + it.base + row
                                           : static_cast<size_t>(it.bh) * p.S + row;
                     p.lse[li] = (m_use * c + log2f(l_row)) * 0.69314718055994530942f;
