@@ -27,7 +27,7 @@ FA_F16, FA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
                     "fa_device_status", "fa_kernels_per_call", "fa_splitkv_workspace_size",
                     "fa_splitkv_launches", "fa_fwd_splitkv", "fa_fwd_gqa", "fa_fwd_gqa_splitkv",
-                    "fa_fwd_varlen", "fa_fwd_local")
+                    "fa_fwd_varlen", "fa_fwd_local", "fa_selftest_timeout")
 
 _LIB = None
 
@@ -76,6 +76,8 @@ def library() -> ctypes.CDLL:
         # ..., B, H, H_kv, S, D, causal, window_left, window_right, scale, dtype, stream
         lib.fa_fwd_local.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_local.restype = i
+        lib.fa_selftest_timeout.argtypes = [vp, vp, vp, vp, i, i, i, vp]
+        lib.fa_selftest_timeout.restype = i
         _LIB = lib
     return _LIB
 

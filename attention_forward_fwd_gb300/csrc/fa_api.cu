@@ -139,7 +139,7 @@ size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D) {
 template <int D, bool BF16, int NS, int RS, int FEAT>
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
            int S, int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace,
-           const int* cu_seqlens, int total, int win_left, int win_right) {
+           const int* cu_seqlens, int total, int win_left, int win_right, int drop_first_q) {
     auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS, FEAT>;
     constexpr int kSmem = fa::SmemLayout<D, NS, RS>::kAlloc;
     // The dynamic shared-memory opt-in is per device; remember it per device.
@@ -170,6 +170,7 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.cu_seqlens = cu_seqlens;
     p.win_left = win_left;
     p.win_right = win_right;
+    p.drop_first_q = drop_first_q;
     p.total = total;
     p.o_ptr = O;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
@@ -256,7 +257,7 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
 int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
              int S, int D, int causal, float scale, int dtype, cudaStream_t st, const SplitPlan& plan,
              void* ws, const int* cu_seqlens = nullptr, int total = 0, int win_left = -1,
-             int win_right = -1) {
+             int win_right = -1, int drop_first_q = 0) {
     // <head dim, bf16, K/V ring slots, softmax threads per query row, feature>:
     // packed variable-length batches and local windows have kernel variants of
     // their own; the plain one compiles neither
@@ -264,11 +265,11 @@ int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, i
                      : (win_left >= 0 || win_right >= 0) ? fa::kLocal : fa::kPlain;
 #define FA_LAUNCH(D_, BF16_, NS_, RS_)                                                                 \
     (feat == fa::kPacked  ? launch<D_, BF16_, NS_, RS_, fa::kPacked>(Q, K, V, O, LSE, B, H, Hkv, S,  \
-                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right) \
+                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right, drop_first_q) \
      : feat == fa::kLocal ? launch<D_, BF16_, NS_, RS_, fa::kLocal>(Q, K, V, O, LSE, B, H, Hkv, S,   \
-                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right) \
+                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right, drop_first_q) \
                           : launch<D_, BF16_, NS_, RS_, fa::kPlain>(Q, K, V, O, LSE, B, H, Hkv, S,   \
-                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right))
+                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right, drop_first_q))
     if (dtype == FA_F16) {
         if (D == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);
         return FA_LAUNCH(128, false, kRingD128, kRowSplitD128);
@@ -400,6 +401,15 @@ int fa_device_status(int clear) {
 }
 
 int fa_kernels_per_call(void) { return 1; }
+
+int fa_selftest_timeout(const void* Q, const void* K, const void* V, void* O, int S, int D, int dtype,
+                        fa_stream_t stream) {
+    const int v = validate(Q, K, V, O, nullptr, 1, 1, S, D, 1.f, dtype);
+    if (v != FA_OK) return v;
+    return dispatch(Q, K, V, O, nullptr, 1, 1, 1, S, D, 0, D == 64 ? 0.125f : 0.08838835f, dtype,
+                    reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr,
+                    nullptr, 0, -1, -1, /*drop_first_q=*/1);
+}
 
 }  // extern "C"
 

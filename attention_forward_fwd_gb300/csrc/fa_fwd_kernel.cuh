@@ -116,6 +116,10 @@ struct FwdParams {
     const int* cu_seqlens;
     int total;
     void* o_ptr;        // O, for the row-by-row stores of a sequence's last tile
+    // Test support (fa_selftest_timeout): 1 = the first item's Q is never
+    // loaded, so the waits on it run out and the kernel must end in the
+    // timeout status instead of hanging.  0 in every other call.
+    int drop_first_q;
     // Work items: the (query block, split) pairs of every head, numbered
     // w = y * (B*H) + b*H + h with y the block's visit index (heaviest first
     // when causal).  Each CTA runs items blockIdx.x, 2G-1-blockIdx.x,
@@ -473,7 +477,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             if (w < 0) break;
             const WorkItem it = decode_item<FEAT>(p, w);
             if (FEAT == kPacked && it.nkv == 0) continue;
-            load_q(it);
+            if (!p.drop_first_q) load_q(it);
             first_round = min(NS, 2 * it.nkv);
             for (int i = 0; i < first_round; ++i) load_item(it, i, i);
             break;

@@ -141,6 +141,17 @@ int fa_fwd_gqa_splitkv(const void* Q, const void* K, const void* V, void* O, flo
                        fa_stream_t stream);
 
 /*
+ * Test support: runs the forward (B = H = 1, non-causal) with the first
+ * query tile's load withheld, so that the waits on it can never complete.
+ * Every such wait gives up after about a second and the kernel ends early;
+ * fa_device_status() then reports FA_ERR_TIMEOUT and the CUDA context stays
+ * usable.  O is left undefined.  Errors before launch as fa_fwd.  Not part of
+ * the attention computation; the pages have no counterpart.
+ */
+int fa_selftest_timeout(const void* Q, const void* K, const void* V, void* O, int S, int D,
+                        int dtype, fa_stream_t stream);
+
+/*
  * Local (sliding-window) attention.  The page "CuTe 详解：以 FlashAttention-2
  * 拆解 Layout、TiledCopy 与 TiledMMA" names a "causal/local mask" among what a
  * production FA2 forward also handles (section 哪些结论可以迁移，哪些只是本例

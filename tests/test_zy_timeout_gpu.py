@@ -1,0 +1,44 @@
+"""The bounded waits end a kernel whose input never arrives in a timeout
+status instead of a hang, and the CUDA context stays usable.  The test
+support call withholds the first query tile's load; no GPU fault is made.
+(Collected late: it leaves a device status behind until it clears it.)"""
+import time
+
+import numpy as np
+import pytest
+
+import fa_inputs
+from oracle import attention_reference
+
+from gpu_common import assert_close, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.timeout(120)
+@pytest.mark.parametrize("D,dtype", [(64, "f16"), (128, "bf16"), (128, "f16"), (64, "bf16")])
+def test_withheld_load_ends_in_timeout_not_a_hang(D, dtype):
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    fa.build()
+    fa.fa_device_status(clear=True)
+    S = 512
+    q = torch.zeros(1, S, 1, D, dtype=torch.float16 if dtype == "f16" else torch.bfloat16,
+                    device="cuda")
+    o = torch.empty_like(q)
+    code = fa.FA_F16 if dtype == "f16" else fa.FA_BF16
+    t0 = time.time()
+    rc = fa.library().fa_selftest_timeout(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(),
+                                          S, D, code, None)
+    assert rc == fa.FA_OK
+    status = fa.fa_device_status(clear=True)
+    elapsed = time.time() - t0
+    assert status == fa.FA_ERR_TIMEOUT, status
+    assert elapsed < 30.0, elapsed                      # seconds, not a hang
+    assert fa.fa_device_status(clear=False) == fa.FA_OK
+    # the context is still usable: a normal call afterwards is exact
+    qb, kb, vb = fa_inputs.make_qkv(1, 2, 300, D, dtype, "normal", 80)
+    O, L = run_gpu(qb, kb, vb, dtype, True, D ** -0.5)
+    Oref, Lref = attention_reference(qb, kb, vb, dtype, True, D ** -0.5)
+    assert_close(O, L, Oref, Lref, dtype, "after the timeout")
+    assert fa.fa_device_status(clear=False) == fa.FA_OK
