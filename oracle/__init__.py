@@ -8,3 +8,6 @@ from .attention import (  # noqa: F401
     attention_reference, attention_reference_f64, attention_rows,
     softmax_probabilities, online_softmax_attention, attention_reference_varlen,
 )
+from .dropout import (  # noqa: F401
+    philox4x32_10, dropout_keep, dropout_threshold, attention_reference_dropout,
+)

@@ -587,3 +587,68 @@ def test_window_rows_match_full_reference():
     rows = [0, 5, 36, 37, 38, 299]
     o, l = attention_rows(qb, kb, vb, "f16", True, 0.125, 0, 3, rows, window=(37, -1))
     assert np.array_equal(o, O[0, rows, 3]) and np.array_equal(l, L[0, 3, rows])
+
+
+# ------------------------------------------------------ dropout
+from oracle import attention_reference_dropout, dropout_keep, philox4x32_10  # noqa: E402
+
+
+@pytest.mark.parametrize("ctr,key,want", [
+    ((0, 0, 0, 0), (0, 0), (0x6627e8d5, 0xe169c58d, 0xbc57ac4c, 0x9b00dbd8)),
+    ((0xffffffff,) * 4, (0xffffffff,) * 2, (0x408f276d, 0x41c83b0e, 0xa20bc7c6, 0x6d5451fd)),
+    ((0x243f6a88, 0x85a308d3, 0x13198a2e, 0x03707344), (0xa4093822, 0x299f31d0),
+     (0xd16cfe09, 0x94fdcceb, 0x5001e420, 0x24126ea1)),
+])
+def test_philox_known_answer_vectors(ctr, key, want):
+    """Philox4x32-10 against the known-answer vectors published with the
+    generator (Random123 distribution)."""
+    got = philox4x32_10(*[np.array([c]) for c in ctr], *key)
+    assert tuple(int(w[0]) for w in got) == want
+
+
+def test_dropout_zero_probability_is_the_plain_definition():
+    qb, kb, vb = fa_inputs.make_qkv(1, 3, 90, 64, "f16", "normal", 51, h_kv=1)
+    for causal in (False, True):
+        O, L = attention_reference(qb, kb, vb, "f16", causal, 0.125)
+        Od, Ld = attention_reference_dropout(qb, kb, vb, "f16", causal, 0.125, 0.0, 1234)
+        assert np.allclose(Od, O, rtol=0, atol=1e-13) and np.array_equal(Ld, L)
+
+
+def test_dropout_keeps_the_lse_and_the_expected_fraction():
+    qb, kb, vb = fa_inputs.make_qkv(1, 2, 256, 64, "f16", "normal", 52)
+    _, L = attention_reference(qb, kb, vb, "f16", True, 0.125)
+    for p in (0.1, 0.5, 0.9):
+        _, Ld = attention_reference_dropout(qb, kb, vb, "f16", True, 0.125, p, 99)
+        assert np.array_equal(Ld, L)
+        keep = dropout_keep(2, 3, 256, p, 7)
+        n = keep.size
+        assert abs(keep.mean() - (1 - p)) < 5 * math.sqrt(p * (1 - p) / n), p
+
+
+def test_dropout_is_unbiased_over_seeds():
+    """The mean of O over many seeds approaches the undropped O."""
+    qb, kb, vb = fa_inputs.make_qkv(1, 1, 24, 64, "f16", "normal", 53)
+    O, _ = attention_reference(qb, kb, vb, "f16", False, 0.125)
+    acc = np.zeros_like(O)
+    n = 400
+    for s in range(n):
+        acc += attention_reference_dropout(qb, kb, vb, "f16", False, 0.125, 0.3, 1000 + s)[0]
+    assert np.abs(acc / n - O).max() < 0.06
+
+
+def test_dropout_mask_read_back_through_one_hot_values():
+    """V row j = e_j makes O[i, j] = P_ij keep_ij / (1 - p): the applied mask
+    is exactly dropout_keep at (row i, key j) -- not its transpose."""
+    S, D, p, seed = 48, 64, 0.4, 0x1234_5678_9ABC
+    qb, kb, _ = fa_inputs.make_qkv(1, 2, S, D, "f16", "normal", 54)
+    v = np.zeros((1, S, 2, D), dtype=np.float32)
+    for j in range(S):
+        v[0, j, :, j] = 1.0
+    vb = fa_inputs.f32_to_bits(v, "f16")
+    for causal in (False, True):
+        O, _ = attention_reference_dropout(qb, kb, vb, "f16", causal, 0.125, p, seed)
+        keep = dropout_keep(1, 2, S, p, seed)
+        vis = np.tril(np.ones((S, S), dtype=bool)) if causal else np.ones((S, S), dtype=bool)
+        for h in range(2):
+            got = O[0, :, h, :S] != 0
+            assert np.array_equal(got, keep[0, h] & vis), (causal, h)
