@@ -17,7 +17,7 @@ __all__ = ["fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
            "fa_device_status", "fa_kernels_per_call", "attention_forward",
            "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_launches",
            "fa_fwd_gqa", "fa_fwd_gqa_splitkv", "fa_fwd_varlen", "attention_forward_varlen",
-           "fa_fwd_local",
+           "fa_fwd_local", "fa_fwd_dropout",
            "FaError", "library", "EXPORTED_SYMBOLS", "FA_F16", "FA_BF16"]
 
 (FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT,
@@ -27,7 +27,7 @@ FA_F16, FA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
                     "fa_device_status", "fa_kernels_per_call", "fa_splitkv_workspace_size",
                     "fa_splitkv_launches", "fa_fwd_splitkv", "fa_fwd_gqa", "fa_fwd_gqa_splitkv",
-                    "fa_fwd_varlen", "fa_fwd_local", "fa_selftest_timeout")
+                    "fa_fwd_varlen", "fa_fwd_local", "fa_selftest_timeout", "fa_fwd_dropout")
 
 _LIB = None
 
@@ -77,6 +77,10 @@ def library() -> ctypes.CDLL:
         lib.fa_fwd_local.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_local.restype = i
         lib.fa_selftest_timeout.argtypes = [vp, vp, vp, vp, i, i, i, vp]
+        # ..., B, H, H_kv, S, D, causal, p_drop, seed, scale, dtype, stream
+        lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_double,
+                                       ctypes.c_ulonglong, f, i, vp]
+        lib.fa_fwd_dropout.restype = i
         lib.fa_selftest_timeout.restype = i
         _LIB = lib
     return _LIB
@@ -154,6 +158,15 @@ def fa_fwd_local(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, window_left, window_
                                       float(scale), int(dtype), stream))
 
 
+def fa_fwd_dropout(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, p_drop, seed, scale, dtype,
+                   stream) -> int:
+    """Raw C-ABI call with attention dropout (probability p_drop, Philox seed)."""
+    return int(library().fa_fwd_dropout(Q, K, V, O, LSE, int(B), int(H), int(H_kv), int(S), int(D),
+                                        int(bool(causal)), float(p_drop),
+                                        int(seed) & 0xFFFFFFFFFFFFFFFF, float(scale), int(dtype),
+                                        stream))
+
+
 def fa_fwd_varlen(Q, K, V, O, LSE, cu_seqlens, B, max_seqlen, total, H, H_kv, D, causal, scale,
                   dtype, stream) -> int:
     """Raw C-ABI call on a packed variable-length batch; returns the status."""
@@ -179,7 +192,8 @@ def _workspace(device, stream_handle: int, nbytes: int):
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
                       out=None, lse=None, with_lse: bool = True, stream=None,
-                      split_kv: bool = True, window=None):
+                      split_kv: bool = True, window=None, dropout_p: float = 0.0,
+                      seed: int = 0):
     """O, LSE for torch CUDA tensors q [B, S, H, D] and k, v [B, S, H_kv, D].
 
     q, k, v must be contiguous fp16 or bf16 tensors on the same CUDA device;
@@ -191,6 +205,10 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     workspace is allocated with torch and cached per device and stream).
     ``window = (left, right)`` restricts query i to keys i - left .. i + right
     (-1: no bound on that side); windowed calls are not split.
+    ``dropout_p > 0`` drops each probability with that chance (the mask is a
+    function of ``seed`` and the element's batch, head, row and key) and
+    scales the kept ones by 1 / (1 - dropout_p); LSE stays the undropped one.
+    Dropout calls are not split and do not combine with ``window``.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -206,6 +224,10 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         raise ValueError("k, v must match q in B, S, D, with H_kv dividing H")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
+    if not (0.0 <= dropout_p < 1.0):
+        raise ValueError("dropout_p must be in [0, 1)")
+    if dropout_p > 0.0 and window is not None:
+        raise ValueError("dropout does not combine with a window")
     B, S, H, D = q.shape
     H_kv = k.shape[2]
     if scale is None:
@@ -223,8 +245,12 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     with torch.cuda.device(q.device):
         st = torch.cuda.current_stream().cuda_stream if stream is None else int(stream)
         lse_ptr = lse.data_ptr() if lse is not None else None
-        nbytes = fa_splitkv_workspace_size(B, H, S, D, causal) if split_kv and window is None else 0
-        if window is not None:
+        nbytes = (fa_splitkv_workspace_size(B, H, S, D, causal)
+                  if split_kv and window is None and dropout_p == 0.0 else 0)
+        if dropout_p > 0.0:
+            rc = fa_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                                B, H, H_kv, S, D, causal, dropout_p, seed, scale, dtype, st)
+        elif window is not None:
             rc = fa_fwd_local(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
                               B, H, H_kv, S, D, causal, int(window[0]), int(window[1]), scale,
                               dtype, st)

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -136,10 +137,24 @@ size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D) {
     return slots * (static_cast<size_t>(fa::kBM) * D + 2 * fa::kBM) * sizeof(float);
 }
 
+// What a call adds to the plain batched forward (one at a time).
+struct Options {
+    const int* cu_seqlens = nullptr;   // packed variable-length batch
+    int total = 0;
+    int win_left = -1, win_right = -1; // local attention
+    bool dropout = false;              // attention dropout
+    unsigned long long seed = 0;
+    uint32_t drop_threshold = 0;
+    float drop_inv_keep = 1.f;
+    int drop_first_q = 0;              // test support: the first Q load is withheld
+};
+
 template <int D, bool BF16, int NS, int RS, int FEAT>
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
            int S, int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace,
-           const int* cu_seqlens, int total, int win_left, int win_right, int drop_first_q) {
+           const Options& opt) {
+    const int* cu_seqlens = opt.cu_seqlens;
+    const int total = opt.total;
     auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS, FEAT>;
     constexpr int kSmem = fa::SmemLayout<D, NS, RS>::kAlloc;
     // The dynamic shared-memory opt-in is per device; remember it per device.
@@ -168,9 +183,13 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.causal = causal ? 1 : 0;
     p.kv_group = H / Hkv;
     p.cu_seqlens = cu_seqlens;
-    p.win_left = win_left;
-    p.win_right = win_right;
-    p.drop_first_q = drop_first_q;
+    p.win_left = opt.win_left;
+    p.win_right = opt.win_right;
+    p.drop_first_q = opt.drop_first_q;
+    p.drop_seed_lo = static_cast<uint32_t>(opt.seed & 0xffffffffull);
+    p.drop_seed_hi = static_cast<uint32_t>(opt.seed >> 32);
+    p.drop_threshold = opt.drop_threshold;
+    p.drop_inv_keep = opt.drop_inv_keep;
     p.total = total;
     p.o_ptr = O;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
@@ -256,20 +275,20 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
 
 int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
              int S, int D, int causal, float scale, int dtype, cudaStream_t st, const SplitPlan& plan,
-             void* ws, const int* cu_seqlens = nullptr, int total = 0, int win_left = -1,
-             int win_right = -1, int drop_first_q = 0) {
+             void* ws, const Options& opt = Options()) {
     // <head dim, bf16, K/V ring slots, softmax threads per query row, feature>:
-    // packed variable-length batches and local windows have kernel variants of
-    // their own; the plain one compiles neither
-    const int feat = cu_seqlens != nullptr ? fa::kPacked
-                     : (win_left >= 0 || win_right >= 0) ? fa::kLocal : fa::kPlain;
-#define FA_LAUNCH(D_, BF16_, NS_, RS_)                                                                 \
-    (feat == fa::kPacked  ? launch<D_, BF16_, NS_, RS_, fa::kPacked>(Q, K, V, O, LSE, B, H, Hkv, S,  \
-                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right, drop_first_q) \
-     : feat == fa::kLocal ? launch<D_, BF16_, NS_, RS_, fa::kLocal>(Q, K, V, O, LSE, B, H, Hkv, S,   \
-                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right, drop_first_q) \
-                          : launch<D_, BF16_, NS_, RS_, fa::kPlain>(Q, K, V, O, LSE, B, H, Hkv, S,   \
-                                causal, scale, st, plan, ws, cu_seqlens, total, win_left, win_right, drop_first_q))
+    // packed variable-length batches, local windows and dropout have kernel
+    // variants of their own; the plain one compiles none of them
+    const int feat = opt.cu_seqlens != nullptr ? fa::kPacked
+                     : (opt.win_left >= 0 || opt.win_right >= 0) ? fa::kLocal
+                     : opt.dropout ? fa::kDropout : fa::kPlain;
+#define FA_ONE(D_, BF16_, NS_, RS_, F_) \
+    launch<D_, BF16_, NS_, RS_, F_>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, plan, ws, opt)
+#define FA_LAUNCH(D_, BF16_, NS_, RS_)                                    \
+    (feat == fa::kPacked    ? FA_ONE(D_, BF16_, NS_, RS_, fa::kPacked)    \
+     : feat == fa::kLocal   ? FA_ONE(D_, BF16_, NS_, RS_, fa::kLocal)     \
+     : feat == fa::kDropout ? FA_ONE(D_, BF16_, NS_, RS_, fa::kDropout)   \
+                            : FA_ONE(D_, BF16_, NS_, RS_, fa::kPlain))
     if (dtype == FA_F16) {
         if (D == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);
         return FA_LAUNCH(128, false, kRingD128, kRowSplitD128);
@@ -277,6 +296,7 @@ int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     if (D == 64) return FA_LAUNCH(64, true, kRingD64, kRowSplitD64);
     return FA_LAUNCH(128, true, kRingD128, kRowSplitD128);
 #undef FA_LAUNCH
+#undef FA_ONE
 }
 
 }  // namespace
@@ -307,9 +327,29 @@ int fa_fwd_local(const void* Q, const void* K, const void* V, void* O, float* LS
     if (v != FA_OK) return v;
     if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+    Options opt;
+    opt.win_left = window_left;
+    opt.win_right = window_right;
     return dispatch(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype,
-                    reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr,
-                    nullptr, 0, window_left, window_right);
+                    reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr, opt);
+}
+
+int fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                   int H_kv, int S, int D, int causal, double p_drop, unsigned long long seed,
+                   float scale, int dtype, fa_stream_t stream) {
+    const int v = validate(Q, K, V, O, LSE, B, H, S, D, scale, dtype);
+    if (v != FA_OK) return v;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if (!(p_drop >= 0.0 && p_drop < 1.0)) return FA_ERR_INVALID_ARG;
+    Options opt;
+    opt.dropout = true;
+    opt.seed = seed;
+    // keep iff the generator word >= floor(p * 2^32)
+    const double t = std::floor(p_drop * 4294967296.0);
+    opt.drop_threshold = static_cast<uint32_t>(std::min(t, 4294967295.0));
+    opt.drop_inv_keep = static_cast<float>(1.0 / (1.0 - p_drop));
+    return dispatch(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype,
+                    reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr, opt);
 }
 
 int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
@@ -323,9 +363,12 @@ int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* L
     if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) return FA_ERR_UNSUPPORTED;
     const long long nqb = (static_cast<long long>(max_seqlen) + 255) / 256;
     if (static_cast<long long>(B) * H * nqb > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    Options opt;
+    opt.cu_seqlens = cu_seqlens;
+    opt.total = total;
     return dispatch(Q, K, V, O, LSE, B, H, H_kv, max_seqlen, D, causal, scale, dtype,
                     reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, static_cast<int>(nqb)},
-                    nullptr, cu_seqlens, total);
+                    nullptr, opt);
 }
 
 int fa_splitkv_workspace_size(int B, int H, int S, int D, int causal, size_t* bytes) {
@@ -406,9 +449,10 @@ int fa_selftest_timeout(const void* Q, const void* K, const void* V, void* O, in
                         fa_stream_t stream) {
     const int v = validate(Q, K, V, O, nullptr, 1, 1, S, D, 1.f, dtype);
     if (v != FA_OK) return v;
+    Options opt;
+    opt.drop_first_q = 1;
     return dispatch(Q, K, V, O, nullptr, 1, 1, 1, S, D, 0, D == 64 ? 0.125f : 0.08838835f, dtype,
-                    reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr,
-                    nullptr, 0, -1, -1, /*drop_first_q=*/1);
+                    reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr, opt);
 }
 
 }  // extern "C"

@@ -120,6 +120,14 @@ struct FwdParams {
     // loaded, so the waits on it run out and the kernel must end in the
     // timeout status instead of hanging.  0 in every other call.
     int drop_first_q;
+    // Attention dropout (dropout variant only): P(i, j) of head (b, h) is kept
+    // iff the Philox4x32-10 word for it is >= drop_threshold (floor(p * 2^32));
+    // the key is the 64-bit seed, the counter (j / 4, i, h, b) and word j % 4.
+    // Kept values are scaled by drop_inv_keep = 1 / (1 - p); the row sum and
+    // LSE are those of the undropped softmax.
+    uint32_t drop_seed_lo, drop_seed_hi;
+    uint32_t drop_threshold;
+    float drop_inv_keep;
     // Work items: the (query block, split) pairs of every head, numbered
     // w = y * (B*H) + b*H + h with y the block's visit index (heaviest first
     // when causal).  Each CTA runs items blockIdx.x, 2G-1-blockIdx.x,
@@ -236,8 +244,29 @@ struct WorkItem {
 };
 
 // Kernel variants: the plain batched call, packed variable-length batches,
-// and local (sliding-window) attention; each compiles only its own extras.
-enum Feature : int { kPlain = 0, kPacked = 1, kLocal = 2 };
+// local (sliding-window) attention and attention dropout; each compiles only
+// its own extras.
+enum Feature : int { kPlain = 0, kPacked = 1, kLocal = 2, kDropout = 3 };
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC 2011): ten rounds of two 32x32 -> 64-bit products,
+// the key bumped by the Weyl constants between rounds.
+struct Philox4 { uint32_t x, y, z, w; };
+
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 uint32_t k0, uint32_t k1) {
+    constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+    constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t hi0 = __umulhi(kM0, c0), lo0 = kM0 * c0;
+        const uint32_t hi1 = __umulhi(kM1, c2), lo1 = kM1 * c2;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+        k0 += kW0; k1 += kW1;
+    }
+    return Philox4{c0, c1, c2, c3};
+}
 
 template <int FEAT>
 __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
@@ -346,6 +375,26 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     } else {
         __half2 v = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// Packs the probabilities of keys col, col + 1 of query row `row` for P V.
+// With dropout, a dropped one is packed as 0 (the caller's row sum keeps it):
+// keys 4g .. 4g + 3 share one Philox block, drawn at the even pair (odd = 0,
+// col = 4g) into `rnd` and read at the odd one (odd = 1, col = 4g + 2).  The
+// callers' loops are unrolled, so `odd` is known at compile time.
+template <int FEAT, bool BF16>
+__device__ __forceinline__ uint32_t pack_p(const FwdParams& p, float2 pp, int col, int odd, int row,
+                                           const WorkItem& it, Philox4& rnd) {
+    if constexpr (FEAT == kDropout) {
+        if (!odd)
+            rnd = philox4x32_10(static_cast<uint32_t>(col) >> 2, static_cast<uint32_t>(row),
+                                static_cast<uint32_t>(it.h), static_cast<uint32_t>(it.b),
+                                p.drop_seed_lo, p.drop_seed_hi);
+        const uint32_t w0 = odd ? rnd.z : rnd.x, w1 = odd ? rnd.w : rnd.y;
+        return pack2<BF16>(w0 >= p.drop_threshold ? pp.x : 0.f, w1 >= p.drop_threshold ? pp.y : 0.f);
+    } else {
+        return pack2<BF16>(pp.x, pp.y);
     }
 }
 
@@ -886,6 +935,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < kHalf / 32; ++q) {
                         uint32_t pk[16];
+                        Philox4 rnd;
 #pragma unroll
                         for (int kq = 0; kq < 16; ++kq) {
                             const float2 x = __ffma2_rn(
@@ -894,7 +944,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                                 c2, nmc2);
                             const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
                             sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
-                            pk[kq] = pack2<BF16>(pp.x, pp.y);
+                            pk[kq] = pack_p<FEAT, BF16>(p, pp, kv0 + q * 32 + 2 * kq, kq & 1, row, it, rnd);
                         }
                         if (kSepP && q == 0 && j > 0 && ok) {
                             // P_t and O_t are still read / written by P_t V of tile j-1
@@ -964,6 +1014,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
 #pragma unroll
                         for (int q = 0; q < kHalf / 32; ++q) {
                             uint32_t pk[16];
+                            Philox4 rnd;
 #pragma unroll
                             for (int kq = 0; kq < 16; ++kq) {
                                 const float2 x = __ffma2_rn(
@@ -972,7 +1023,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                                     c2, nmc2);
                                 const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
                                 sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
-                                pk[kq] = pack2<BF16>(pp.x, pp.y);
+                                pk[kq] = pack_p<FEAT, BF16>(p, pp, kv0 + q * 32 + 2 * kq, kq & 1, row, it, rnd);
                             }
                             if (!p_free && ok) {
                                 // P_t and O_t are still read / written by P_t V of tile j-1
@@ -1138,7 +1189,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     if (store_thread) ptx::bulk_wait_group_read_all();
                     ptx::named_barrier_sync(tile_bar, kTileThreads);
                 }
-                const float inv_l = 1.f / l_row;
+                float inv_l = 1.f / l_row;
+                if constexpr (FEAT == kDropout) inv_l *= p.drop_inv_keep;   // kept P scaled by 1 / (1 - p)
                 uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +
                                  (static_cast<size_t>(it.base + row) * p.H + it.h) * D;
                 if (eok) {

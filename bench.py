@@ -576,6 +576,54 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
         del q, k, v, o, lse, ws
     res.update(varlen_workload(lib, fa, dev, stream, flush, peak))
     res.update(window_workload(lib, fa, dev, stream, flush, peak))
+    res.update(dropout_workloads(lib, fa, dev, stream, flush, peak))
+    return res
+
+
+def _median_kernel_ms(stream, flush, call):
+    """Median CUDA-event time of call() over 10 runs after 3 warm-ups, L2
+    flushed before each."""
+    import torch
+    ms = []
+    with torch.cuda.stream(stream):
+        for i in range(13):
+            flush.fill_(float(i))
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            rc = call()
+            e1.record(stream)
+            assert rc == 0, rc
+            if i >= 3:
+                ms.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ms)
+
+
+# Attention dropout, p = 0.1: the b4h16 (D = 64 fp16) and b2h16d128 (D = 128
+# bf16) shapes, causal; FLOPs as the plain forward (the mask is extra work).
+DROPOUT = dict(p=0.1, seed=1009, workloads=("b4h16", "b2h16d128"))
+
+
+def dropout_workloads(lib, fa, dev, stream, flush, peak):
+    """Kernel-timed TFLOP/s of the dropout variant (informational)."""
+    import torch
+    res = {}
+    for name in DROPOUT["workloads"]:
+        w = fa_inputs.WORKLOADS[name]
+        qb, kb, vb = fa_inputs.make_qkv_for(w)
+        q, k, v = (fa_inputs.to_torch(x, w.dtype).to(dev) for x in (qb, kb, vb))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+        code = fa.FA_F16 if w.dtype == "f16" else fa.FA_BF16
+        t = _median_kernel_ms(stream, flush, lambda: lib.fa_fwd_dropout(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H,
+            w.kv_heads, w.S, w.D, 1, DROPOUT["p"], DROPOUT["seed"], w.scale, code,
+            stream.cuda_stream))
+        tf = fa_inputs.attention_flops(w.B, w.H, w.S, w.D, True) / (t * 1e-3) / 1e12
+        res[f"dropout{DROPOUT['p']}_{name}/causal"] = {
+            "ms": t, "tflops": tf, "pct_of_peak": 100.0 * tf / peak, "launches": 1}
+        del q, k, v, o, lse
     return res
 
 

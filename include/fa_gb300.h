@@ -152,6 +152,28 @@ int fa_selftest_timeout(const void* Q, const void* K, const void* V, void* O, in
                         int dtype, fa_stream_t stream);
 
 /*
+ * Attention dropout.  The page "CuTe 详解：以 FlashAttention-2 拆解 Layout、
+ * TiledCopy 与 TiledMMA" lists dropout among what a production FA2 forward
+ * also handles (section 哪些结论可以迁移，哪些只是本例特例) without a formula;
+ * the reading here is the usual inverted dropout: each probability P_ij of
+ * head (b, h) is kept with probability 1 - p_drop and the kept ones are scaled
+ * by 1 / (1 - p_drop) before they multiply V.  The max, the row sums and LSE
+ * are those of the undropped softmax.
+ *
+ * The mask is a pure function of (seed, b, h, i, j): element (b, h, i, j) takes
+ * word j mod 4 of the Philox4x32-10 block (Salmon et al., "Parallel random
+ * numbers: as easy as 1, 2, 3", SC 2011) with counter (j / 4, i, h, b) and key
+ * (seed mod 2^32, seed / 2^32), and is kept iff that word >= floor(p_drop *
+ * 2^32).  So p_drop = 0 keeps everything and gives fa_fwd_gqa's result bit for
+ * bit.  Arguments and layout as fa_fwd_gqa (LSE may be NULL); the keys are not
+ * split over CTAs.  Errors: as fa_fwd_gqa, and FA_ERR_INVALID_ARG unless
+ * 0 <= p_drop < 1.
+ */
+int fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                   int B, int H, int H_kv, int S, int D, int causal, double p_drop,
+                   unsigned long long seed, float scale, int dtype, fa_stream_t stream);
+
+/*
  * Local (sliding-window) attention.  The page "CuTe 详解：以 FlashAttention-2
  * 拆解 Layout、TiledCopy 与 TiledMMA" names a "causal/local mask" among what a
  * production FA2 forward also handles (section 哪些结论可以迁移，哪些只是本例
