@@ -344,9 +344,10 @@ int fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* 
     Options opt;
     opt.dropout = true;
     opt.seed = seed;
-    // keep iff the generator word >= floor(p * 2^32)
-    const double t = std::floor(p_drop * 4294967296.0);
-    opt.drop_threshold = static_cast<uint32_t>(std::min(t, 4294967295.0));
+    // keep iff the 16-bit draw >= floor(p * 2^16); the kernel compares it
+    // in the upper half of a 32-bit word
+    const double t = std::min(std::floor(p_drop * 65536.0), 65535.0);
+    opt.drop_threshold = static_cast<uint32_t>(t) << 16;
     opt.drop_inv_keep = static_cast<float>(1.0 / (1.0 - p_drop));
     return dispatch(Q, K, V, O, LSE, B, H, H_kv, S, D, causal, scale, dtype,
                     reinterpret_cast<cudaStream_t>(stream), SplitPlan{0, 1, (S + 255) / 256}, nullptr, opt);

@@ -120,11 +120,12 @@ struct FwdParams {
     // loaded, so the waits on it run out and the kernel must end in the
     // timeout status instead of hanging.  0 in every other call.
     int drop_first_q;
-    // Attention dropout (dropout variant only): P(i, j) of head (b, h) is kept
-    // iff the Philox4x32-10 word for it is >= drop_threshold (floor(p * 2^32));
-    // the key is the 64-bit seed, the counter (j / 4, i, h, b) and word j % 4.
-    // Kept values are scaled by drop_inv_keep = 1 / (1 - p); the row sum and
-    // LSE are those of the undropped softmax.
+    // Attention dropout (dropout variant only): each Philox4x32-10 word holds
+    // two 16-bit draws (low half first), so the block with counter (j / 8, i,
+    // h, b) and the 64-bit seed as key serves keys 8 (j / 8) .. + 7; P(i, j)
+    // of head (b, h) is kept iff draw j % 8 is >= floor(p * 2^16), held here
+    // shifted up by 16 bits.  Kept values are scaled by drop_inv_keep =
+    // 1 / (1 - p); the row sum and LSE are those of the undropped softmax.
     uint32_t drop_seed_lo, drop_seed_hi;
     uint32_t drop_threshold;
     float drop_inv_keep;
@@ -251,21 +252,34 @@ enum Feature : int { kPlain = 0, kPacked = 1, kLocal = 2, kDropout = 3 };
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
 // easy as 1, 2, 3", SC 2011): ten rounds of two 32x32 -> 64-bit products,
 // the key bumped by the Weyl constants between rounds.
-struct Philox4 { uint32_t x, y, z, w; };
-
-__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                                 uint32_t k0, uint32_t k1) {
+// N blocks with counters (g0 + n, c1, c2, c3) side by side, so that the
+// compiler can interleave their rounds (each round is a chain of two wide
+// multiplies and two XORs; one block alone leaves the SM waiting on it).
+// Word k of block n goes to w[4 n + k].
+template <int N>
+__device__ __forceinline__ void philox4x32_10(uint32_t g0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                              uint32_t k0, uint32_t k1, uint32_t (&w)[4 * N]) {
     constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
     constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
 #pragma unroll
+    for (int n = 0; n < N; ++n) {
+        w[4 * n + 0] = g0 + n;
+        w[4 * n + 1] = c1;
+        w[4 * n + 2] = c2;
+        w[4 * n + 3] = c3;
+    }
+#pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t hi0 = __umulhi(kM0, c0), lo0 = kM0 * c0;
-        const uint32_t hi1 = __umulhi(kM1, c2), lo1 = kM1 * c2;
-        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            uint32_t* c = w + 4 * n;
+            const uint32_t hi0 = __umulhi(kM0, c[0]), lo0 = kM0 * c[0];
+            const uint32_t hi1 = __umulhi(kM1, c[2]), lo1 = kM1 * c[2];
+            const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+            c[0] = n0; c[1] = lo1; c[2] = n2; c[3] = lo0;
+        }
         k0 += kW0; k1 += kW1;
     }
-    return Philox4{c0, c1, c2, c3};
 }
 
 template <int FEAT>
@@ -378,21 +392,26 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-// Packs the probabilities of keys col, col + 1 of query row `row` for P V.
-// With dropout, a dropped one is packed as 0 (the caller's row sum keeps it):
-// keys 4g .. 4g + 3 share one Philox block, drawn at the even pair (odd = 0,
-// col = 4g) into `rnd` and read at the odd one (odd = 1, col = 4g + 2).  The
-// callers' loops are unrolled, so `odd` is known at compile time.
+// Dropout draws for the keys col0 .. col0 + 8 N - 1 (col0 % 8 == 0) of query
+// row `row`: N Philox blocks, counters (col0 / 8 + n, row, h, b).  Word k of
+// block n holds the draws of keys col0 + 8 n + 2 k (low half) and + 1 (high).
+template <int N>
+__device__ __forceinline__ void drop_words(const FwdParams& p, int col0, int row, const WorkItem& it,
+                                           uint32_t (&w)[4 * N]) {
+    philox4x32_10<N>(static_cast<uint32_t>(col0) >> 3, static_cast<uint32_t>(row),
+                     static_cast<uint32_t>(it.h), static_cast<uint32_t>(it.b), p.drop_seed_lo,
+                     p.drop_seed_hi, w);
+}
+
+// Packs the probabilities of two adjacent keys for P V.  With dropout, a
+// dropped one is packed as 0 (the caller's row sum keeps it); w is the word
+// of drop_words that holds the pair's draws.
 template <int FEAT, bool BF16>
-__device__ __forceinline__ uint32_t pack_p(const FwdParams& p, float2 pp, int col, int odd, int row,
-                                           const WorkItem& it, Philox4& rnd) {
+__device__ __forceinline__ uint32_t pack_p(const FwdParams& p, float2 pp, uint32_t w) {
     if constexpr (FEAT == kDropout) {
-        if (!odd)
-            rnd = philox4x32_10(static_cast<uint32_t>(col) >> 2, static_cast<uint32_t>(row),
-                                static_cast<uint32_t>(it.h), static_cast<uint32_t>(it.b),
-                                p.drop_seed_lo, p.drop_seed_hi);
-        const uint32_t w0 = odd ? rnd.z : rnd.x, w1 = odd ? rnd.w : rnd.y;
-        return pack2<BF16>(w0 >= p.drop_threshold ? pp.x : 0.f, w1 >= p.drop_threshold ? pp.y : 0.f);
+        // low half >= t  <=>  (w << 16) >= (t << 16);  high half >= t  <=>  w >= (t << 16)
+        return pack2<BF16>((w << 16) >= p.drop_threshold ? pp.x : 0.f,
+                           w >= p.drop_threshold ? pp.y : 0.f);
     } else {
         return pack2<BF16>(pp.x, pp.y);
     }
@@ -935,7 +954,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < kHalf / 32; ++q) {
                         uint32_t pk[16];
-                        Philox4 rnd;
+                        uint32_t dw[16] = {};   // dropout draws of these 32 keys
+                        if constexpr (FEAT == kDropout) drop_words<4>(p, kv0 + q * 32, row, it, dw);
 #pragma unroll
                         for (int kq = 0; kq < 16; ++kq) {
                             const float2 x = __ffma2_rn(
@@ -944,7 +964,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                                 c2, nmc2);
                             const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
                             sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
-                            pk[kq] = pack_p<FEAT, BF16>(p, pp, kv0 + q * 32 + 2 * kq, kq & 1, row, it, rnd);
+                            pk[kq] = pack_p<FEAT, BF16>(p, pp, dw[kq]);
                         }
                         if (kSepP && q == 0 && j > 0 && ok) {
                             // P_t and O_t are still read / written by P_t V of tile j-1
@@ -1014,7 +1034,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
 #pragma unroll
                         for (int q = 0; q < kHalf / 32; ++q) {
                             uint32_t pk[16];
-                            Philox4 rnd;
+                            uint32_t dw[4] = {};   // dropout draws of 8 of these keys
 #pragma unroll
                             for (int kq = 0; kq < 16; ++kq) {
                                 const float2 x = __ffma2_rn(
@@ -1023,7 +1043,11 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                                     c2, nmc2);
                                 const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
                                 sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
-                                pk[kq] = pack_p<FEAT, BF16>(p, pp, kv0 + q * 32 + 2 * kq, kq & 1, row, it, rnd);
+                                // (one block at a time: two threads share a row here
+                                // and registers are short)
+                                if constexpr (FEAT == kDropout)
+                                    if ((kq & 3) == 0) drop_words<1>(p, kv0 + q * 32 + 2 * kq, row, it, dw);
+                                pk[kq] = pack_p<FEAT, BF16>(p, pp, dw[kq & 3]);
                             }
                             if (!p_free && ok) {
                                 // P_t and O_t are still read / written by P_t V of tile j-1

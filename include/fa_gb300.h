@@ -160,12 +160,14 @@ int fa_selftest_timeout(const void* Q, const void* K, const void* V, void* O, in
  * by 1 / (1 - p_drop) before they multiply V.  The max, the row sums and LSE
  * are those of the undropped softmax.
  *
- * The mask is a pure function of (seed, b, h, i, j): element (b, h, i, j) takes
- * word j mod 4 of the Philox4x32-10 block (Salmon et al., "Parallel random
- * numbers: as easy as 1, 2, 3", SC 2011) with counter (j / 4, i, h, b) and key
- * (seed mod 2^32, seed / 2^32), and is kept iff that word >= floor(p_drop *
- * 2^32).  So p_drop = 0 keeps everything and gives fa_fwd_gqa's result bit for
- * bit.  Arguments and layout as fa_fwd_gqa (LSE may be NULL); the keys are not
+ * The mask is a pure function of (seed, b, h, i, j).  Each 32-bit word of a
+ * Philox4x32-10 block (Salmon et al., "Parallel random numbers: as easy as
+ * 1, 2, 3", SC 2011) holds two 16-bit draws, low half first; element
+ * (b, h, i, j) takes draw j mod 8 (half j mod 2 of word (j mod 8) / 2) of the
+ * block with counter (j / 8, i, h, b) and key (seed mod 2^32, seed / 2^32),
+ * and is kept iff that draw >= floor(p_drop * 2^16) (so the keep probability
+ * is within 2^-16 of 1 - p_drop).  p_drop = 0 keeps everything and gives
+ * fa_fwd_gqa's result bit for bit.  Arguments and layout as fa_fwd_gqa (LSE may be NULL); the keys are not
  * split over CTAs.  Errors: as fa_fwd_gqa, and FA_ERR_INVALID_ARG unless
  * 0 <= p_drop < 1.
  */

@@ -9,5 +9,5 @@ from .attention import (  # noqa: F401
     softmax_probabilities, online_softmax_attention, attention_reference_varlen,
 )
 from .dropout import (  # noqa: F401
-    philox4x32_10, dropout_keep, dropout_threshold, attention_reference_dropout,
+    philox4x32_10, dropout_keep, dropout_threshold, dropout_draws, attention_reference_dropout,
 )

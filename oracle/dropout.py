@@ -19,10 +19,14 @@ as 1, 2, 3", SC 2011), written here from its definition: a 128-bit counter
 with M0 = 0xD2511F53, M1 = 0xCD9E8D57, and the key bumped by
 (0x9E3779B9, 0xBB67AE85) before every round but the first.
 
-Element (b, h, i, j) (query row i, key j) takes word j mod 4 of the block
-with counter (j div 4, i, h, b) and key (seed mod 2^32, seed div 2^32); it is
-kept iff that word >= floor(p * 2^32) -- an integer decision, the same on
-any machine.  Parity status: pinned by tests/test_oracle.py (the generator's
+Each 32-bit output word holds two 16-bit draws (low half first), so one
+block serves eight keys: element (b, h, i, j) (query row i, key j) takes
+draw j mod 8 -- half j mod 2 of word (j mod 8) div 2 -- of the block with
+counter (j div 8, i, h, b) and key (seed mod 2^32, seed div 2^32); it is
+kept iff that draw >= floor(p * 2^16) -- an integer decision, the same on
+any machine.  (p is thereby taken to a multiple of 2^-16: the keep
+probability is 1 - floor(p * 2^16) / 2^16, within 2^-16 of 1 - p; the kept
+values are scaled by 1 / (1 - p) as asked.)  Parity status: pinned by tests/test_oracle.py (the generator's
 published known-answer vectors, p = 0, the kept fraction, unbiasedness, and
 the mask read back through a one-hot V).
 """
@@ -34,7 +38,8 @@ import numpy as np
 
 from .attention import _kv_group, _visible, decode
 
-__all__ = ["philox4x32_10", "dropout_keep", "attention_reference_dropout"]
+__all__ = ["philox4x32_10", "dropout_threshold", "dropout_draws", "dropout_keep",
+           "attention_reference_dropout"]
 
 _M0, _M1 = np.uint64(0xD2511F53), np.uint64(0xCD9E8D57)
 _W0, _W1 = np.uint64(0x9E3779B9), np.uint64(0xBB67AE85)
@@ -58,27 +63,35 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
 
 
 def dropout_threshold(p_drop: float) -> int:
-    """floor(p * 2^32), the smallest kept word."""
+    """floor(p * 2^16), the smallest kept 16-bit draw."""
     if not (0.0 <= p_drop < 1.0):
         raise ValueError("p_drop must be in [0, 1)")
-    return min(int(math.floor(p_drop * 4294967296.0)), 4294967295)
+    return min(int(math.floor(p_drop * 65536.0)), 65535)
+
+
+def dropout_draws(b: int, h: int, rows, ng: int, seed: int) -> np.ndarray:
+    """The 16-bit draws of head (b, h) for the given query rows and keys
+    0 .. 8 * ng - 1, shape [len(rows), 8 * ng]."""
+    rows = np.asarray(rows, dtype=np.uint64)
+    n = len(rows)
+    k0, k1 = seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF
+    g = np.broadcast_to(np.arange(ng, dtype=np.uint64)[None, :], (n, ng))
+    i = np.broadcast_to(rows[:, None], (n, ng))
+    words = philox4x32_10(g, i, np.full((n, ng), h, dtype=np.uint64),
+                          np.full((n, ng), b, dtype=np.uint64), k0, k1)
+    w = np.stack(words, axis=-1)                                  # [n, ng, 4]
+    halves = np.stack([w & 0xFFFF, w >> np.uint64(16)], axis=-1)  # [n, ng, 4, 2]
+    return halves.reshape(n, 8 * ng)      # key 8 g + 2 word + half
 
 
 def dropout_keep(B: int, H: int, S: int, p_drop: float, seed: int) -> np.ndarray:
     """keep[b, h, i, j] for query rows i and keys j of an S x S score matrix."""
     t = np.uint64(dropout_threshold(p_drop))
-    k0, k1 = seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF
-    ng = (S + 3) // 4
-    g = np.arange(ng, dtype=np.uint64)[None, :]
-    i = np.arange(S, dtype=np.uint64)[:, None]
+    ng = (S + 7) // 8
     keep = np.empty((B, H, S, S), dtype=bool)
     for b in range(B):
         for h in range(H):
-            words = philox4x32_10(np.broadcast_to(g, (S, ng)), np.broadcast_to(i, (S, ng)),
-                                  np.full((S, ng), h, dtype=np.uint64),
-                                  np.full((S, ng), b, dtype=np.uint64), k0, k1)
-            w = np.stack(words, axis=-1).reshape(S, 4 * ng)[:, :S]   # column j = 4 * g + word
-            keep[b, h] = w >= t
+            keep[b, h] = dropout_draws(b, h, np.arange(S), ng, seed)[:, :S] >= t
     return keep
 
 

@@ -1,7 +1,8 @@
 """GPU parity of attention dropout (fa_fwd_dropout) against the fp64 oracle.
 
-Every probability P_ij is kept iff its Philox4x32-10 word is >= floor(p *
-2^32) and the kept ones are scaled by 1 / (1 - p); LSE is the undropped one.
+Every probability P_ij is kept iff its 16-bit Philox4x32-10 draw is >=
+floor(p * 2^16) and the kept ones are scaled by 1 / (1 - p); LSE is the
+undropped one.
 The keep decision is an integer comparison, so the mask is checked bit for
 bit (read back through a V that routes each key to its own output column);
 O is checked against the oracle with the forward's tolerance times 1 / (1 -
@@ -133,7 +134,7 @@ def test_dropout_full_size_sampled_rows():
     import torch
     import attention_forward_fwd_gb300 as fa
     from oracle.attention import decode
-    from oracle.dropout import philox4x32_10, dropout_threshold
+    from oracle.dropout import dropout_draws, dropout_threshold
     w = fa_inputs.WORKLOADS["b2h16d128"]
     p, seed = 0.1, 2024
     qb, kb, vb = fa_inputs.make_qkv_for(w)
@@ -152,10 +153,7 @@ def test_dropout_full_size_sampled_rows():
         m = z.max(axis=1)
         e = np.exp(z - m[:, None])
         l = e.sum(axis=1)
-        g = np.arange(w.S // 4, dtype=np.uint64)[None, :]
-        words = philox4x32_10(g, rows.astype(np.uint64)[:, None], np.uint64(h), np.uint64(b),
-                              seed & 0xFFFFFFFF, seed >> 32)
-        keep = np.stack(words, axis=-1).reshape(len(rows), w.S) >= thr
+        keep = dropout_draws(b, h, rows, w.S // 8, seed) >= thr
         Oref = (e * keep / l[:, None]) @ vh / (1.0 - p)
         Lref = m + np.log(l)
         _assert_dropout_close(O[b, rows, h, :], L[b, h, rows], Oref, Lref, w.dtype, p,

@@ -590,7 +590,8 @@ def test_window_rows_match_full_reference():
 
 
 # ------------------------------------------------------ dropout
-from oracle import attention_reference_dropout, dropout_keep, philox4x32_10  # noqa: E402
+from oracle import (attention_reference_dropout, dropout_keep, dropout_threshold,  # noqa: E402
+                    philox4x32_10)
 
 
 @pytest.mark.parametrize("ctr,key,want", [
@@ -604,6 +605,31 @@ def test_philox_known_answer_vectors(ctr, key, want):
     generator (Random123 distribution)."""
     got = philox4x32_10(*[np.array([c]) for c in ctr], *key)
     assert tuple(int(w[0]) for w in got) == want
+
+
+def test_dropout_mask_elements_one_by_one():
+    """Element (b, h, i, j) of the mask, from one Philox call each: counter
+    (j div 8, i, h, b), word (j mod 8) div 2, low half for even j; kept iff the
+    half >= floor(p 2^16).  Catches a transposed or mis-strided layout."""
+    B, H, S, p, seed = 2, 3, 77, 0.37, 0xFEDC_BA98_7654_3210
+    keep = dropout_keep(B, H, S, p, seed)
+    t = math.floor(p * 65536)
+    rng = np.random.default_rng(3)
+    for _ in range(300):
+        b, h, i, j = (int(rng.integers(n)) for n in (B, H, S, S))
+        words = philox4x32_10(np.array([j // 8]), np.array([i]), np.array([h]), np.array([b]),
+                              seed % 2**32, seed // 2**32)
+        w = int(words[(j % 8) // 2][0])
+        half = (w >> 16) if j % 2 else (w & 0xFFFF)
+        assert keep[b, h, i, j] == (half >= t), (b, h, i, j)
+
+
+def test_dropout_threshold_quantisation():
+    """p is taken to floor(p 2^16) / 2^16: p = 0.5 drops exactly the draws
+    below 32768, and every p < 1 keeps the draw 65535."""
+    assert dropout_threshold(0.0) == 0 and dropout_threshold(0.5) == 32768
+    assert dropout_threshold(1.0 - 2.0 ** -20) == 65535
+    assert dropout_threshold(0.1) == 6553
 
 
 def test_dropout_zero_probability_is_the_plain_definition():
