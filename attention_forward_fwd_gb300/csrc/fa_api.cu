@@ -88,6 +88,10 @@ int num_sms() {
     return cached[dev];
 }
 
+// The kernel's parameters (four tensor maps and FwdParams) must fit the 4 KiB
+// of a launch's parameter space.
+static_assert(sizeof(fa::FwdParams) + 4 * sizeof(CUtensorMap) <= 4096, "kernel parameters too large");
+
 // How the keys of each query block are split over CTAs.
 struct SplitPlan {
     int chunk = 0;          // key tiles per split (0: no split)
@@ -123,7 +127,7 @@ SplitPlan plan_split(int B, int H, int S, bool causal, int sms) {
         else lo = mid + 1;
     }
     const int max_splits = (nkv_all + lo - 1) / lo;
-    if (max_splits <= 1) return plan;
+    if (max_splits <= 1 || ctas_per_head_for(S, causal, lo) > fa::kMaxSplitItems) return plan;
     plan.chunk = lo;
     plan.max_splits = max_splits;
     plan.ctas_per_head = static_cast<int>(ctas_per_head_for(S, causal, lo));
@@ -203,15 +207,16 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.ws_o = plan.chunk ? static_cast<float*>(workspace) : nullptr;
     p.ws_ml = plan.chunk ? static_cast<float*>(workspace) + o_floats : nullptr;
     if (plan.chunk) {
-        // first CTA (blockIdx.y) of each query block's splits, in visit order
+        // (visit index, split, splits) of each item of a head, in visit order
         const bool c = causal != 0;
         int y = 0;
         for (int i = 0; i < p.nqb; ++i) {
-            p.split_begin[i] = static_cast<uint16_t>(y);
             const int qb = c ? (p.nqb - 1 - i) : i;
-            y += (fa::key_tiles_for_block(qb, S, c) + plan.chunk - 1) / plan.chunk;
+            const int ns = (fa::key_tiles_for_block(qb, S, c) + plan.chunk - 1) / plan.chunk;
+            for (int sp = 0; sp < ns; ++sp, ++y)
+                p.split_item[y] = static_cast<uint32_t>(i) | (static_cast<uint32_t>(sp) << 8) |
+                                  (static_cast<uint32_t>(ns) << 20);
         }
-        p.split_begin[p.nqb] = static_cast<uint16_t>(y);
     }
     // one CTA per SM, each running its share of the work items (at most one
     // CTA per item)

@@ -98,8 +98,10 @@ constexpr int kStatusBadSeqlens = 5;   // a sequence offset was out of range (se
 // Device status word: 0, or the status of the first wait that ran out.
 __device__ int g_fa_device_status;
 
-// query blocks per head beyond which the keys are never split
+// query blocks per head, and work items per head, beyond which the keys are
+// never split
 constexpr int kMaxSplitBlocks = 128;
+constexpr int kMaxSplitItems = 256;
 
 struct FwdParams {
     int B, H, S;
@@ -148,9 +150,12 @@ struct FwdParams {
     int max_splits;     // splits of the longest query block
     float* ws_o;        // partial o~ tiles (fp32)
     float* ws_ml;       // partial (m * scale * log2e, l) per row
-    // split mode: CTAs [split_begin[i], split_begin[i+1]) of a head hold the
-    // splits of the i-th query block visited (heaviest first when causal)
-    uint16_t split_begin[kMaxSplitBlocks + 1];
+    // split mode: item y of a head is split (split_item[y] >> 8) & 0xfff of
+    // the (split_item[y] & 0xff)-th query block visited (heaviest first when
+    // causal), which has split_item[y] >> 20 splits.  One table entry per
+    // item: the decode takes one load, not a search (a chain of dependent
+    // parameter loads is slow right after launch).
+    uint32_t split_item[kMaxSplitItems];
 };
 
 // Workspace of the split-over-keys path.  One partial slot per (b*H + h,
@@ -314,16 +319,11 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
         nsplit = 1;
         it.split = 0;
     } else {
-        // the visit index i with split_begin[i] <= y < split_begin[i+1]
-        int lo = 0, hi = p.nqb;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (p.split_begin[mid] <= y) lo = mid;
-            else hi = mid;
-        }
+        const uint32_t e = p.split_item[y];
+        const int lo = static_cast<int>(e & 0xffu);
         qb = causal ? (p.nqb - 1 - lo) : lo;
-        nsplit = p.split_begin[lo + 1] - p.split_begin[lo];
-        it.split = y - p.split_begin[lo];
+        nsplit = static_cast<int>(e >> 20);
+        it.split = static_cast<int>((e >> 8) & 0xfffu);
         it.jb = it.split * p.kv_chunk;
         je = it.jb + p.kv_chunk;
     }
@@ -513,6 +513,14 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     // CTA-wide sync, so that their latency overlaps the TMEM allocation.
     int first_round = 0;   // ring items of the first item loaded before the sync
     if (warp == kLoadWarp && lane == 0) {
+        // The kernel parameters are fixed before the launch: decode the first
+        // item now, so that the latency of its parameter loads (cold right
+        // after launch) overlaps the set-up and the wait for the previous
+        // kernel.  Packed batches read their offsets from global memory,
+        // which the previous kernel may still write: those decode after it.
+        const int w_first = cta_item(0, p.items);
+        WorkItem it_first{};
+        if (FEAT != kPacked && w_first >= 0) it_first = decode_item<FEAT>(p, w_first);
         ptx::mbar_init(qbar, 1);
         ptx::mbar_init(bar_addr(&bars->q_empty), kQTiles);
         for (int s = 0; s < NS; ++s) {
@@ -541,9 +549,9 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         // this CTA's first item with key tiles (items of query blocks past the
         // end of a variable-length sequence have none)
         for (int k = 0;; ++k) {
-            const int w = cta_item(k, p.items);
+            const int w = k == 0 ? w_first : cta_item(k, p.items);
             if (w < 0) break;
-            const WorkItem it = decode_item<FEAT>(p, w);
+            const WorkItem it = (FEAT != kPacked && k == 0) ? it_first : decode_item<FEAT>(p, w);
             if (FEAT == kPacked && it.nkv == 0) continue;
             if (!p.drop_first_q) load_q(it);
             first_round = min(NS, 2 * it.nkv);
