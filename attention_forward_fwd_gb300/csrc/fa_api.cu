@@ -134,8 +134,16 @@ SplitPlan plan_split(int B, int H, int S, bool causal, int sms) {
     return plan;
 }
 
-size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D) {
+// Head dimensions the library takes: multiples of 8 up to 128 (the row
+// strides of the tensor maps must be multiples of 16 bytes).  D = 64 and
+// D = 128 run at full width; any other runs on the next kernel up, whose
+// extra columns the tensor maps read as zeros.
+bool supported_dim(int D) { return D >= 8 && D <= 128 && D % 8 == 0; }
+int kernel_dim(int D) { return D <= 64 ? 64 : 128; }
+
+size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D_head) {
     if (plan.chunk == 0) return 0;
+    const int D = kernel_dim(D_head);   // the partials have the kernel's width
     const size_t ntq = (S + fa::kBM - 1) / fa::kBM;
     const size_t slots = static_cast<size_t>(B) * H * ntq * plan.max_splits;
     return slots * (static_cast<size_t>(fa::kBM) * D + 2 * fa::kBM) * sizeof(float);
@@ -155,8 +163,8 @@ struct Options {
 
 template <int D, bool BF16, int NS, int RS, int FEAT>
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
-           int S, int causal, float scale, cudaStream_t stream, const SplitPlan& plan, void* workspace,
-           const Options& opt) {
+           int S, int Dh, int causal, float scale, cudaStream_t stream, const SplitPlan& plan,
+           void* workspace, const Options& opt) {
     const int* cu_seqlens = opt.cu_seqlens;
     const int total = opt.total;
     auto kern = fa::fa_fwd_kernel<D, BF16, NS, RS, FEAT>;
@@ -176,14 +184,15 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     const int mb = cu_seqlens ? 1 : B;
     const int ms = cu_seqlens ? total : S;
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, Q, BF16, mb, ms, H, D, fa::kBM) || !make_map(&mk, K, BF16, mb, ms, Hkv, D, fa::kBN) ||
-        !make_map(&mv, V, BF16, mb, ms, Hkv, D, fa::kBN) || !make_map(&mo, O, BF16, mb, ms, H, D, fa::kBM))
+    if (!make_map(&mq, Q, BF16, mb, ms, H, Dh, fa::kBM) || !make_map(&mk, K, BF16, mb, ms, Hkv, Dh, fa::kBN) ||
+        !make_map(&mv, V, BF16, mb, ms, Hkv, Dh, fa::kBN) || !make_map(&mo, O, BF16, mb, ms, H, Dh, fa::kBM))
         return FA_ERR_CUDA;
 
     fa::FwdParams p;
     p.B = B;
     p.H = H;
     p.S = S;
+    p.d_head = Dh;
     p.causal = causal ? 1 : 0;
     p.kv_group = H / Hkv;
     p.cu_seqlens = cu_seqlens;
@@ -264,7 +273,7 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
     if (B < 1 || H < 1 || S < 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!supported_dim(D)) return FA_ERR_UNSUPPORTED;
     const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                           reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O);
     if (mis & 15u) return FA_ERR_UNSUPPORTED;
@@ -288,17 +297,18 @@ int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, i
                      : (opt.win_left >= 0 || opt.win_right >= 0) ? fa::kLocal
                      : opt.dropout ? fa::kDropout : fa::kPlain;
 #define FA_ONE(D_, BF16_, NS_, RS_, F_) \
-    launch<D_, BF16_, NS_, RS_, F_>(Q, K, V, O, LSE, B, H, Hkv, S, causal, scale, st, plan, ws, opt)
+    launch<D_, BF16_, NS_, RS_, F_>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt)
 #define FA_LAUNCH(D_, BF16_, NS_, RS_)                                    \
     (feat == fa::kPacked    ? FA_ONE(D_, BF16_, NS_, RS_, fa::kPacked)    \
      : feat == fa::kLocal   ? FA_ONE(D_, BF16_, NS_, RS_, fa::kLocal)     \
      : feat == fa::kDropout ? FA_ONE(D_, BF16_, NS_, RS_, fa::kDropout)   \
                             : FA_ONE(D_, BF16_, NS_, RS_, fa::kPlain))
+    const int kd = kernel_dim(D);
     if (dtype == FA_F16) {
-        if (D == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);
+        if (kd == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);
         return FA_LAUNCH(128, false, kRingD128, kRowSplitD128);
     }
-    if (D == 64) return FA_LAUNCH(64, true, kRingD64, kRowSplitD64);
+    if (kd == 64) return FA_LAUNCH(64, true, kRingD64, kRowSplitD64);
     return FA_LAUNCH(128, true, kRingD128, kRowSplitD128);
 #undef FA_LAUNCH
 #undef FA_ONE
@@ -379,7 +389,7 @@ int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* L
 
 int fa_splitkv_workspace_size(int B, int H, int S, int D, int causal, size_t* bytes) {
     if (bytes == nullptr || B < 1 || H < 1 || S < 1) return FA_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!supported_dim(D)) return FA_ERR_UNSUPPORTED;
     const int sms = num_sms();
     if (sms <= 0) return FA_ERR_CUDA;
     *bytes = workspace_bytes_for(plan_split(B, H, S, causal != 0, sms), B, H, S, D);
@@ -387,7 +397,7 @@ int fa_splitkv_workspace_size(int B, int H, int S, int D, int causal, size_t* by
 }
 
 int fa_splitkv_launches(int B, int H, int S, int D, int causal) {
-    if (B < 1 || H < 1 || S < 1 || (D != 64 && D != 128)) return 0;
+    if (B < 1 || H < 1 || S < 1 || !supported_dim(D)) return 0;
     return plan_split(B, H, S, causal != 0, num_sms()).chunk ? 2 : 1;
 }
 

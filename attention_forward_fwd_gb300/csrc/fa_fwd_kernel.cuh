@@ -105,6 +105,11 @@ constexpr int kMaxSplitItems = 256;
 
 struct FwdParams {
     int B, H, S;
+    // The caller's head dimension (a multiple of 8, at most the kernel's D).
+    // The tensor maps cover only these columns: TMA reads the others as
+    // zeros and drops them on the O stores, so S and O are exact; the direct
+    // stores below use it for the row stride and skip the columns past it.
+    int d_head;
     int causal;
     int kv_group;       // query heads per K/V head (K, V have H / kv_group heads)
     // Local attention: key j is kept for query i iff i - win_left <= j <= i +
@@ -1224,7 +1229,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 float inv_l = 1.f / l_row;
                 if constexpr (FEAT == kDropout) inv_l *= p.drop_inv_keep;   // kept P scaled by 1 / (1 - p)
                 uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +
-                                 (static_cast<size_t>(it.base + row) * p.H + it.h) * D;
+                                 (static_cast<size_t>(it.base + row) * p.H + it.h) * p.d_head;
                 if (eok) {
                     ptx::tc_fence_after_sync();
 #pragma unroll
@@ -1246,7 +1251,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                             v.w = pack2<BF16>(__uint_as_float(o[u * 8 + 6]) * inv_l,
                                               __uint_as_float(o[u * 8 + 7]) * inv_l);
                             if (direct) {
-                                if (row < it.S) *reinterpret_cast<uint4*>(orow + cc * 8) = v;
+                                if (row < it.S && cc * 8 < p.d_head) *reinterpret_cast<uint4*>(orow + cc * 8) = v;
                             } else {
                                 const int box = cc >> 3;
                                 const int phys = (cc & 7) ^ (r & 7);
@@ -1397,8 +1402,8 @@ __global__ void __launch_bounds__(kCombineThreads) fa_combine_kernel(const FwdPa
     v.z = pack2<BF16>(acc[4] * inv_l, acc[5] * inv_l);
     v.w = pack2<BF16>(acc[6] * inv_l, acc[7] * inv_l);
     uint16_t* out = reinterpret_cast<uint16_t*>(O) +
-                    ((static_cast<size_t>(b) * p.S + row) * p.H + h) * D + cchunk * 8;
-    *reinterpret_cast<uint4*>(out) = v;
+                    ((static_cast<size_t>(b) * p.S + row) * p.H + h) * p.d_head + cchunk * 8;
+    if (cchunk * 8 < p.d_head) *reinterpret_cast<uint4*>(out) = v;
     if (p.lse != nullptr && cchunk == 0)
         p.lse[static_cast<size_t>(bh) * p.S + row] = (M + log2f(Lsum)) * 0.69314718055994530942f;
 }

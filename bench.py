@@ -406,6 +406,7 @@ def run_ours(args, w):
         return 0
 
     peak, peak_sust, peak_kind = _peaks()
+    clk_summary = clk.summary()
     achieved = flops_step / (ms_per_step * 1e-3) / 1e12     # one GPU, kernel time
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": _traffic(w.name),
@@ -423,8 +424,9 @@ def run_ours(args, w):
                        "l2": "flushed (256 MB write) before every timed step",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_peak": 100.0 * achieved / peak,
+            "pct_of_theoretical": _theoretical(achieved, clk_summary, dev),
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary(),
+            "clocks": clk_summary,
             "roofline": roofline,
             "e2e": e2e,
             "wall_s_timed_region": t_wall}
@@ -436,6 +438,26 @@ def run_ours(args, w):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+# dense fp16 / bf16 tensor work per SM and clock on sm_10x: one M128 N128 K16
+# MMA (2 * 128 * 128 * 16 FLOPs) every 64 cycles
+FLOP_PER_CLK_PER_SM = 8192
+
+
+def _theoretical(achieved, clocks, dev):
+    """achieved as a % of SMs x clock x 8192 FLOP/clk, at the maximum SM clock
+    and at the median clock sampled during the timed region."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {"flop_per_clk_per_sm": FLOP_PER_CLK_PER_SM, "sms": sms}
+    for key, mhz in (("at_max_clock", clocks.get("sm_max_mhz")), ("at_sampled_clock", clocks.get("sm_mhz"))):
+        if mhz:
+            tf = sms * mhz * 1e6 * FLOP_PER_CLK_PER_SM / 1e12
+            out[key] = {"sm_mhz": mhz, "tflops": tf, "pct": 100.0 * achieved / tf}
+        else:
+            out[key] = None
+    return out
 
 
 def end_to_end(args, w, lib, fa, dev, stream, tq, tk, tv, modes, dtype_code, ws, world, flops_step):
@@ -577,6 +599,34 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
     res.update(varlen_workload(lib, fa, dev, stream, flush, peak))
     res.update(window_workload(lib, fa, dev, stream, flush, peak))
     res.update(dropout_workloads(lib, fa, dev, stream, flush, peak))
+    res.update(head_dim_workloads(lib, fa, dev, stream, flush, peak))
+    return res
+
+
+# Head dimensions other than 64 / 128 (they run on the next kernel up, the
+# extra columns read as zeros): B4 H16 S4096 causal at D = 32 (fp16) and
+# D = 96 (bf16); FLOPs counted with the caller's D.
+HEAD_DIMS = ((32, "f16", 1010), (96, "bf16", 1011))
+
+
+def head_dim_workloads(lib, fa, dev, stream, flush, peak):
+    """Kernel-timed TFLOP/s at other head dimensions (informational)."""
+    import torch
+    res = {}
+    B, H, S = 4, 16, 4096
+    for D, dt, seed in HEAD_DIMS:
+        qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dt, "normal", seed)
+        q, k, v = (fa_inputs.to_torch(x, dt).to(dev) for x in (qb, kb, vb))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+        code = fa.FA_F16 if dt == "f16" else fa.FA_BF16
+        t = _median_kernel_ms(stream, flush, lambda: lib.fa_fwd_gqa(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, H, S, D, 1,
+            D ** -0.5, code, stream.cuda_stream))
+        tf = fa_inputs.attention_flops(B, H, S, D, True) / (t * 1e-3) / 1e12
+        res[f"headdim{D}_b{B}h{H}s{S}/causal"] = {
+            "ms": t, "tflops": tf, "pct_of_peak": 100.0 * tf / peak, "launches": 1}
+        del q, k, v, o, lse
     return res
 
 

@@ -66,8 +66,11 @@ GOOD = dict(Q=4096, K=8192, V=12288, O=16384, LSE=20480, B=1, H=1, S=128, D=64,
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
-    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
-    (dict(D=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=100), fa.FA_ERR_UNSUPPORTED),   # not a multiple of 8
+    (dict(D=136), fa.FA_ERR_UNSUPPORTED),   # above 128
+    (dict(D=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=4), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=0), fa.FA_ERR_UNSUPPORTED),
     (dict(Q=4096 + 8), fa.FA_ERR_UNSUPPORTED),
     (dict(O=16384 + 2), fa.FA_ERR_UNSUPPORTED),
     (dict(LSE=20480 + 2), fa.FA_ERR_UNSUPPORTED),
@@ -83,7 +86,7 @@ def test_bad_arguments_are_rejected_before_launch(lib, change, status):
 
 def test_dtype_specific_entry_points_validate(lib):
     assert fa.fa_fwd_f16(None, 1, 1, 1, None, 1, 1, 1, 64, 0, 1.0, None) == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_fwd_bf16(16, 16, 16, 16, None, 1, 1, 1, 80, 0, 1.0, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_bf16(16, 16, 16, 16, None, 1, 1, 1, 84, 0, 1.0, None) == fa.FA_ERR_UNSUPPORTED
 
 
 def test_binding_rejects_cpu_tensors():
@@ -97,13 +100,13 @@ def test_splitkv_entry_points_validate_before_cuda(lib):
     import ctypes
     assert lib.fa_splitkv_workspace_size(1, 1, 128, 64, 0, None) == fa.FA_ERR_INVALID_ARG
     n = ctypes.c_size_t(0)
-    assert lib.fa_splitkv_workspace_size(1, 1, 128, 80, 0, ctypes.byref(n)) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_splitkv_workspace_size(1, 1, 128, 84, 0, ctypes.byref(n)) == fa.FA_ERR_UNSUPPORTED
     assert lib.fa_splitkv_workspace_size(0, 1, 128, 64, 0, ctypes.byref(n)) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_splitkv_launches(1, 1, 0, 64, 0) == 0
     bad = fa.fa_fwd_splitkv(None, 16, 16, 16, None, 1, 1, 128, 64, 0, 0.125, fa.FA_F16,
                             None, 0, None)
     assert bad == fa.FA_ERR_INVALID_ARG
-    bad = fa.fa_fwd_splitkv(16, 16, 16, 16, None, 1, 1, 128, 96, 0, 0.125, fa.FA_F16,
+    bad = fa.fa_fwd_splitkv(16, 16, 16, 16, None, 1, 1, 128, 100, 0, 0.125, fa.FA_F16,
                             None, 0, None)
     assert bad == fa.FA_ERR_UNSUPPORTED
 
@@ -119,7 +122,7 @@ def test_gqa_entry_points_reject_bad_group_before_cuda(lib, H, H_kv):
 def test_gqa_entry_points_validate_like_fa_fwd(lib):
     assert fa.fa_fwd_gqa(None, 16, 16, 16, None, 1, 4, 2, 128, 64, 0, 0.125, fa.FA_F16, None) \
         == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_fwd_gqa(16, 16, 16, 16, None, 1, 4, 2, 128, 96, 0, 0.125, fa.FA_F16, None) \
+    assert fa.fa_fwd_gqa(16, 16, 16, 16, None, 1, 4, 2, 128, 100, 0, 0.125, fa.FA_F16, None) \
         == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_fwd_gqa(16, 16, 24, 16, None, 1, 4, 2, 128, 64, 0, 0.125, fa.FA_F16, None) \
         == fa.FA_ERR_UNSUPPORTED

@@ -1,0 +1,137 @@
+"""GPU parity for head dimensions other than 64 and 128 against the fp64
+oracle.  A head dimension D (a multiple of 8 up to 128) runs on the D = 64 or
+D = 128 kernel, whose tensor maps cover only the D columns: the copies read
+the others as zeros and the O stores leave them out.  Every path that stores
+O is covered: the TMA store, the merge of split keys and the row-by-row
+stores of a packed sequence's last tile, with guard bands around O.
+Tolerances as in test_parity_gpu.py."""
+import numpy as np
+import pytest
+
+import fa_inputs
+from oracle import attention_reference, attention_reference_varlen, attention_rows
+from oracle.dropout import attention_reference_dropout
+
+from gpu_common import TOL_O, assert_close, half_ulp, lse_tol, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+DIMS = [8, 16, 32, 40, 48, 56, 72, 80, 96, 112, 120]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    fa.build()
+    fa.library()
+    fa.fa_device_status(clear=True)
+    yield
+    assert fa.fa_device_status(clear=False) == 0, "a device-side wait timed out"
+
+
+def _dtype(D):
+    return "bf16" if D % 16 else "f16"
+
+
+@pytest.mark.parametrize("split_kv", [False, True], ids=["one-cta-per-block", "split-kv"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", DIMS)
+def test_head_dims(D, causal, split_kv):
+    import attention_forward_fwd_gb300 as fa
+    B, H, S = 1, 2, 700
+    dtype = _dtype(D)
+    if split_kv:
+        assert fa.fa_splitkv_workspace_size(B, H, S, D, causal) > 0
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dtype, "normal", 100 + D)
+    O, L = run_gpu(qb, kb, vb, dtype, causal, D ** -0.5, split_kv=split_kv)
+    Oref, Lref = attention_reference(qb, kb, vb, dtype, causal, D ** -0.5)
+    assert_close(O, L, Oref, Lref, dtype, f"D{D} causal={causal} split={split_kv}")
+
+
+@pytest.mark.parametrize("split_kv", [False, True], ids=["one-cta-per-block", "split-kv"])
+@pytest.mark.parametrize("D", [24, 96])
+def test_output_stays_inside_the_tensor(D, split_kv):
+    """O surrounded by guard bands: no column past D and no row past S is
+    written (rows are D elements apart, not the kernel's width)."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    B, H, S = 1, 3, 555
+    dtype = _dtype(D)
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dtype, "stress", 110 + D)
+    q, k, v = (fa_inputs.to_torch(x, dtype).cuda() for x in (qb, kb, vb))
+    n = B * S * H * D
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 7.0, dtype=q.dtype, device="cuda")
+    o = buf[guard:guard + n].view(B, S, H, D)
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=D ** -0.5, out=o, split_kv=split_kv)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:guard] == 7.0) and torch.all(buf[guard + n:] == 7.0)
+    Oref, Lref = attention_reference(qb, kb, vb, dtype, True, D ** -0.5)
+    assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), Oref, Lref, dtype,
+                 f"guarded D{D}")
+
+
+@pytest.mark.parametrize("D", [32, 96])
+def test_packed_batch_row_stores(D):
+    """Packed sequences whose last tiles are stored row by row, with the
+    next sequence's rows right after them."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    dtype = _dtype(D)
+    lens = [1, 130, 257, 0, 300, 77]
+    qb, kb, vb, cu = fa_inputs.make_varlen(lens, 4, D, dtype, "normal", 120 + D, h_kv=2)
+    q, k, v = (fa_inputs.to_torch(x, dtype).cuda() for x in (qb, kb, vb))
+    cu_t = torch.from_numpy(cu).cuda()
+    o, lse = fa.attention_forward_varlen(q, k, v, cu_t, max(lens), causal=True, scale=D ** -0.5)
+    torch.cuda.synchronize()
+    Oref, Lref = attention_reference_varlen(qb, kb, vb, cu, dtype, True, D ** -0.5)
+    assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), Oref, Lref, dtype,
+                 f"packed D{D}")
+
+
+def test_grouped_heads_window_and_dropout_at_other_dims():
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    # grouped K/V heads (8 query heads over 2), D = 40
+    qb, kb, vb = fa_inputs.make_qkv(2, 8, 400, 40, "bf16", "normal", 131, h_kv=2)
+    O, L = run_gpu(qb, kb, vb, "bf16", True, 40 ** -0.5)
+    Oref, Lref = attention_reference(qb, kb, vb, "bf16", True, 40 ** -0.5)
+    assert_close(O, L, Oref, Lref, "bf16", "GQA D40")
+    # sliding window, D = 96
+    qb, kb, vb = fa_inputs.make_qkv(1, 4, 900, 96, "f16", "normal", 132)
+    q, k, v = (fa_inputs.to_torch(x, "f16").cuda() for x in (qb, kb, vb))
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=96 ** -0.5, window=(200, -1))
+    torch.cuda.synchronize()
+    Oref, Lref = attention_reference(qb, kb, vb, "f16", True, 96 ** -0.5, window=(200, -1))
+    assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), Oref, Lref, "f16",
+                 "window D96")
+    # dropout, D = 48
+    qb, kb, vb = fa_inputs.make_qkv(1, 2, 333, 48, "f16", "normal", 133)
+    q, k, v = (fa_inputs.to_torch(x, "f16").cuda() for x in (qb, kb, vb))
+    o, lse = fa.attention_forward(q, k, v, causal=False, scale=48 ** -0.5, dropout_p=0.25, seed=5)
+    torch.cuda.synchronize()
+    Oref, Lref = attention_reference_dropout(qb, kb, vb, "f16", False, 48 ** -0.5, 0.25, 5)
+    # the dropout tests' bound: the forward's tolerance times 1 / (1 - p)
+    d = np.abs(o.double().cpu().numpy() - Oref)
+    assert np.all(d <= TOL_O["f16"] / 0.75 + half_ulp(Oref, "f16")), d.max()
+    assert np.all(np.abs(lse.double().cpu().numpy() - Lref) <= lse_tol(Lref))
+
+
+def test_head_dim_96_full_size_sampled_rows():
+    """B2 H16 S8192 D96 bf16, causal (the b2h16d128 shape with D = 96): sampled
+    rows of a few heads against the oracle, computed for those rows only."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    B, H, S, D = 2, 16, 8192, 96
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, "bf16", "normal", 134)
+    q, k, v = (fa_inputs.to_torch(x, "bf16").cuda() for x in (qb, kb, vb))
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=D ** -0.5)
+    torch.cuda.synchronize()
+    O, L = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    rng = np.random.default_rng(9)
+    for b, h in ((0, 0), (1, 15), (0, 9)):
+        rows = np.sort(np.concatenate([rng.choice(S, 20, replace=False), [0, S - 1]]))
+        Oref, Lref = attention_rows(qb, kb, vb, "bf16", True, D ** -0.5, b, h, rows)
+        assert_close(O[b, rows, h, :], L[b, h, rows], Oref, Lref, "bf16", f"D96 b={b} h={h}")
