@@ -285,6 +285,23 @@ def cpu_baseline(w: fa_inputs.Workload, budget_s: float = 15.0, inputs=None):
                       f"fp64 numpy, BLAS threads = cores; {dt:.1f} s"}
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (the slowest rank sets the job's time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank: float, max_ms: float) -> float:
+    """TFLOP/s of all ranks together: every rank did flops_per_rank in at
+    most max_ms (replicas: the work grows with the ranks, weak scaling)."""
+    return world * flops_per_rank / (max_ms * 1e-3) / 1e12
+
+
 def run_reference(args, w):
     world, rank, _ = _dist_env()
     if rank != 0:
@@ -383,13 +400,9 @@ def run_ours(args, w):
     if world > 1:
         torch.distributed.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step * args.steps, total_ms)
     status = fa.fa_device_status(clear=False)
     if status != 0:
         raise RuntimeError(f"device status {status}: {fa.fa_status_string(status)}")
@@ -544,18 +557,20 @@ def end_to_end(args, w, lib, fa, dev, stream, tq, tk, tv, modes, dtype_code, ws,
         return ev0.elapsed_time(ev1) / n
 
     n = max(3, min(args.steps, 50))
-    ms = timed(pipelined_step, n)
-    serial_ms = timed(serial_step, n)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = max_over_ranks(timed(pipelined_step, n), world, dev)
+    serial_ms = max_over_ranks(timed(serial_step, n), world, dev)
     # the downloaded result is the kernels' output
     got = h_out[(n - 1) % 2][:o_bytes].view(tq.dtype)
     if not torch.isfinite(got.float()).all():
         raise RuntimeError("end-to-end output is not finite")
-    return {"value": world * flops_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    return {"value": whole_job_tflops(world, flops_step, ms), "unit": "TFLOP/s",
             "h2d_bytes_per_step": n_all * elt, "d2h_bytes_per_step": out_bytes,
             "ms_per_step": ms, "steps": n,
             "copies": "one packed upload and one packed download per step on their own "
                       "streams, two buffer slots (overlapping the neighbouring steps' kernels)",
-            "serial_value": world * flops_step / (serial_ms * 1e-3) / 1e12,
+            "serial_value": whole_job_tflops(world, flops_step, serial_ms),
             "serial_ms_per_step": serial_ms}
 
 
