@@ -443,6 +443,7 @@ def run_ours(args, w):
             "roofline": roofline,
             "e2e": e2e,
             "wall_s_timed_region": t_wall}
+    line["pages_protocol"] = pages_protocol(step, stream, dev, flops_step)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if args.all_workloads:
@@ -471,6 +472,39 @@ def _theoretical(achieved, clocks, dev):
         else:
             out[key] = None
     return out
+
+
+def pages_protocol(step, stream, dev, flops_step, forwards=100, rounds=9):
+    """The timing protocol of the pages (section 正确性、编译与计时方法 of
+    page "CuTe 详解：以 FlashAttention-2 拆解 Layout、TiledCopy 与 TiledMMA"):
+    a CUDA graph of `forwards` steps replayed `rounds` times, median with min
+    and max.  The inputs stay in L2 between forwards here, unlike the main
+    timing, so this is context for the pages' own table, not the metric."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(forwards):
+                step()
+        ms = []
+        with torch.cuda.stream(stream):   # the replays run on the current stream
+            g.replay()
+            torch.cuda.synchronize(dev)
+            for _ in range(rounds):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ms.append(e0.elapsed_time(e1) / forwards)
+        del g
+    except Exception as exc:   # capture is optional context: report, do not fail the run
+        return {"error": f"{type(exc).__name__}: {exc}"[:300]}
+    tf = [flops_step / (m * 1e-3) / 1e12 for m in ms]
+    return {"what": f"CUDA graph of {forwards} steps, {rounds} replays, L2 warm",
+            "us_per_step_median": statistics.median(ms) * 1000, "tflops_median": statistics.median(tf),
+            "tflops_min": min(tf), "tflops_max": max(tf)}
 
 
 def end_to_end(args, w, lib, fa, dev, stream, tq, tk, tv, modes, dtype_code, ws, world, flops_step):
