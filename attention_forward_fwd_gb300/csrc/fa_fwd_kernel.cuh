@@ -219,16 +219,24 @@ struct Barriers {
 // Shared memory: Q tiles, the K / V ring and, where there is room (D = 64),
 // a buffer of its own for staging the O tiles of the TMA-store epilogue, so
 // that the next item's Q can be loaded while the O of this one is stored.
-// Otherwise O is staged in the Q buffer it replaces.
+// Where there is none (D = 128) the softmax threads store their O rows to
+// global memory themselves (kDirectO), so that the Q buffer is free once the
+// item's last S = Q K^T has run; the other choice (kStageInQ) stages O in
+// the Q buffer it replaces, and the next Q waits for that store.
+#ifndef FA_DIRECT_O_D128
+#define FA_DIRECT_O_D128 1
+#endif
 template <int D, int NS, int RS>
 struct SmemLayout {
     static constexpr int kQBytes = kBM * D * 2;
     static constexpr int kKVBytes = kBN * D * 2;
-    static constexpr bool kStageInQ = !separate_p(D);
+    static constexpr bool kDirectO = !separate_p(D) && FA_DIRECT_O_D128;
+    static constexpr bool kStageInQ = !separate_p(D) && !kDirectO;
+    static constexpr bool kOwnStage = !kDirectO && !kStageInQ;
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQTiles * kQBytes;
-    static constexpr int kOffStage = kStageInQ ? kOffQ : kOffKV + NS * kKVBytes;
-    static constexpr int kOffBar = kOffKV + NS * kKVBytes + (kStageInQ ? 0 : kQTiles * kQBytes);
+    static constexpr int kOffStage = kOwnStage ? kOffKV + NS * kKVBytes : kOffQ;
+    static constexpr int kOffBar = kOffKV + NS * kKVBytes + (kOwnStage ? kQTiles * kQBytes : 0);
     static constexpr int kBytes = kOffBar + static_cast<int>(sizeof(Barriers<NS, RS>));
     static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024
     static_assert(kAlloc <= 232448, "shared memory beyond the 227 KiB a CTA may use");
@@ -442,6 +450,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     // (same thread, in order).
     constexpr bool kSepP = separate_p(D);
     constexpr bool kStageInQ = L::kStageInQ;
+    constexpr bool kDirectO = L::kDirectO;
     constexpr int kPCol0 = kSepP ? (2 * kBN + 2 * D) : 0;   // P_0 column
     constexpr int kPColStride = kSepP ? (kBN / 2) : kBN;     // P_1 - P_0
     // Each of the kRowSplit threads of a row writes the packed P of its
@@ -808,11 +817,23 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 const uint32_t g00 = gs[0], g10 = gs[1];
                 if (!(ok = wait_warp(qbar, ki & 1))) break;
                 ++ki;
+                // with O stored directly, the Q buffer of tile t is free once
+                // its last S_t is complete (a tile without keys: now, after
+                // this item's Q load)
+                const uint32_t q_empty = bar_addr(&bars->q_empty);
+                if (kDirectO && nkv0 <= s0) ptx::mbar_arrive_warp(q_empty);
+                if (kDirectO && nkv1 <= s1) ptx::mbar_arrive_warp(q_empty);
                 const int k0 = gi0 + ring_k(0, nkv);
                 if (!(ok = wait_warp(full_bar(k0), full_par(k0)))) break;
                 ptx::tc_fence_after_sync();
-                if (s0 == 0 && nkv0 > 0) issue_s(0, k0);
-                if (s1 == 0 && nkv1 > 0) issue_s(1, k0);
+                if (s0 == 0 && nkv0 > 0) {
+                    issue_s(0, k0);
+                    if (kDirectO && nkv0 == 1) ptx::tc_commit_warp(q_empty);
+                }
+                if (s1 == 0 && nkv1 > 0) {
+                    issue_s(1, k0);
+                    if (kDirectO && nkv1 == 1) ptx::tc_commit_warp(q_empty);
+                }
                 ptx::tc_commit_warp(bar_addr(&bars->kv_empty[k0 % NS]));
                 for (int j = 0; ok && j < nkv; ++j) {
                     const int iv = gi0 + ring_v(j, nkv);
@@ -829,14 +850,20 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                         if (!(ok = wait_warp(full_bar(ik), full_par(ik)))) break;
                         ptx::tc_fence_after_sync();
                     }
-                    if (j + 1 >= s0 && j + 1 < nkv0) issue_s(0, ik);
+                    if (j + 1 >= s0 && j + 1 < nkv0) {
+                        issue_s(0, ik);
+                        if (kDirectO && j + 2 == nkv0) ptx::tc_commit_warp(q_empty);
+                    }
                     if (j >= s1 && j < nkv1) {
                         if (!(ok = wait_warp(bar_addr(&bars->p_full[1]), (g10 + j - s1) & 1))) break;
                         ptx::tc_fence_after_sync();
                         issue_pv(1, iv, j > s1);
                     }
                     ptx::tc_commit_warp(bar_addr(&bars->kv_empty[iv % NS]));
-                    if (j + 1 >= s1 && j + 1 < nkv1) issue_s(1, ik);
+                    if (j + 1 >= s1 && j + 1 < nkv1) {
+                        issue_s(1, ik);
+                        if (kDirectO && j + 2 == nkv1) ptx::tc_commit_warp(q_empty);
+                    }
                     if (next) ptx::tc_commit_warp(bar_addr(&bars->kv_empty[ik % NS]));
                 }
                 gs[0] += max(0, nkv0 - s0);
@@ -1219,7 +1246,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 // one thread stores it; rows past S are dropped by the store.
                 // The last tile of a packed sequence is stored row by row
                 // instead (the rows after it belong to the next sequence).
-                const bool direct = FEAT == kPacked && r0 + kBM > it.S;
+                const bool direct = kDirectO || (FEAT == kPacked && r0 + kBM > it.S);
                 uint8_t* stage = smem + L::kOffStage + t * L::kQBytes;
                 if (!kStageInQ && !direct && ki > 0) {
                     // the previous item's store must have read the staging buffer
@@ -1228,8 +1255,10 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 }
                 float inv_l = 1.f / l_row;
                 if constexpr (FEAT == kDropout) inv_l *= p.drop_inv_keep;   // kept P scaled by 1 / (1 - p)
+                // row of O: batch tb (0 when packed) of S rows, then the
+                // sequence start `base` (0 unless packed)
                 uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +
-                                 (static_cast<size_t>(it.base + row) * p.H + it.h) * p.d_head;
+                                 ((static_cast<size_t>(it.tb) * p.S + it.base + row) * p.H + it.h) * p.d_head;
                 if (eok) {
                     ptx::tc_fence_after_sync();
 #pragma unroll
