@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_wide.cuh"
 #include "fa_gb300.h"
 
 namespace {
@@ -92,6 +93,15 @@ int num_sms() {
 // of a launch's parameter space.
 static_assert(sizeof(fa::FwdParams) + 4 * sizeof(CUtensorMap) <= 4096, "kernel parameters too large");
 
+// Head dimensions the library takes: multiples of 8 up to 256 (the row
+// strides of the tensor maps must be multiples of 16 bytes).  D = 64, 128
+// and 256 run at full width; any other runs on the next kernel up, whose
+// extra columns the tensor maps read as zeros.  D > 128 has a kernel of its
+// own (one query tile per CTA), without the key split or the packed,
+// windowed and dropout variants.
+bool supported_dim(int D) { return D >= 8 && D <= fa::kWideD && D % 8 == 0; }
+int kernel_dim(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : fa::kWideD; }
+
 // How the keys of each query block are split over CTAs.
 struct SplitPlan {
     int chunk = 0;          // key tiles per split (0: no split)
@@ -109,8 +119,9 @@ long long ctas_per_head_for(int S, bool causal, int chunk) {
 // Split the keys only when one CTA per query block leaves most of the SMs
 // idle; then take the smallest chunk (>= 2 key tiles) whose grid still fits in
 // one wave of `sms` CTAs.
-SplitPlan plan_split(int B, int H, int S, bool causal, int sms) {
+SplitPlan plan_split(int B, int H, int S, int D, bool causal, int sms) {
     SplitPlan plan;
+    if (kernel_dim(D) > 128) return plan;   // the wide kernel does not split
     const int rows_per_cta = fa::kQTiles * fa::kBM;
     const int nqb = (S + rows_per_cta - 1) / rows_per_cta;
     const int nkv_all = (S + fa::kBN - 1) / fa::kBN;
@@ -134,12 +145,6 @@ SplitPlan plan_split(int B, int H, int S, bool causal, int sms) {
     return plan;
 }
 
-// Head dimensions the library takes: multiples of 8 up to 128 (the row
-// strides of the tensor maps must be multiples of 16 bytes).  D = 64 and
-// D = 128 run at full width; any other runs on the next kernel up, whose
-// extra columns the tensor maps read as zeros.
-bool supported_dim(int D) { return D >= 8 && D <= 128 && D % 8 == 0; }
-int kernel_dim(int D) { return D <= 64 ? 64 : 128; }
 
 size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D_head) {
     if (plan.chunk == 0) return 0;
@@ -287,6 +292,51 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
     return FA_OK;
 }
 
+// D in (128, 256]: one CTA per (head, 128-row query tile), programmatic
+// dependent launch as the main kernel.
+template <bool BF16>
+int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                int Hkv, int S, int Dh, int causal, float scale, cudaStream_t stream, const Options& opt) {
+    auto kern = fa::fa_fwd_wide_kernel<BF16>;
+    constexpr int kSmem = fa::WideSmem::kAlloc;
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_CUDA;
+    std::call_once(once[dev], [&] {
+        attr_err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    });
+    if (attr_err[dev] != cudaSuccess) return FA_ERR_CUDA;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, Q, BF16, B, S, H, Dh, fa::kBM) || !make_map(&mk, K, BF16, B, S, Hkv, Dh, fa::kBN) ||
+        !make_map(&mv, V, BF16, B, S, Hkv, Dh, fa::kBN))
+        return FA_ERR_CUDA;
+    fa::FwdParams p = {};
+    p.B = B;
+    p.H = H;
+    p.S = S;
+    p.d_head = Dh;
+    p.causal = causal ? 1 : 0;
+    p.kv_group = H / Hkv;
+    p.o_ptr = O;
+    p.lse = LSE;
+    p.drop_first_q = opt.drop_first_q;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    const long long ctas = static_cast<long long>(B) * H * ((S + fa::kBM - 1) / fa::kBM);
+    if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(fa::kWideThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
              int S, int D, int causal, float scale, int dtype, cudaStream_t st, const SplitPlan& plan,
              void* ws, const Options& opt = Options()) {
@@ -304,6 +354,11 @@ int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, i
      : feat == fa::kDropout ? FA_ONE(D_, BF16_, NS_, RS_, fa::kDropout)   \
                             : FA_ONE(D_, BF16_, NS_, RS_, fa::kPlain))
     const int kd = kernel_dim(D);
+    if (kd > 128) {
+        if (feat != fa::kPlain || plan.chunk != 0) return FA_ERR_UNSUPPORTED;
+        return dtype == FA_F16 ? launch_wide<false>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, opt)
+                               : launch_wide<true>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, opt);
+    }
     if (dtype == FA_F16) {
         if (kd == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);
         return FA_LAUNCH(128, false, kRingD128, kRowSplitD128);
@@ -392,13 +447,13 @@ int fa_splitkv_workspace_size(int B, int H, int S, int D, int causal, size_t* by
     if (!supported_dim(D)) return FA_ERR_UNSUPPORTED;
     const int sms = num_sms();
     if (sms <= 0) return FA_ERR_CUDA;
-    *bytes = workspace_bytes_for(plan_split(B, H, S, causal != 0, sms), B, H, S, D);
+    *bytes = workspace_bytes_for(plan_split(B, H, S, D, causal != 0, sms), B, H, S, D);
     return FA_OK;
 }
 
 int fa_splitkv_launches(int B, int H, int S, int D, int causal) {
     if (B < 1 || H < 1 || S < 1 || !supported_dim(D)) return 0;
-    return plan_split(B, H, S, causal != 0, num_sms()).chunk ? 2 : 1;
+    return plan_split(B, H, S, D, causal != 0, num_sms()).chunk ? 2 : 1;
 }
 
 int fa_fwd_gqa_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
@@ -409,7 +464,7 @@ int fa_fwd_gqa_splitkv(const void* Q, const void* K, const void* V, void* O, flo
     if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     const int sms = num_sms();
     if (sms <= 0) return FA_ERR_CUDA;
-    const SplitPlan plan = plan_split(B, H, S, causal != 0, sms);
+    const SplitPlan plan = plan_split(B, H, S, D, causal != 0, sms);
     const size_t need = workspace_bytes_for(plan, B, H, S, D);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FA_ERR_INVALID_ARG;
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 15u)) return FA_ERR_UNSUPPORTED;
@@ -524,7 +579,7 @@ extern "C" int fa_fwd_splitkv_static(const void* Q, const void* K, const void* V
     if (v != FA_OK) return v;
     const int sms = num_sms();
     if (sms <= 0) return FA_ERR_CUDA;
-    const SplitPlan plan = plan_split(B, H, S, causal != 0, sms);
+    const SplitPlan plan = plan_split(B, H, S, D, causal != 0, sms);
     const size_t need = workspace_bytes_for(plan, B, H, S, D);
     if (need > kStaticWorkspaceBytes) return FA_ERR_UNSUPPORTED;
     void* ws = nullptr;

@@ -1,0 +1,299 @@
+// FlashAttention-2 forward for head dimensions 136 .. 256 on sm_103a.
+//
+// The same computation as fa_fwd_kernel (page "CuTe 详解：以 FlashAttention-2
+// 拆解 Layout、TiledCopy 与 TiledMMA": S = Q K^T (section 先看全局), the online
+// softmax with the O correction (section 沿 C fragment 做 Online Softmax), the
+// second product P V (section V 的转置只发生在视图里) and the O + LSE epilogue
+// (section 第二次 GEMM 与输出 Epilogue)), laid out for a 256-wide head: one
+// 128-row query tile per CTA, so that its S (128 columns) and O (256 columns)
+// fit in tensor memory, P written over S.  Shared memory holds the Q tile
+// (4 boxes of 64 columns, 64 KiB) and two 64 KiB slots: K(j) in one, V(j) in
+// the other.  The tensor pipe runs S(j), P V(j), S(j+1), ... in issue order,
+// so the commit that reports S(j) complete also reports P V(j-1) complete:
+// the softmax of tile j may then rescale O and overwrite P.
+//
+// Warps 0-3: softmax, thread = query row = TMEM lane.  Warp 4: TMEM
+// allocation and MMA issue (converged warp, one elected lane).  Warp 5: TMA
+// producer (lane 0 issues).  Every wait is bounded (wait_phase); after a
+// timeout each role stops, the producer waits (bounded) for its copies, the
+// MMA warp for its MMAs, and the CTA frees its tensor memory and exits.
+#pragma once
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+constexpr int kWideD = 256;
+constexpr int kWideThreads = 192;
+constexpr int kWideAtoms = kWideD / 64;                 // 64-column boxes per row
+constexpr int kWideTileBytes = kBM * kWideD * 2;        // one 128 x 256 16-bit tile
+constexpr uint32_t kWideTmemCols = 512;                 // S/P [0, 128), O [128, 384)
+
+struct WideBars {
+    uint64_t q_full;
+    uint64_t kv_full[2];    // slot 0: K(j), slot 1: V(j)
+    uint64_t kv_empty[2];
+    uint64_t s_full;        // S(j) complete (and every MMA before it)
+    uint64_t p_full;        // P(j) stored by the 128 softmax threads
+    uint64_t o_done;        // the last P V complete
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct WideSmem {
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kWideTileBytes;
+    static constexpr int kOffBar = kOffKV + 2 * kWideTileBytes;
+    static constexpr int kAlloc = kOffBar + static_cast<int>(sizeof(WideBars)) + 1024;
+    static_assert(kAlloc <= 232448, "shared memory beyond the 227 KiB a CTA may use");
+};
+
+// Work item x of the grid: heads fastest, query tiles heaviest first when
+// causal (as the main kernel's order).
+template <bool BF16>
+__global__ void __launch_bounds__(kWideThreads, 1)
+    fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    WideBars* bars = reinterpret_cast<WideBars*>(smem + WideSmem::kOffBar);
+    volatile int* abort_flag = &bars->abort;
+    auto bar = [&](const uint64_t* b) { return ptx::smem_addr(b); };
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ------------------------------------------------------------ the item
+    const int bhn = p.B * p.H;
+    const int x = static_cast<int>(blockIdx.x);
+    const int y = x / bhn;
+    const int bh = x - y * bhn;
+    const int b = bh / p.H;
+    const int h = bh - b * p.H;
+    const int hkv = h / p.kv_group;
+    const bool causal = p.causal != 0;
+    const int ntq = (p.S + kBM - 1) / kBM;
+    const int qt = causal ? (ntq - 1 - y) : y;
+    const int r0 = qt * kBM;
+    const int n_tiles = key_tiles_for(r0, p.S, causal);   // >= 1 (key 0 is always visible)
+
+    if (threadIdx.x == 32 * 5) {
+        ptx::mbar_init(bar(&bars->q_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(bar(&bars->kv_full[s]), 1);
+            ptx::mbar_init(bar(&bars->kv_empty[s]), 1);
+        }
+        ptx::mbar_init(bar(&bars->s_full), 1);
+        ptx::mbar_init(bar(&bars->p_full), kBM);
+        ptx::mbar_init(bar(&bars->o_done), 1);
+        ptx::mbar_init(bar(&bars->drain), 1);
+        bars->abort = 0;
+        ptx::fence_barrier_init();
+        ptx::tma_prefetch_map(&tmQ);
+        ptx::tma_prefetch_map(&tmK);
+        ptx::tma_prefetch_map(&tmV);
+    }
+    if (warp == 4) {
+        ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kWideTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    ptx::launch_dependents();
+
+    auto wait_warp = [&](uint32_t b_, uint32_t parity, bool honour_abort = true) {
+        return __all_sync(0xffffffffu, wait_phase(b_, parity, abort_flag, honour_abort));
+    };
+
+    if (warp == 5) {
+        // ---------------------------------------------------- TMA producer
+        ptx::grid_dependency_wait();   // the previous kernel may write Q, K, V
+        const uint32_t q_dst = sbase + WideSmem::kOffQ;
+        const uint32_t slot0 = sbase + WideSmem::kOffKV;
+        auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int head, int row0) {
+            ptx::mbar_arrive_expect_tx(full, kWideTileBytes);
+            for (int c = 0; c < kWideAtoms; ++c)
+                ptx::tma_load_4d(dst + c * (kBM * 128), map, full, c * 64, head, row0, b);
+        };
+        if (lane == 0) {
+            if (!p.drop_first_q) load_tile(&tmQ, q_dst, bar(&bars->q_full), h, r0);
+        }
+        bool ok = true;
+        int issued = 0;   // 2 * tiles whose K and V were issued
+        for (int j = 0; j < n_tiles && ok; ++j) {
+            for (int s = 0; s < 2 && ok; ++s) {
+                // slot s was last used by tile j - 1
+                if (j > 0 && !(ok = wait_warp(bar(&bars->kv_empty[s]), static_cast<uint32_t>((j - 1) & 1)))) break;
+                if (lane == 0)
+                    load_tile(s == 0 ? &tmK : &tmV, slot0 + s * kWideTileBytes, bar(&bars->kv_full[s]), hkv,
+                              j * kBN);
+                ++issued;
+            }
+        }
+        if (*abort_flag) {
+            // let every copy this warp started land before the CTA exits
+            wait_warp(bar(&bars->q_full), 0, false);
+            for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
+                wait_warp(bar(&bars->kv_full[i & 1]), static_cast<uint32_t>((i >> 1) & 1), false);
+        }
+    } else if (warp == 4) {
+        // ------------------------------------------------------ MMA issue
+        constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
+        constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, kWideD, BF16, true);
+        const uint32_t slot0 = sbase + WideSmem::kOffKV;
+        bool ok = wait_warp(bar(&bars->q_full), 0);
+        const uint64_t qd = ptx::sdesc_sw128(sbase + WideSmem::kOffQ, 16, 1024);
+        const uint64_t kd = ptx::sdesc_sw128(slot0, 16, 1024);
+        const uint64_t vd = ptx::sdesc_sw128(slot0 + kWideTileBytes, kBN * 128, 1024);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+            const uint32_t par = static_cast<uint32_t>(j & 1);
+            if (!(ok = wait_warp(bar(&bars->kv_full[0]), par))) break;
+            ptx::tc_fence_after_sync();
+            // S(j) = Q K(j)^T over the 256 columns, K=16 steps through the
+            // four 64-column boxes (32 bytes per step inside a box)
+#pragma unroll
+            for (int kk = 0; kk < kWideD / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                ptx::mma_ss_warp(tmem, qd + (off >> 4), kd + (off >> 4), kIdescQK, kk > 0);
+            }
+            ptx::tc_commit_warp(bar(&bars->s_full));
+            ptx::tc_commit_warp(bar(&bars->kv_empty[0]));
+            // O (+)= P(j) V(j): P from the first 64 columns of S(j)'s tensor
+            // memory, V MN-major (64-column boxes 128*128 bytes apart)
+            if (!(ok = wait_warp(bar(&bars->p_full), par))) break;
+            if (!(ok = wait_warp(bar(&bars->kv_full[1]), par))) break;
+            ptx::tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                ptx::mma_ts_warp(tmem + kBN, tmem + kk * 8, vd + ((kk * 16 * 128) >> 4), kIdescPV,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+            ptx::tc_commit_warp(bar(&bars->kv_empty[1]));
+        }
+        if (ok) ptx::tc_commit_warp(bar(&bars->o_done));
+        // every MMA must be complete before the tensor memory is freed
+        ptx::tc_commit_warp(bar(&bars->drain));
+        wait_warp(bar(&bars->drain), 0, false);
+    } else {
+        // --------------------------------------------------------- softmax
+        const int r = static_cast<int>(threadIdx.x);   // row of the tile, TMEM lane
+        const int row = r0 + r;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+        const uint32_t tS = tmem + lane_off;             // S(j), then P(j) over it
+        const uint32_t tO = tmem + lane_off + kBN;       // O, 256 columns
+        const float c = p.scale_log2;
+        float m_use = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            ok = ok && wait_phase(bar(&bars->s_full), static_cast<uint32_t>(j & 1), abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after_sync();
+            uint32_t s[kBN];
+#pragma unroll
+            for (int q = 0; q < kBN / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence<kBN>(s);
+            // keys past the end and, on the diagonal tile, keys after the row
+            const int kv0 = j * kBN;
+            const int last = causal ? min(p.S - 1, row) : (p.S - 1);
+            if (kv0 + kBN - 1 > last || kv0 + kBN > p.S) {
+#pragma unroll
+                for (int kq = 0; kq < kBN; ++kq)
+                    if (kv0 + kq > last) s[kq] = __float_as_uint(-INFINITY);
+            }
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int kq = 0; kq < kBN / 2; ++kq)
+                mx[kq % 4] = ptx::fmax3(mx[kq % 4], __uint_as_float(s[2 * kq]), __uint_as_float(s[2 * kq + 1]));
+            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            const float m_new = fmaxf(m_use, m_tile);
+            // lazy rescale: move the reference only when the max grew by more
+            // than kTauLog2 (log2 units); the first tile always moves it
+            float alpha = 1.f;
+            const bool rescale = (m_new - m_use) * c > kTauLog2;
+            if (rescale) {
+                alpha = ptx::ex2_approx((m_use - m_new) * c);   // 0 on the first tile
+                m_use = m_new;
+            }
+            // O holds the products of earlier tiles (complete: S(j) ran after
+            // them); rows whose reference moved scale it by alpha
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                for (int q = 0; q < kWideD / 32; ++q) {
+                    uint32_t o[32];
+                    ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence<32>(o);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+                    ptx::tmem_st_32x32b_x32(tO + q * 32, o);
+                }
+            }
+            const float mc = m_use * c;
+            const float2 c2 = make_float2(c, c);
+            const float2 nmc2 = make_float2(-mc, -mc);
+            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+            for (int q = 0; q < kBN / 32; ++q) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int kq = 0; kq < 16; ++kq) {
+                    const float2 xv = __ffma2_rn(make_float2(__uint_as_float(s[q * 32 + 2 * kq]),
+                                                             __uint_as_float(s[q * 32 + 2 * kq + 1])),
+                                                 c2, nmc2);
+                    const float2 pp = make_float2(ptx::ex2_approx(xv.x), ptx::ex2_approx(xv.y));
+                    sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
+                    pk[kq] = pack2<BF16>(pp.x, pp.y);
+                }
+                ptx::tmem_st_32x32b_x16(tS + q * 16, pk);
+            }
+            const float2 sum = __fadd2_rn(sum2[0], sum2[1]);
+            l = l * alpha + (sum.x + sum.y);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(bar(&bars->p_full));
+        }
+        // ---------------------------------------------------------- epilogue
+        ok = ok && wait_phase(bar(&bars->o_done), 0, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            ptx::tc_fence_after_sync();
+            const float inv_l = 1.f / l;
+            uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +
+                             ((static_cast<size_t>(b) * p.S + row) * p.H + h) * p.d_head;
+#pragma unroll 1
+            for (int q = 0; q < kWideD / 32; ++q) {
+                uint32_t o[32];
+                ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence<32>(o);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int col = q * 32 + u * 8;
+                    uint4 v;
+                    v.x = pack2<BF16>(__uint_as_float(o[u * 8 + 0]) * inv_l, __uint_as_float(o[u * 8 + 1]) * inv_l);
+                    v.y = pack2<BF16>(__uint_as_float(o[u * 8 + 2]) * inv_l, __uint_as_float(o[u * 8 + 3]) * inv_l);
+                    v.z = pack2<BF16>(__uint_as_float(o[u * 8 + 4]) * inv_l, __uint_as_float(o[u * 8 + 5]) * inv_l);
+                    v.w = pack2<BF16>(__uint_as_float(o[u * 8 + 6]) * inv_l, __uint_as_float(o[u * 8 + 7]) * inv_l);
+                    if (row < p.S && col < p.d_head) *reinterpret_cast<uint4*>(orow + col) = v;
+                }
+            }
+            if (p.lse != nullptr && row < p.S)
+                p.lse[static_cast<size_t>(bh) * p.S + row] = (m_use * c + log2f(l)) * 0.69314718055994530942f;
+        }
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 4) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, kWideTmemCols);
+    }
+}
+
+}  // namespace fa

@@ -654,8 +654,8 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
 
 # Head dimensions other than 64 / 128 (they run on the next kernel up, the
 # extra columns read as zeros): B4 H16 S4096 causal at D = 32 (fp16) and
-# D = 96 (bf16); FLOPs counted with the caller's D.
-HEAD_DIMS = ((32, "f16", 1010), (96, "bf16", 1011))
+# D = 96 and D = 256 (bf16); FLOPs counted with the caller's D.
+HEAD_DIMS = ((32, "f16", 1010), (96, "bf16", 1011), (256, "bf16", 1012))
 
 
 def head_dim_workloads(lib, fa, dev, stream, flush, peak):

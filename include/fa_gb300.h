@@ -20,15 +20,19 @@
  *
  * Memory layout (all buffers are caller-owned DEVICE memory):
  *   Q, K, V, O : contiguous [B, S, H, D], element type fp16 or bf16 (all four
- *                the same), D a multiple of 8 from 8 to 128; base addresses
- *                16-byte aligned.  D = 64 and D = 128 run at full width; any
- *                other D runs on the kernel of the next of the two (the page
+ *                the same), D a multiple of 8 from 8 to 256; base addresses
+ *                16-byte aligned.  D = 64, 128 and 256 run at full width; any
+ *                other D runs on the kernel of the next of the three (the page
  *                "CuTe 详解：以 FlashAttention-2 拆解 Layout、TiledCopy 与
  *                TiledMMA" lists other head dimensions among a production
  *                FA2's needs, section 哪些结论可以迁移，哪些只是本例特例): its
  *                tensor maps cover only the D columns, so the copies read the
  *                rest as zeros and the O stores leave it out, and the tensor
  *                cores do that padded work (a D = 96 call costs a D = 128 one).
+ *                D > 128 has a kernel of its own (one 128-row query tile per
+ *                CTA): the plain and grouped-K/V calls take it (the split
+ *                entry points run it unsplit, with no workspace); the packed,
+ *                windowed and dropout calls return FA_ERR_UNSUPPORTED there.
  *   LSE        : contiguous fp32 [B, H, S], or NULL to skip writing it.
  *
  * Ownership and ordering: the library keeps no pointer after a call returns
@@ -41,7 +45,7 @@
  *   FA_ERR_INVALID_ARG  a NULL Q/K/V/O, B/H/S < 1, scale not finite or <= 0,
  *                       an unknown dtype, or sizes whose element count
  *                       overflows 64 bits
- *   FA_ERR_UNSUPPORTED  D not a multiple of 8 in [8, 128], a base address not 16-byte
+ *   FA_ERR_UNSUPPORTED  D not a multiple of 8 in [8, 256], a base address not 16-byte
  *                       aligned, ceil(S / 256) > 65535, or
  *                       B * H * ceil(S / 256) > 2^31 - 1
  *   FA_ERR_CUDA         a CUDA runtime or driver call failed (the CUDA error

@@ -67,8 +67,8 @@ GOOD = dict(Q=4096, K=8192, V=12288, O=16384, LSE=20480, B=1, H=1, S=128, D=64,
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
     (dict(D=100), fa.FA_ERR_UNSUPPORTED),   # not a multiple of 8
-    (dict(D=136), fa.FA_ERR_UNSUPPORTED),   # above 128
-    (dict(D=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=264), fa.FA_ERR_UNSUPPORTED),   # above 256
+    (dict(D=512), fa.FA_ERR_UNSUPPORTED),
     (dict(D=4), fa.FA_ERR_UNSUPPORTED),
     (dict(D=0), fa.FA_ERR_UNSUPPORTED),
     (dict(Q=4096 + 8), fa.FA_ERR_UNSUPPORTED),

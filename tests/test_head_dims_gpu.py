@@ -135,3 +135,71 @@ def test_head_dim_96_full_size_sampled_rows():
         rows = np.sort(np.concatenate([rng.choice(S, 20, replace=False), [0, S - 1]]))
         Oref, Lref = attention_rows(qb, kb, vb, "bf16", True, D ** -0.5, b, h, rows)
         assert_close(O[b, rows, h, :], L[b, h, rows], Oref, Lref, "bf16", f"D96 b={b} h={h}")
+
+
+# ------------------------------------------------- D > 128: the wide kernel
+WIDE = [136, 160, 192, 200, 248, 256]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", WIDE)
+def test_wide_head_dims(D, causal):
+    """Several query tiles, a ragged last tile, grouped K/V heads."""
+    B, H, H_kv, S = 2, 4, 2, 333
+    dtype = "bf16" if D % 16 else "f16"
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dtype, "normal", 140 + D, h_kv=H_kv)
+    O, L = run_gpu(qb, kb, vb, dtype, causal, D ** -0.5)
+    Oref, Lref = attention_reference(qb, kb, vb, dtype, causal, D ** -0.5)
+    assert_close(O, L, Oref, Lref, dtype, f"D{D} causal={causal}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_wide_peaky_scores_and_guard_bands(dtype):
+    """Peaky scores (the reference max moves, O is rescaled) and guard bands
+    around O; the split entry point runs the wide kernel unsplit."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    B, H, S, D = 1, 3, 700, 256
+    assert fa.fa_splitkv_workspace_size(B, H, S, D, True) == 0
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dtype, "stress", 150)
+    q, k, v = (fa_inputs.to_torch(x, dtype).cuda() for x in (qb, kb, vb))
+    n = B * S * H * D
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 7.0, dtype=q.dtype, device="cuda")
+    o = buf[guard:guard + n].view(B, S, H, D)
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=D ** -0.5, out=o)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:guard] == 7.0) and torch.all(buf[guard + n:] == 7.0)
+    Oref, Lref = attention_reference(qb, kb, vb, dtype, True, D ** -0.5)
+    assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), Oref, Lref, dtype, "stress D256")
+
+
+def test_wide_unsupported_variants_are_rejected():
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    q = torch.zeros((1, 256, 2, 256), dtype=torch.float16, device="cuda")
+    with pytest.raises(fa.FaError):
+        fa.attention_forward(q, q, q, window=(64, -1))
+    with pytest.raises(fa.FaError):
+        fa.attention_forward(q, q, q, dropout_p=0.1)
+    cu = torch.tensor([0, 100, 256], dtype=torch.int32, device="cuda")
+    with pytest.raises(fa.FaError):
+        fa.attention_forward_varlen(q[0], q[0], q[0], cu, 156)
+    torch.cuda.synchronize()
+
+
+def test_wide_full_size_sampled_rows():
+    """B2 H16 S8192 D256 bf16, causal: sampled rows of a few heads."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    B, H, S, D = 2, 16, 8192, 256
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, "bf16", "normal", 151)
+    q, k, v = (fa_inputs.to_torch(x, "bf16").cuda() for x in (qb, kb, vb))
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=D ** -0.5)
+    torch.cuda.synchronize()
+    O, L = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    rng = np.random.default_rng(10)
+    for b, h in ((0, 0), (1, 15), (1, 4)):
+        rows = np.sort(np.concatenate([rng.choice(S, 20, replace=False), [0, S - 1]]))
+        Oref, Lref = attention_rows(qb, kb, vb, "bf16", True, D ** -0.5, b, h, rows)
+        assert_close(O[b, rows, h, :], L[b, h, rows], Oref, Lref, "bf16", f"D256 b={b} h={h}")
