@@ -1,7 +1,7 @@
 """GPU parity for head dimensions other than 64 and 128 against the fp64
-oracle.  A head dimension D (a multiple of 8 up to 128) runs on the D = 64 or
-D = 128 kernel, whose tensor maps cover only the D columns: the copies read
-the others as zeros and the O stores leave them out.  Every path that stores
+oracle.  A head dimension D (a multiple of 8 up to 256) runs on the D = 64,
+D = 128 or D = 256 kernel, whose tensor maps cover only the D columns: the
+copies read the others as zeros and the O stores leave them out.  Every path that stores
 O is covered: the TMA store, the merge of split keys and the row-by-row
 stores of a packed sequence's last tile, with guard bands around O.
 Tolerances as in test_parity_gpu.py."""
