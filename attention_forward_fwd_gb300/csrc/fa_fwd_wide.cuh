@@ -6,11 +6,13 @@
 // second product P V (section V 的转置只发生在视图里) and the O + LSE epilogue
 // (section 第二次 GEMM 与输出 Epilogue)), laid out for a 256-wide head: one
 // 128-row query tile per CTA, so that its S (128 columns) and O (256 columns)
-// fit in tensor memory, P written over S.  Shared memory holds the Q tile
+// fit in tensor memory: S in two buffers (columns [0, 128) and [384, 512)),
+// P written over its S, O in [128, 384).  Shared memory holds the Q tile
 // (4 boxes of 64 columns, 64 KiB) and two 64 KiB slots: K(j) in one, V(j) in
-// the other.  The tensor pipe runs S(j), P V(j), S(j+1), ... in issue order,
-// so the commit that reports S(j) complete also reports P V(j-1) complete:
-// the softmax of tile j may then rescale O and overwrite P.
+// the other.  The tensor pipe runs S(0), S(1), P V(0), S(2), P V(1), ...:
+// S(j+1) overlaps the softmax of tile j.  S(j) is issued after P V(j-2), so
+// when S(j) is complete the P V that last read its buffer is too; O may be
+// rescaled once P V(j-1) has reported on its own barrier.
 //
 // Warps 0-3: softmax, thread = query row = TMEM lane.  Warp 4: TMEM
 // allocation and MMA issue (converged warp, one elected lane).  Warp 5: TMA
@@ -27,15 +29,24 @@ constexpr int kWideD = 256;
 constexpr int kWideThreads = 192;
 constexpr int kWideAtoms = kWideD / 64;                 // 64-column boxes per row
 constexpr int kWideTileBytes = kBM * kWideD * 2;        // one 128 x 256 16-bit tile
-constexpr uint32_t kWideTmemCols = 512;                 // S/P [0, 128), O [128, 384)
+constexpr uint32_t kWideTmemCols = 512;   // S/P buffers [0, 128) and [384, 512), O [128, 384)
+constexpr uint32_t kWideS1 = 384;         // column of the second S/P buffer
 
 struct WideBars {
     uint64_t q_full;
     uint64_t kv_full[2];    // slot 0: K(j), slot 1: V(j)
     uint64_t kv_empty[2];
-    uint64_t s_full;        // S(j) complete (and every MMA before it)
-    uint64_t p_full;        // P(j) stored by the 128 softmax threads
-    uint64_t o_done;        // the last P V complete
+    uint64_t s_full[2];     // S(j) complete in buffer j % 2 (and every MMA before it)
+    // P(j) stored in buffer j % 2 by the 128 softmax threads.  One barrier
+    // per buffer: S(j+1) is issued before the MMA warp waits for P(j), so the
+    // softmax may store P(j+1) before that wait is seen, and a single barrier
+    // could move two phases past it; P(j+2) needs S(j+2), which is issued
+    // only after P V(j)
+    uint64_t p_full[2];
+    uint64_t o_done;        // one phase per P V(j)
+    // the last P V complete: the epilogue cannot wait on o_done, which may
+    // then be one, two or no phases short of it (parity tells two apart)
+    uint64_t o_last;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -85,9 +96,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             ptx::mbar_init(bar(&bars->kv_full[s]), 1);
             ptx::mbar_init(bar(&bars->kv_empty[s]), 1);
         }
-        ptx::mbar_init(bar(&bars->s_full), 1);
-        ptx::mbar_init(bar(&bars->p_full), kBM);
+        ptx::mbar_init(bar(&bars->s_full[0]), 1);
+        ptx::mbar_init(bar(&bars->s_full[1]), 1);
+        ptx::mbar_init(bar(&bars->p_full[0]), kBM);
+        ptx::mbar_init(bar(&bars->p_full[1]), kBM);
         ptx::mbar_init(bar(&bars->o_done), 1);
+        ptx::mbar_init(bar(&bars->o_last), 1);
         ptx::mbar_init(bar(&bars->drain), 1);
         bars->abort = 0;
         ptx::fence_barrier_init();
@@ -122,23 +136,35 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         if (lane == 0) {
             if (!p.drop_first_q) load_tile(&tmQ, q_dst, bar(&bars->q_full), h, r0);
         }
+        // K(j+1) is needed before V(j) (the MMA order is S(j+1), P V(j)):
+        // K(0), V(0), K(1), then K(j+1), V(j).  Tile i of a slot waits for
+        // the slot's previous tile to be consumed (completion i of its
+        // empty barrier).
         bool ok = true;
-        int issued = 0;   // 2 * tiles whose K and V were issued
-        for (int j = 0; j < n_tiles && ok; ++j) {
-            for (int s = 0; s < 2 && ok; ++s) {
-                // slot s was last used by tile j - 1
-                if (j > 0 && !(ok = wait_warp(bar(&bars->kv_empty[s]), static_cast<uint32_t>((j - 1) & 1)))) break;
-                if (lane == 0)
-                    load_tile(s == 0 ? &tmK : &tmV, slot0 + s * kWideTileBytes, bar(&bars->kv_full[s]), hkv,
-                              j * kBN);
-                ++issued;
-            }
+        int nk = 0, nv = 0;   // K / V tiles issued
+        auto load_k = [&](int i) {
+            if (i > 0 && !(ok = wait_warp(bar(&bars->kv_empty[0]), static_cast<uint32_t>((i - 1) & 1)))) return;
+            if (lane == 0) load_tile(&tmK, slot0, bar(&bars->kv_full[0]), hkv, i * kBN);
+            ++nk;
+        };
+        auto load_v = [&](int i) {
+            if (i > 0 && !(ok = wait_warp(bar(&bars->kv_empty[1]), static_cast<uint32_t>((i - 1) & 1)))) return;
+            if (lane == 0) load_tile(&tmV, slot0 + kWideTileBytes, bar(&bars->kv_full[1]), hkv, i * kBN);
+            ++nv;
+        };
+        load_k(0);
+        if (ok) load_v(0);
+        if (ok && n_tiles > 1) load_k(1);
+        for (int j = 1; j < n_tiles && ok; ++j) {
+            if (j + 1 < n_tiles) load_k(j + 1);
+            if (ok) load_v(j);
         }
         if (*abort_flag) {
             // let every copy this warp started land before the CTA exits
+            // (only the last of each slot can still be in flight)
             wait_warp(bar(&bars->q_full), 0, false);
-            for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
-                wait_warp(bar(&bars->kv_full[i & 1]), static_cast<uint32_t>((i >> 1) & 1), false);
+            if (nk > 0) wait_warp(bar(&bars->kv_full[0]), static_cast<uint32_t>((nk - 1) & 1), false);
+            if (nv > 0) wait_warp(bar(&bars->kv_full[1]), static_cast<uint32_t>((nv - 1) & 1), false);
         }
     } else if (warp == 4) {
         // ------------------------------------------------------ MMA issue
@@ -149,31 +175,41 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         const uint64_t qd = ptx::sdesc_sw128(sbase + WideSmem::kOffQ, 16, 1024);
         const uint64_t kd = ptx::sdesc_sw128(slot0, 16, 1024);
         const uint64_t vd = ptx::sdesc_sw128(slot0 + kWideTileBytes, kBN * 128, 1024);
-        for (int j = 0; j < n_tiles && ok; ++j) {
-            const uint32_t par = static_cast<uint32_t>(j & 1);
-            if (!(ok = wait_warp(bar(&bars->kv_full[0]), par))) break;
+        // S(i) into buffer i % 2: Q K(i)^T over the 256 columns, K=16 steps
+        // through the four 64-column boxes (32 bytes per step inside a box)
+        auto issue_s = [&](int i) {
+            if (!(ok = wait_warp(bar(&bars->kv_full[0]), static_cast<uint32_t>(i & 1)))) return;
             ptx::tc_fence_after_sync();
-            // S(j) = Q K(j)^T over the 256 columns, K=16 steps through the
-            // four 64-column boxes (32 bytes per step inside a box)
+            const uint32_t d = tmem + ((i & 1) ? kWideS1 : 0u);
 #pragma unroll
             for (int kk = 0; kk < kWideD / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-                ptx::mma_ss_warp(tmem, qd + (off >> 4), kd + (off >> 4), kIdescQK, kk > 0);
+                ptx::mma_ss_warp(d, qd + (off >> 4), kd + (off >> 4), kIdescQK, kk > 0);
             }
-            ptx::tc_commit_warp(bar(&bars->s_full));
+            ptx::tc_commit_warp(bar(&bars->s_full[i & 1]));
             ptx::tc_commit_warp(bar(&bars->kv_empty[0]));
-            // O (+)= P(j) V(j): P from the first 64 columns of S(j)'s tensor
-            // memory, V MN-major (64-column boxes 128*128 bytes apart)
-            if (!(ok = wait_warp(bar(&bars->p_full), par))) break;
+        };
+        if (ok) issue_s(0);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+            const uint32_t par = static_cast<uint32_t>(j & 1);
+            if (j + 1 < n_tiles) {
+                issue_s(j + 1);
+                if (!ok) break;
+            }
+            // O (+)= P(j) V(j): P from the first 64 columns of S(j)'s buffer,
+            // V MN-major (64-column boxes 128*128 bytes apart)
+            if (!(ok = wait_warp(bar(&bars->p_full[j & 1]), static_cast<uint32_t>((j >> 1) & 1)))) break;
             if (!(ok = wait_warp(bar(&bars->kv_full[1]), par))) break;
             ptx::tc_fence_after_sync();
+            const uint32_t pa = tmem + ((j & 1) ? kWideS1 : 0u);
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-                ptx::mma_ts_warp(tmem + kBN, tmem + kk * 8, vd + ((kk * 16 * 128) >> 4), kIdescPV,
+                ptx::mma_ts_warp(tmem + kBN, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), kIdescPV,
                                  (j > 0 || kk > 0) ? 1u : 0u);
             ptx::tc_commit_warp(bar(&bars->kv_empty[1]));
+            ptx::tc_commit_warp(bar(&bars->o_done));
+            if (j + 1 == n_tiles) ptx::tc_commit_warp(bar(&bars->o_last));
         }
-        if (ok) ptx::tc_commit_warp(bar(&bars->o_done));
         // every MMA must be complete before the tensor memory is freed
         ptx::tc_commit_warp(bar(&bars->drain));
         wait_warp(bar(&bars->drain), 0, false);
@@ -182,17 +218,18 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         const int r = static_cast<int>(threadIdx.x);   // row of the tile, TMEM lane
         const int row = r0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-        const uint32_t tS = tmem + lane_off;             // S(j), then P(j) over it
+        const uint32_t tS0 = tmem + lane_off;            // S(j), then P(j) over it, buffer j % 2
         const uint32_t tO = tmem + lane_off + kBN;       // O, 256 columns
         const float c = p.scale_log2;
         float m_use = -INFINITY;
         float l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            ok = ok && wait_phase(bar(&bars->s_full), static_cast<uint32_t>(j & 1), abort_flag);
+            ok = ok && wait_phase(bar(&bars->s_full[j & 1]), static_cast<uint32_t>((j >> 1) & 1), abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after_sync();
+            const uint32_t tS = tS0 + ((j & 1) ? kWideS1 : 0u);
             uint32_t s[kBN];
 #pragma unroll
             for (int q = 0; q < kBN / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
@@ -220,9 +257,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 alpha = ptx::ex2_approx((m_use - m_new) * c);   // 0 on the first tile
                 m_use = m_new;
             }
-            // O holds the products of earlier tiles (complete: S(j) ran after
-            // them); rows whose reference moved scale it by alpha
+            // rows whose reference moved scale O by alpha, once P V(j-1) is
+            // complete (phase j-1 of o_done: P V(j-2) is complete already, as
+            // S(j) was issued after it, and P V(j) waits for this P(j))
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                ok = wait_phase(bar(&bars->o_done), static_cast<uint32_t>((j - 1) & 1), abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ptx::tc_fence_after_sync();
 #pragma unroll 1
                 for (int q = 0; q < kWideD / 32; ++q) {
                     uint32_t o[32];
@@ -256,10 +298,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             l = l * alpha + (sum.x + sum.y);
             ptx::tmem_st_wait();
             ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(bar(&bars->p_full));
+            ptx::mbar_arrive(bar(&bars->p_full[j & 1]));
         }
         // ---------------------------------------------------------- epilogue
-        ok = ok && wait_phase(bar(&bars->o_done), 0, abort_flag);
+        ok = ok && wait_phase(bar(&bars->o_last), 0, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             ptx::tc_fence_after_sync();
