@@ -678,3 +678,32 @@ def test_dropout_mask_read_back_through_one_hot_values():
         for h in range(2):
             got = O[0, :, h, :S] != 0
             assert np.array_equal(got, keep[0, h] & vis), (causal, h)
+
+
+# ------------------------------------------------------ other head dimensions
+@pytest.mark.parametrize("D", [8, 40, 136, 256])
+def test_head_dims_closed_forms_and_torch(D):
+    """The definition at head dimensions the kernels take besides 64 / 128:
+    identical keys give the (prefix) mean of V, causal row 0 gives V row 0
+    with LSE = its own logit, and torch's math attention agrees in fp64."""
+    torch = pytest.importorskip("torch")
+    S, H = 37, 2
+    qb, kb, vb = fa_inputs.make_qkv(1, H, S, D, "bf16", "normal", 500 + D)
+    kb = kb.copy()
+    kb[0, :, 1, :] = kb[0, 0, 1, :]                    # head 1: every key equals key 0
+    q, k, v = (decode_bf16(x) for x in (qb, kb, vb))
+    scale = D ** -0.5
+    for causal in (False, True):
+        O, L = attention_reference(qb, kb, vb, "bf16", causal, scale)
+        v1 = v[0, :, 1, :]
+        want = (np.cumsum(v1, axis=0) / np.arange(1, S + 1)[:, None]) if causal else \
+            np.broadcast_to(v1.mean(axis=0), v1.shape)
+        np.testing.assert_allclose(O[0, :, 1, :], want, atol=1e-12)
+        if causal:
+            np.testing.assert_allclose(O[0, 0, :, :], v[0, 0, :, :], atol=1e-12)
+            z00 = scale * np.einsum("hd,hd->h", q[0, 0], k[0, 0])
+            np.testing.assert_allclose(L[0, :, 0], z00, atol=1e-12)
+        tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(x.transpose(0, 2, 1, 3))) for x in (q, k, v))
+        mask = torch.ones(S, S, dtype=torch.bool).tril() if causal else None
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=scale)
+        np.testing.assert_allclose(O, ref.numpy().transpose(0, 2, 1, 3), atol=1e-12)
