@@ -203,3 +203,23 @@ def test_wide_full_size_sampled_rows():
         rows = np.sort(np.concatenate([rng.choice(S, 20, replace=False), [0, S - 1]]))
         Oref, Lref = attention_rows(qb, kb, vb, "bf16", True, D ** -0.5, b, h, rows)
         assert_close(O[b, rows, h, :], L[b, h, rows], Oref, Lref, "bf16", f"D256 b={b} h={h}")
+
+
+@pytest.mark.parametrize("S", [1, 2, 127, 129, 255, 257, 383])
+@pytest.mark.parametrize("causal", [False, True])
+def test_wide_edge_lengths(S, causal):
+    """One key, tile boundaries and lengths that are not multiples of 8."""
+    D, dtype = 256, "f16"
+    qb, kb, vb = fa_inputs.make_qkv(1, 2, S, D, dtype, "stress", 160 + S)
+    O, L = run_gpu(qb, kb, vb, dtype, causal, D ** -0.5)
+    Oref, Lref = attention_reference(qb, kb, vb, dtype, causal, D ** -0.5)
+    assert_close(O, L, Oref, Lref, dtype, f"D256 S{S} causal={causal}")
+
+
+def test_wide_many_heads_one_wave_and_more():
+    """More CTAs than SMs (B4 H40 S300 -> 480 CTAs), grouped K/V heads."""
+    B, H, H_kv, S, D = 4, 40, 8, 300, 192
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, "bf16", "normal", 170, h_kv=H_kv)
+    O, L = run_gpu(qb, kb, vb, "bf16", True, D ** -0.5)
+    Oref, Lref = attention_reference(qb, kb, vb, "bf16", True, D ** -0.5)
+    assert_close(O, L, Oref, Lref, "bf16", "D192 many heads")
