@@ -197,7 +197,8 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     """O, LSE for torch CUDA tensors q [B, S, H, D] and k, v [B, S, H_kv, D].
 
     q, k, v must be contiguous fp16 or bf16 tensors on the same CUDA device;
-    H_kv must divide H (query head h uses K/V head h // (H / H_kv)).
+    H_kv must divide H (query head h uses K/V head h // (H / H_kv)); D is a
+    multiple of 8 up to 256 (above 128 without ``window`` or dropout).
     ``out`` / ``lse`` may be preallocated ([B, S, H, D] same dtype; [B, H, S]
     fp32).  Work is enqueued on ``stream`` (default: the current stream) and
     not waited for.  ``split_kv`` lets the library split the keys of each
