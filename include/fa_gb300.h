@@ -243,9 +243,10 @@ int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* L
  *   - A shape whose split needs more than 24 MiB (fa_splitkv_workspace_size)
  *     is rejected with FA_ERR_UNSUPPORTED before anything is launched; shapes
  *     that are not split need no scratch and always run.  On a 152-SM GB300
- *     every split of D = 64, and of D = 128 without the causal mask, fits
- *     (at most about 20 MiB); the longest D = 128 causal splits (up to about
- *     38 MiB, e.g. B = H = 1, S = 4096) are rejected.
+ *     every split of D <= 64, and of D <= 128 without the causal mask, fits
+ *     (at most about 20 MiB); the longest causal splits of 64 < D <= 128 (up
+ *     to about 38 MiB, e.g. B = H = 1, S = 4096) are rejected.  D > 128 is
+ *     never split.
  *   - The first call on a device looks up the array's device address on that
  *     device (with it current); make that first call before any stream
  *     capture on the device.
@@ -266,7 +267,8 @@ const char* fa_status_string(int status);
 
 /*
  * Device-side status of the calls made so far on the current device:
- * FA_OK, or FA_ERR_TIMEOUT if some kernel gave up on a wait.  Synchronises
+ * FA_OK, or the first failure seen: FA_ERR_TIMEOUT if some kernel gave up on
+ * a wait, FA_ERR_BAD_SEQLENS if fa_fwd_varlen met offsets out of range.  Synchronises
  * the device.  clear != 0 resets the word to FA_OK.  Returns FA_ERR_CUDA if the
  * status word cannot be read.
  */
