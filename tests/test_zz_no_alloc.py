@@ -74,6 +74,9 @@ def _static(lib, q, k, v, causal, scale, code):
     (1, 1, 4096, 64, "f16", True),
     (1, 2, 2000, 128, "bf16", True),
     (2, 3, 300, 64, "f16", False),
+    (1, 1, 3000, 40, "f16", True),      # other head dimensions: split on the D = 64 kernel
+    (1, 1, 1500, 96, "bf16", False),    # ... on the D = 128 kernel
+    (1, 2, 700, 256, "f16", True),      # D > 128: never split, no scratch
 ])
 def test_static_scratch_matches_caller_workspace(lib, B, H, S, D, dtype, causal):
     import torch
