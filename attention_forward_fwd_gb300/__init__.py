@@ -181,13 +181,41 @@ _WORKSPACES = {}
 
 
 def _workspace(device, stream_handle: int, nbytes: int):
+    """The cached workspace of (device, stream), grown to nbytes.  It is
+    allocated while the call's own stream is current, so that the caching
+    allocator hands a replaced buffer's memory out again only in that
+    stream's order, after the kernels that still read it."""
     import torch
     key = (str(device), int(stream_handle))
     buf = _WORKSPACES.get(key)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _WORKSPACES.pop(key, None)
+        target = next((st for st in (torch.cuda.current_stream(device),
+                                     torch.cuda.default_stream(device))
+                       if st.cuda_stream == stream_handle), None)
+        if target is None:
+            target = torch.cuda.ExternalStream(stream_handle, device=device)
+        with torch.cuda.stream(target):
+            buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
         _WORKSPACES[key] = buf
     return buf
+
+
+def _stream_handle(stream) -> int:
+    """The cudaStream_t of `stream`: None (torch's current stream), a torch
+    stream object, or a raw handle."""
+    import torch
+    if stream is None:
+        return int(torch.cuda.current_stream().cuda_stream)
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _check_devices(device, **tensors):
+    """Every tensor given must live on `device` (the kernels take raw pointers
+    and would read another GPU's memory through them)."""
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, q on {device}")
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
@@ -200,8 +228,8 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     H_kv must divide H (query head h uses K/V head h // (H / H_kv)); D is a
     multiple of 8 up to 256 (above 128 without ``window`` or dropout).
     ``out`` / ``lse`` may be preallocated ([B, S, H, D] same dtype; [B, H, S]
-    fp32).  Work is enqueued on ``stream`` (default: the current stream) and
-    not waited for.  ``split_kv`` lets the library split the keys of each
+    fp32), on q's device.  Work is enqueued on ``stream`` (a torch stream or
+    a raw handle; default: the current stream) and not waited for.  ``split_kv`` lets the library split the keys of each
     query block over several CTAs when the shape leaves SMs idle (the
     workspace is allocated with torch and cached per device and stream).
     ``window = (left, right)`` restricts query i to keys i - left .. i + right
@@ -225,6 +253,7 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         raise ValueError("k, v must match q in B, S, D, with H_kv dividing H")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
+    _check_devices(q.device, k=k, v=v, out=out, lse=lse)
     if not (0.0 <= dropout_p < 1.0):
         raise ValueError("dropout_p must be in [0, 1)")
     if dropout_p > 0.0 and window is not None:
@@ -244,7 +273,7 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor")
     dtype = FA_F16 if q.dtype == torch.float16 else FA_BF16
     with torch.cuda.device(q.device):
-        st = torch.cuda.current_stream().cuda_stream if stream is None else int(stream)
+        st = _stream_handle(stream)
         lse_ptr = lse.data_ptr() if lse is not None else None
         nbytes = (fa_splitkv_workspace_size(B, H, S, D, causal)
                   if split_kv and window is None and dropout_p == 0.0 else 0)
@@ -276,9 +305,10 @@ def attention_forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool 
     q [total, H, D], k, v [total, H_kv, D] (contiguous fp16 / bf16, H_kv
     dividing H), cu_seqlens an int32 CUDA tensor [B + 1] of sequence offsets
     (cu_seqlens[0] = 0), max_seqlen the longest sequence.  Returns
-    out [total, H, D] and lse [H, total] (fp32).  Work is enqueued on
-    ``stream`` (default: the current stream) and not waited for; offsets that
-    are out of range are reported by ``fa_device_status()``.
+    out [total, H, D] and lse [H, total] (fp32); every tensor on q's device.
+    Work is enqueued on ``stream`` (a torch stream or a raw handle; default:
+    the current stream) and not waited for; offsets that are out of range are
+    reported by ``fa_device_status()``.
     """
     import torch
     for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens", cu_seqlens)):
@@ -290,6 +320,7 @@ def attention_forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool 
         raise ValueError("q, k, v must be fp16 or bf16 of one dtype")
     if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
         raise ValueError("cu_seqlens must be an int32 tensor [B + 1]")
+    _check_devices(q.device, k=k, v=v, cu_seqlens=cu_seqlens, out=out, lse=lse)
     if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape or k.shape[0] != q.shape[0] \
             or k.shape[2] != q.shape[2] or q.shape[1] % k.shape[1] != 0:
         raise ValueError("q must be [total, H, D] and k, v [total, H_kv, D], H_kv dividing H")
@@ -309,7 +340,7 @@ def attention_forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool 
         raise ValueError("lse must be a contiguous fp32 [H, total] tensor")
     dtype = FA_F16 if q.dtype == torch.float16 else FA_BF16
     with torch.cuda.device(q.device):
-        st = torch.cuda.current_stream().cuda_stream if stream is None else int(stream)
+        st = _stream_handle(stream)
         rc = fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                            lse.data_ptr() if lse is not None else None, cu_seqlens.data_ptr(),
                            B, max_seqlen, total, H, H_kv, D, causal, scale, dtype, st)

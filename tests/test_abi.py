@@ -137,3 +137,25 @@ def test_binding_rejects_mismatched_kv_heads():
     k = torch.zeros(1, 8, 3, 64, dtype=torch.float16, device="cuda")
     with pytest.raises(ValueError):
         fa.attention_forward(q, k, k)
+
+
+def test_binding_takes_torch_stream_objects_and_raw_handles():
+    class FakeStream:
+        cuda_stream = 0x1234
+    assert fa._stream_handle(FakeStream()) == 0x1234
+    assert fa._stream_handle(0x5678) == 0x5678
+
+
+def test_binding_rejects_tensors_on_another_device():
+    import torch
+    here, there = torch.device("cuda", 0), torch.device("cuda", 1)
+
+    class T:
+        def __init__(self, dev):
+            self.device = dev
+    fa._check_devices(here, k=T(here), v=T(here), out=None, lse=None)
+    for name in ("k", "v", "out", "lse", "cu_seqlens"):
+        tensors = dict(k=T(here), v=T(here))
+        tensors[name] = T(there)
+        with pytest.raises(ValueError, match=name):
+            fa._check_devices(here, **tensors)

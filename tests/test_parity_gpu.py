@@ -285,3 +285,32 @@ def test_output_written_only_inside_the_tensor():
     assert torch.all(lbuf[:64] == 3.0) and torch.all(lbuf[64 + B * H * S:] == 3.0)
     Oref, Lref = attention_reference(qb, kb, vb, "f16", False, 0.125)
     assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), Oref, Lref, "f16")
+
+
+def test_stream_argument_with_a_split_call():
+    """A torch stream object passed as ``stream=`` (not made current): the
+    split path's workspace is allocated for that stream, the call runs there,
+    and the result matches the oracle; a second shape that needs a larger
+    workspace (about 1.1 MB, then 9.7 MB on 152 SMs) replaces the cached
+    buffer of that stream."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    s = torch.cuda.Stream()
+    key = (str(torch.device("cuda", torch.cuda.current_device())), int(s.cuda_stream))
+    fa._WORKSPACES.pop(key, None)   # stream handles are recycled by torch's pool
+    sizes = []
+    for S, seed in ((1024, 21), (3000, 22)):
+        need = fa.fa_splitkv_workspace_size(1, 1, S, 64, False)
+        assert need > 0
+        qb, kb, vb = fa_inputs.make_qkv(1, 1, S, 64, "f16", "normal", seed)
+        q, k, v = (fa_inputs.to_torch(x, "f16").cuda() for x in (qb, kb, vb))
+        torch.cuda.synchronize()
+        o, lse = fa.attention_forward(q, k, v, causal=False, scale=0.125, stream=s)
+        s.synchronize()
+        assert fa._WORKSPACES[key].numel() >= need
+        sizes.append(fa._WORKSPACES[key].numel())
+        Oref, Lref = attention_reference(qb, kb, vb, "f16", False, 0.125)
+        assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), Oref, Lref, "f16",
+                     f"S{S} on a stream object")
+    if fa.fa_splitkv_workspace_size(1, 1, 3000, 64, False) > sizes[0]:
+        assert sizes[1] > sizes[0]
