@@ -24,7 +24,8 @@ roofline   the dominant kernel (the only kernel of the path) against the
            measured tensor peak; traffic is read from the committed ncu
            summary when it was taken on the current kernel sources.
 cpu_baseline  the fp64 oracle as it stands on the host cores, on a bounded
-           sample of the same workload.
+           sample of the same workload; with the host's CPU model and the
+           oracle on one thread over the S = 256 workload.
 
 --impl reference times the oracle alone (the reference arm) on the same
 workload, metric and unit.  With N > 1 (torchrun) every rank runs an
@@ -289,6 +290,38 @@ def cpu_baseline(w: fa_inputs.Workload, budget_s: float = 15.0, inputs=None):
                       f"fp64 numpy, BLAS threads = cores; {dt:.1f} s"}
 
 
+def _cpu_model() -> str:
+    """The host CPU's model name, as the kernel reports it (x86 and Arm)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "CPU part"):
+        for line in text.splitlines():
+            if line.split(":")[0].strip() == key:
+                return f"{key}: {line.split(':', 1)[1].strip()}"
+    return "unknown"
+
+
+def cpu_baseline_one_thread(workload: str = "s256", budget_s: float = 1.0):
+    """The oracle on one host thread: a child process with the BLAS thread
+    pools set to one before numpy loads, on a bounded sample of `workload`."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench, fa_inputs; "
+            "print(json.dumps(bench.cpu_baseline(fa_inputs.WORKLOADS[%r], budget_s=%r)))"
+            % (ROOT, workload, float(budget_s)))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=300)
+    if r.returncode != 0:
+        return {"error": (r.stderr.strip().splitlines() or ["exit %d" % r.returncode])[-1]}
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    out["cores"] = 1
+    out["sample"] = out["sample"].replace("BLAS threads = cores", "BLAS threads = 1")
+    return out
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest of every rank's x (the slowest rank sets the job's time)."""
     if world == 1:
@@ -450,6 +483,8 @@ def run_ours(args, w):
     line["pages_protocol"] = pages_protocol(step, stream, dev, flops_step)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+        line["cpu_baseline"]["cpu_model"] = _cpu_model()
+        line["cpu_baseline"]["one_thread_s256"] = cpu_baseline_one_thread("s256")
     if args.all_workloads:
         line["other_workloads"] = other_workloads(lib, fa, dev, stream, flush, w.name, peak)
     print(json.dumps(line), flush=True)

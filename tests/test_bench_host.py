@@ -102,3 +102,12 @@ def test_cpu_baseline_takes_at_least_one_whole_head():
     assert out["kind"] == "oracle" and out["unit"] == "TFLOP/s"
     assert out["value"] > 0 and out["cores"] >= 1
     assert out["sample"].startswith("1 (b,h) heads of s256")
+
+
+def test_one_thread_oracle_sample_and_cpu_model():
+    bench = _bench()
+    assert bench._cpu_model()
+    out = bench.cpu_baseline_one_thread("s256", budget_s=0.05)
+    assert "error" not in out, out
+    assert out["cores"] == 1 and out["kind"] == "oracle" and out["value"] > 0
+    assert "BLAS threads = 1" in out["sample"]
