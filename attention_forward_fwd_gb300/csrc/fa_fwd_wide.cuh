@@ -31,6 +31,9 @@ constexpr int kWideAtoms = kWideD / 64;                 // 64-column boxes per r
 constexpr int kWideTileBytes = kBM * kWideD * 2;        // one 128 x 256 16-bit tile
 constexpr uint32_t kWideTmemCols = 512;   // S/P buffers [0, 128) and [384, 512), O [128, 384)
 constexpr uint32_t kWideS1 = 384;         // column of the second S/P buffer
+// K and V bytes of the heads whose CTAs are ordered together (a share of the
+// 126 MB L2, leaving room for the next group and the Q / O traffic)
+constexpr long long kWideL2Share = 32ll << 20;
 
 struct WideBars {
     uint64_t q_full;
@@ -60,8 +63,11 @@ struct WideSmem {
     static_assert(kAlloc <= 232448, "shared memory beyond the 227 KiB a CTA may use");
 };
 
-// Work item x of the grid: heads fastest, query tiles heaviest first when
-// causal (as the main kernel's order).
+// Work item x of the grid.  Heads are taken in groups whose K and V fit in
+// kWideL2Share bytes together; inside a group, heads fastest and query tiles
+// heaviest first when causal.  The CTAs of a group run at about the same
+// time, so each head's K / V comes from DRAM about once, where an order over
+// all heads at once read every head's prefix again in every wave of CTAs.
 template <bool BF16>
 __global__ void __launch_bounds__(kWideThreads, 1)
     fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -78,14 +84,20 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
     // ------------------------------------------------------------ the item
     const int bhn = p.B * p.H;
+    const int ntq = (p.S + kBM - 1) / kBM;
+    const long long kv_head_bytes = 4ll * p.S * p.d_head;   // K and V of one head, 16-bit
+    const int group = static_cast<int>(
+        max(1ll, min(static_cast<long long>(bhn), kWideL2Share / kv_head_bytes)));
     const int x = static_cast<int>(blockIdx.x);
-    const int y = x / bhn;
-    const int bh = x - y * bhn;
+    const int g0 = (x / (group * ntq)) * group;   // first head of x's group
+    const int gsize = min(group, bhn - g0);
+    const int local = x - g0 * ntq;               // in [0, gsize * ntq)
+    const int y = local / gsize;
+    const int bh = g0 + (local - y * gsize);
     const int b = bh / p.H;
     const int h = bh - b * p.H;
     const int hkv = h / p.kv_group;
     const bool causal = p.causal != 0;
-    const int ntq = (p.S + kBM - 1) / kBM;
     const int qt = causal ? (ntq - 1 - y) : y;
     const int r0 = qt * kBM;
     const int n_tiles = key_tiles_for(r0, p.S, causal);   // >= 1 (key 0 is always visible)
