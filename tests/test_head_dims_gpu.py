@@ -223,3 +223,23 @@ def test_wide_many_heads_one_wave_and_more():
     O, L = run_gpu(qb, kb, vb, "bf16", True, D ** -0.5)
     Oref, Lref = attention_reference(qb, kb, vb, "bf16", True, D ** -0.5)
     assert_close(O, L, Oref, Lref, "bf16", "D192 many heads")
+
+
+def test_wide_partial_last_head_group():
+    """The wide kernel numbers its CTAs by groups of heads whose K and V fit
+    in 32 MB together: at S = 8192, D = 256 that is 4 heads, so 6 query heads
+    form a group of 4 and one of 2 (grouped K/V heads, 3 query heads each).
+    Sampled rows of every head, non-causal."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    B, H, H_kv, S, D = 1, 6, 2, 8192, 256
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, "bf16", "normal", 171, h_kv=H_kv)
+    q, k, v = (fa_inputs.to_torch(x, "bf16").cuda() for x in (qb, kb, vb))
+    o, lse = fa.attention_forward(q, k, v, causal=False, scale=D ** -0.5)
+    torch.cuda.synchronize()
+    O, L = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    rng = np.random.default_rng(11)
+    for h in range(H):
+        rows = np.sort(np.concatenate([rng.choice(S, 12, replace=False), [0, S - 1]]))
+        Oref, Lref = attention_rows(qb, kb, vb, "bf16", False, D ** -0.5, 0, h, rows)
+        assert_close(O[0, rows, h, :], L[0, h, rows], Oref, Lref, "bf16", f"D256 h={h}")
