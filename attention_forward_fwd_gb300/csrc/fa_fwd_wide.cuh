@@ -32,8 +32,11 @@ constexpr int kWideTileBytes = kBM * kWideD * 2;        // one 128 x 256 16-bit 
 constexpr uint32_t kWideTmemCols = 512;   // S/P buffers [0, 128) and [384, 512), O [128, 384)
 constexpr uint32_t kWideS1 = 384;         // column of the second S/P buffer
 // K and V bytes of the heads whose CTAs are ordered together (a share of the
-// 126 MB L2, leaving room for the next group and the Q / O traffic)
-constexpr long long kWideL2Share = 32ll << 20;
+// 126 MB L2, leaving room for the next group and the Q / O traffic).  Causal
+// calls take larger groups: their query tiles differ in cost, and a group
+// must hold enough of them for the heaviest-first order to balance the SMs.
+constexpr long long kWideL2Share = 16ll << 20;
+constexpr long long kWideL2ShareCausal = 32ll << 20;
 
 struct WideBars {
     uint64_t q_full;
@@ -64,8 +67,9 @@ struct WideSmem {
 };
 
 // Work item x of the grid.  Heads are taken in groups whose K and V fit in
-// kWideL2Share bytes together; inside a group, heads fastest and query tiles
-// heaviest first when causal.  The CTAs of a group run at about the same
+// kWideL2Share (causal: kWideL2ShareCausal) bytes together; inside a group,
+// heads fastest and query tiles heaviest first when causal.  The CTAs of a
+// group run at about the same
 // time, so each head's K / V comes from DRAM about once, where an order over
 // all heads at once read every head's prefix again in every wave of CTAs.
 template <bool BF16>
@@ -85,9 +89,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     // ------------------------------------------------------------ the item
     const int bhn = p.B * p.H;
     const int ntq = (p.S + kBM - 1) / kBM;
+    const bool causal = p.causal != 0;
     const long long kv_head_bytes = 4ll * p.S * p.d_head;   // K and V of one head, 16-bit
-    const int group = static_cast<int>(
-        max(1ll, min(static_cast<long long>(bhn), kWideL2Share / kv_head_bytes)));
+    const int group = static_cast<int>(max(
+        1ll, min(static_cast<long long>(bhn), (causal ? kWideL2ShareCausal : kWideL2Share) / kv_head_bytes)));
     const int x = static_cast<int>(blockIdx.x);
     const int g0 = (x / (group * ntq)) * group;   // first head of x's group
     const int gsize = min(group, bhn - g0);
@@ -97,7 +102,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int b = bh / p.H;
     const int h = bh - b * p.H;
     const int hkv = h / p.kv_group;
-    const bool causal = p.causal != 0;
     const int qt = causal ? (ntq - 1 - y) : y;
     const int r0 = qt * kBM;
     const int n_tiles = key_tiles_for(r0, p.S, causal);   // >= 1 (key 0 is always visible)

@@ -225,21 +225,23 @@ def test_wide_many_heads_one_wave_and_more():
     assert_close(O, L, Oref, Lref, "bf16", "D192 many heads")
 
 
-def test_wide_partial_last_head_group():
+@pytest.mark.parametrize("H,H_kv,causal", [(6, 2, True), (5, 1, False)])
+def test_wide_partial_last_head_group(H, H_kv, causal):
     """The wide kernel numbers its CTAs by groups of heads whose K and V fit
-    in 32 MB together: at S = 8192, D = 256 that is 4 heads, so 6 query heads
-    form a group of 4 and one of 2 (grouped K/V heads, 3 query heads each).
-    Sampled rows of every head, non-causal."""
+    in 32 MB (causal) or 16 MB (non-causal) together: at S = 8192, D = 256
+    that is 4 or 2 heads, so 6 causal query heads form groups of 4 and 2, and
+    5 non-causal ones groups of 2, 2 and 1 (grouped K/V heads in both).
+    Sampled rows of every head."""
     import torch
     import attention_forward_fwd_gb300 as fa
-    B, H, H_kv, S, D = 1, 6, 2, 8192, 256
-    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, "bf16", "normal", 171, h_kv=H_kv)
+    B, S, D = 1, 8192, 256
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, "bf16", "normal", 171 + H, h_kv=H_kv)
     q, k, v = (fa_inputs.to_torch(x, "bf16").cuda() for x in (qb, kb, vb))
-    o, lse = fa.attention_forward(q, k, v, causal=False, scale=D ** -0.5)
+    o, lse = fa.attention_forward(q, k, v, causal=causal, scale=D ** -0.5)
     torch.cuda.synchronize()
     O, L = o.double().cpu().numpy(), lse.double().cpu().numpy()
     rng = np.random.default_rng(11)
     for h in range(H):
         rows = np.sort(np.concatenate([rng.choice(S, 12, replace=False), [0, S - 1]]))
-        Oref, Lref = attention_rows(qb, kb, vb, "bf16", False, D ** -0.5, 0, h, rows)
+        Oref, Lref = attention_rows(qb, kb, vb, "bf16", causal, D ** -0.5, 0, h, rows)
         assert_close(O[0, rows, h, :], L[0, h, rows], Oref, Lref, "bf16", f"D256 h={h}")
