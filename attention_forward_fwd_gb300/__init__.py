@@ -14,7 +14,7 @@ import os
 from .build import LIB_PATH, build  # noqa: F401
 
 __all__ = ["fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
-           "fa_device_status", "fa_kernels_per_call", "attention_forward",
+           "fa_device_status", "fa_last_device_status", "attention_forward",
            "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_launches",
            "fa_fwd_gqa", "fa_fwd_gqa_splitkv", "fa_fwd_varlen", "attention_forward_varlen",
            "fa_fwd_local", "fa_fwd_dropout",
@@ -25,7 +25,7 @@ __all__ = ["fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
 FA_F16, FA_BF16 = 0, 1
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
-                    "fa_device_status", "fa_kernels_per_call", "fa_splitkv_workspace_size",
+                    "fa_device_status", "fa_last_device_status", "fa_splitkv_workspace_size",
                     "fa_splitkv_launches", "fa_fwd_splitkv", "fa_fwd_gqa", "fa_fwd_gqa_splitkv",
                     "fa_fwd_varlen", "fa_fwd_local", "fa_selftest_timeout", "fa_fwd_dropout")
 
@@ -57,8 +57,8 @@ def library() -> ctypes.CDLL:
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_device_status.argtypes = [i]
         lib.fa_device_status.restype = i
-        lib.fa_kernels_per_call.argtypes = []
-        lib.fa_kernels_per_call.restype = i
+        lib.fa_last_device_status.argtypes = [vp]
+        lib.fa_last_device_status.restype = i
         lib.fa_splitkv_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         lib.fa_splitkv_workspace_size.restype = i
         lib.fa_splitkv_launches.argtypes = [i, i, i, i, i]
@@ -94,8 +94,11 @@ def fa_device_status(clear: bool = False) -> int:
     return int(library().fa_device_status(1 if clear else 0))
 
 
-def fa_kernels_per_call() -> int:
-    return int(library().fa_kernels_per_call())
+def fa_last_device_status(stream=None) -> int:
+    """The device status word after the work enqueued on `stream` so far
+    (a torch stream, a raw handle, or None for the current stream); waits
+    for that stream only and does not clear the word."""
+    return int(library().fa_last_device_status(_stream_handle(stream)))
 
 
 def fa_fwd(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype, stream) -> int:

@@ -18,6 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+COMPILE_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC"]
 
 
 def _nvcc() -> str:
@@ -35,11 +36,32 @@ def _sources():
     return deps
 
 
+STAMP_PATH = LIB_PATH + ".sha256"
+
+
+def source_hash() -> str:
+    """SHA-256 over the library's sources (names and contents), the compile
+    command's flags and this machine's architecture: the stamp a built
+    library must carry to be reused."""
+    import hashlib
+    import platform
+    h = hashlib.sha256()
+    h.update(" ".join(ARCH_FLAGS + COMPILE_FLAGS).encode())
+    h.update(platform.machine().encode())
+    for path in _sources():
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
 def needs_build() -> bool:
-    if not os.path.exists(LIB_PATH):
+    """True unless the library exists and its stamp matches the sources (file
+    times are not trusted: a copied tree can carry a library newer than
+    sources it was not built from)."""
+    if not (os.path.exists(LIB_PATH) and os.path.exists(STAMP_PATH)):
         return True
-    t = os.path.getmtime(LIB_PATH)
-    return any(os.path.getmtime(d) > t for d in _sources())
+    with open(STAMP_PATH) as f:
+        return f.read().strip() != source_hash()
 
 
 # Registers per thread the attention kernel must launch with, by its last
@@ -82,14 +104,15 @@ def check_launch_registers(ptxas_log: str) -> None:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if it is missing or older than its sources."""
+    """Compile the library unless it exists with the stamp of the current
+    sources."""
     if not force and not needs_build():
         return LIB_PATH
     out_dir = os.path.join(ROOT, "_build")
     os.makedirs(out_dir, exist_ok=True)
     tmp = LIB_PATH + ".tmp"
-    cmd = [_nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-shared",
-           "-Xcompiler", "-fPIC", "-Xptxas", "-v", "-I", INCLUDE,
+    stamp = source_hash()
+    cmd = [_nvcc(), *ARCH_FLAGS, *COMPILE_FLAGS, "-Xptxas", "-v", "-I", INCLUDE,
            "-o", tmp, os.path.join(CSRC, "fa_api.cu")]
     res = subprocess.run(cmd, capture_output=True, text=True)
     with open(os.path.join(out_dir, "ptxas.txt"), "w") as f:
@@ -102,6 +125,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         os.remove(tmp)
         raise
     os.replace(tmp, LIB_PATH)
+    with open(STAMP_PATH, "w") as f:
+        f.write(stamp + "\n")
     if verbose:
         print(res.stderr)
     return LIB_PATH

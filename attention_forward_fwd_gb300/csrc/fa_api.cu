@@ -77,15 +77,17 @@ constexpr int kRowSplitD128 = FA_ROW_SPLIT_D128;
 constexpr int kRingD64 = FA_RING_D64;
 constexpr int kRingD128 = FA_RING_D128;
 
+// SMs of the current device (0 if it cannot be read), looked up once per
+// device; host threads may call concurrently.
 int num_sms() {
-    static int cached[64] = {0};
+    static std::once_flag once[64];
+    static int cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached[dev] == 0) {
+    std::call_once(once[dev], [&] {
         int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cached[dev] = n;
-    }
+        cached[dev] = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? n : 0;
+    });
     return cached[dev];
 }
 
@@ -514,7 +516,16 @@ int fa_device_status(int clear) {
     return v;
 }
 
-int fa_kernels_per_call(void) { return 1; }
+int fa_last_device_status(fa_stream_t stream) {
+    // pageable destination: the copy returns once it has landed, in stream order
+    int v = 0;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyFromSymbolAsync(&v, fa::g_fa_device_status, sizeof(int), 0, cudaMemcpyDeviceToHost,
+                                  st) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+    return v;
+}
 
 int fa_selftest_timeout(const void* Q, const void* K, const void* V, void* O, int S, int D, int dtype,
                         fa_stream_t stream) {
@@ -582,12 +593,11 @@ extern "C" int fa_fwd_splitkv_static(const void* Q, const void* K, const void* V
     const SplitPlan plan = plan_split(B, H, S, D, causal != 0, sms);
     const size_t need = workspace_bytes_for(plan, B, H, S, D);
     if (need > kStaticWorkspaceBytes) return FA_ERR_UNSUPPORTED;
-    void* ws = nullptr;
-    if (need > 0) {
-        int status = FA_OK;
-        ws = static_workspace_address(&status);
-        if (ws == nullptr) return status;
-    }
+    // looked up on every call (free after the first), so that the first call
+    // on a device does the lookup whether or not its shape is split
+    int status = FA_OK;
+    void* ws = static_workspace_address(&status);
+    if (ws == nullptr) return status;
     return dispatch(Q, K, V, O, LSE, B, H, H, S, D, causal, scale, dtype,
                     reinterpret_cast<cudaStream_t>(stream), plan, ws);
 }

@@ -90,7 +90,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int bhn = p.B * p.H;
     const int ntq = (p.S + kBM - 1) / kBM;
     const bool causal = p.causal != 0;
-    const long long kv_head_bytes = 4ll * p.S * p.d_head;   // K and V of one head, 16-bit
+    // K and V bytes (16-bit) per query head: query heads h .. h + kv_group - 1
+    // share one K/V head, so a group of them holds 1/kv_group of that each
+    const long long kv_head_bytes = max(1ll, 4ll * p.S * p.d_head / p.kv_group);
     const int group = static_cast<int>(max(
         1ll, min(static_cast<long long>(bhn), (causal ? kWideL2ShareCausal : kWideL2Share) / kv_head_bytes)));
     const int x = static_cast<int>(blockIdx.x);

@@ -5,10 +5,11 @@
                     [--impl ours|reference]
 
 One step = one pass of the hot path over one batch of the workload: every
-mask mode the workload is run with (s4096: non-causal and causal), each one
-call of the C-ABI entry point fa_fwd_splitkv (which splits the keys of each
-query block over several CTAs when the shape would leave SMs idle, and then
-launches the merge kernel as a second launch).  Metric: attention forward TFLOP/s, counting
+mask mode the workload is run with (the default b2h16d128 -- B2 H16 S8192
+D128 bf16, the largest single-GPU configuration -- non-causal and causal),
+each one call of the C-ABI entry point fa_fwd_gqa_splitkv (which splits the
+keys of each query block over several CTAs when the shape would leave SMs
+idle, and then merges the partial results).  Metric: attention forward TFLOP/s, counting
 4*B*H*S^2*D FLOPs per call (half when causal), and its fraction of the
 measured dense bf16/fp16 tensor peak.
 
@@ -26,6 +27,11 @@ roofline   the dominant kernel (the only kernel of the path) against the
 cpu_baseline  the fp64 oracle as it stands on the host cores, on a bounded
            sample of the same workload; with the host's CPU model and the
            oracle on one thread over the S = 256 workload.
+
+configs    kernel-timed TFLOP/s of the other four target configurations (s256,
+           s4096, b4h16, stress; every mask mode), L2 flushed before each
+           call; --all-workloads adds grouped K/V heads, packed batches,
+           windows, dropout and other head dimensions.
 
 --impl reference times the oracle alone (the reference arm) on the same
 workload, metric and unit.  With N > 1 (torchrun) every rank runs an
@@ -52,7 +58,9 @@ import numpy as np  # noqa: E402
 
 import fa_inputs  # noqa: E402
 
-DEFAULT_WORKLOAD = "s4096"
+DEFAULT_WORKLOAD = "b2h16d128"
+# the five target configurations (the headline is one of them)
+TARGET_WORKLOADS = ("s256", "s4096", "b4h16", "b2h16d128", "stress")
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -481,12 +489,17 @@ def run_ours(args, w):
             "e2e": e2e,
             "wall_s_timed_region": t_wall}
     line["pages_protocol"] = pages_protocol(step, stream, dev, flops_step)
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
         line["cpu_baseline"]["cpu_model"] = _cpu_model()
         line["cpu_baseline"]["one_thread_s256"] = cpu_baseline_one_thread("s256")
+    if not args.no_configs:
+        line["configs"] = other_workloads(lib, fa, dev, stream, flush, w.name, peak,
+                                          names=TARGET_WORKLOADS, extras=False)
     if args.all_workloads:
-        line["other_workloads"] = other_workloads(lib, fa, dev, stream, flush, w.name, peak)
+        line["other_workloads"] = other_workloads(
+            lib, fa, dev, stream, flush, w.name, peak,
+            names=[n for n in fa_inputs.WORKLOADS if n not in TARGET_WORKLOADS], extras=True)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -647,11 +660,14 @@ def end_to_end(args, w, lib, fa, dev, stream, tq, tk, tv, modes, dtype_code, ws,
             "serial_ms_per_step": serial_ms}
 
 
-def other_workloads(lib, fa, dev, stream, flush, skip, peak):
-    """Kernel-timed TFLOP/s of every other workload and mode (informational)."""
+def other_workloads(lib, fa, dev, stream, flush, skip, peak, names, extras):
+    """Kernel-timed TFLOP/s of the workloads `names` but `skip`, every mask
+    mode, L2 flushed before each call (median of 10 after 3 warm-ups); with
+    `extras`, also the packed, windowed, dropout and head-dimension shapes."""
     import torch
     res = {}
-    for name, w in fa_inputs.WORKLOADS.items():
+    for name in names:
+        w = fa_inputs.WORKLOADS[name]
         if name == skip:
             continue
         qb, kb, vb = fa_inputs.make_qkv_for(w)
@@ -684,6 +700,8 @@ def other_workloads(lib, fa, dev, stream, flush, skip, peak):
                 "ms": t, "tflops": tf, "pct_of_peak": 100.0 * tf / peak,
                 "launches": fa.fa_splitkv_launches(w.B, w.H, w.S, w.D, causal)}
         del q, k, v, o, lse, ws
+    if not extras:
+        return res
     res.update(varlen_workload(lib, fa, dev, stream, flush, peak))
     res.update(window_workload(lib, fa, dev, stream, flush, peak))
     res.update(dropout_workloads(lib, fa, dev, stream, flush, peak))
@@ -853,7 +871,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--all-workloads", action="store_true",
-                    help="also time every other workload (informational)")
+                    help="also time the workloads beyond the five target configurations")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the kernel-timed numbers of the other target configurations")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=10.0,

@@ -50,10 +50,12 @@
  *                       B * H * ceil(S / 256) > 2^31 - 1
  *   FA_ERR_CUDA         a CUDA runtime or driver call failed (the CUDA error
  *                       is left set for the caller to read)
- *   FA_ERR_TIMEOUT      reported by fa_device_status(): a device-side wait
+ *   FA_ERR_TIMEOUT      reported by fa_device_status() and
+ *                       fa_last_device_status(): a device-side wait
  *                       exceeded its time limit and the kernel returned early
  *                       (the outputs of that call are undefined)
- *   FA_ERR_BAD_SEQLENS  reported by fa_device_status(): fa_fwd_varlen found a
+ *   FA_ERR_BAD_SEQLENS  reported by fa_device_status() and
+ *                       fa_last_device_status(): fa_fwd_varlen found a
  *                       sequence offset out of range; nothing of that
  *                       sequence was read or written (its O / LSE rows are
  *                       left as they were)
@@ -274,8 +276,17 @@ const char* fa_status_string(int status);
  */
 int fa_device_status(int clear);
 
-/* Number of kernels one fa_fwd call launches (for launch accounting). */
-int fa_kernels_per_call(void);
+/*
+ * The device status word as the calls enqueued on `stream` so far left it:
+ * the word is read after all of that work (a copy ordered on `stream`, then a
+ * wait for `stream` alone; other streams keep running).  Returns FA_OK,
+ * FA_ERR_TIMEOUT or FA_ERR_BAD_SEQLENS as fa_device_status does, without
+ * clearing it; FA_ERR_CUDA if the copy or the wait fails.  The word is one per
+ * device (the current one) and shared by every stream on it, so a failure of
+ * a kernel on another stream that finished before the read shows here too.
+ * Do not call it inside a stream capture (it waits on the stream).
+ */
+int fa_last_device_status(fa_stream_t stream);
 
 #ifdef __cplusplus
 }

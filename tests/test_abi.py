@@ -45,8 +45,15 @@ def test_status_strings(lib):
     assert fa.fa_status_string(99) == "unknown status"
 
 
-def test_kernels_per_call(lib):
-    assert fa.fa_kernels_per_call() == 1
+def test_last_device_status_is_exported_with_a_stream_argument(lib):
+    """The stream-ordered status read takes one stream handle (no GPU call
+    here: only its presence and signature in the header)."""
+    import re
+    with open(os.path.join(ROOT, "include", "fa_gb300.h")) as f:
+        text = f.read()
+    assert re.search(r"int\s+fa_last_device_status\s*\(\s*fa_stream_t\s+stream\s*\)", text)
+    assert "fa_last_device_status" in fa.EXPORTED_SYMBOLS
+    assert lib.fa_last_device_status.argtypes == [ctypes.c_void_p]
 
 
 GOOD = dict(Q=4096, K=8192, V=12288, O=16384, LSE=20480, B=1, H=1, S=128, D=64,

@@ -12,7 +12,7 @@ import pytest
 import fa_inputs
 from oracle import attention_reference, attention_rows
 
-from gpu_common import assert_close, o_tol, run_gpu
+from gpu_common import assert_bare_tolerance, assert_close, o_tol, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -189,6 +189,7 @@ def test_workload_s256():
         O, L = run_gpu(qb, kb, vb, w.dtype, causal, w.scale)
         Oref, Lref = attention_reference(qb, kb, vb, w.dtype, causal, w.scale)
         assert_close(O, L, Oref, Lref, w.dtype, "s256")
+        assert_bare_tolerance(O, Oref, w.dtype, "s256")
 
 
 @pytest.mark.parametrize("split_kv", [False, True], ids=["one-cta-per-block", "split-kv"])
@@ -198,7 +199,8 @@ def test_workload_s4096(causal, split_kv):
     qb, kb, vb = fa_inputs.make_qkv_for(w)
     O, L = run_gpu(qb, kb, vb, w.dtype, causal, w.scale, split_kv=split_kv)
     Oref, Lref = attention_reference(qb, kb, vb, w.dtype, causal, w.scale)
-    assert_close(O, L, Oref, Lref, w.dtype, "s4096")
+    assert_close(O, L, Oref, Lref, w.dtype, f"s4096 causal={causal} split={split_kv}")
+    assert_bare_tolerance(O, Oref, w.dtype, "s4096")
 
 
 @pytest.mark.parametrize("causal", [True, False])
@@ -209,7 +211,8 @@ def test_workload_stress_full(causal):
     qb, kb, vb = fa_inputs.make_qkv_for(w)
     O, L = run_gpu(qb, kb, vb, w.dtype, causal, w.scale)
     Oref, Lref = attention_reference(qb, kb, vb, w.dtype, causal, w.scale)
-    assert_close(O, L, Oref, Lref, w.dtype, "stress")
+    assert_close(O, L, Oref, Lref, w.dtype, f"stress causal={causal}")
+    assert_bare_tolerance(O, Oref, w.dtype, "stress")
     b, h = w.identical_key_head
     v = Oref[b, :, h, :]
     assert np.all(np.abs(O[b, :, h, :] - v) <= o_tol(v, "f16"))
@@ -225,12 +228,21 @@ def _sampled_rows(S, rng, n=24):
 @pytest.mark.parametrize("name,causal", [("b4h16", True), ("b2h16d128", True),
                                          ("b2h16d128", False), ("b4h32kv8d128", True)])
 def test_workload_full_size_sampled(name, causal):
-    """Full-size workloads in the launch configuration the bench times;
-    sampled rows of several heads against the oracle row by row."""
+    """Full-size workloads in the launch configuration the bench times,
+    against the oracle row by row: the first and the last 256-row query
+    block of every head (the lightest and heaviest work items when causal,
+    the ragged end), and sampled rows of six heads."""
     w = fa_inputs.WORKLOADS[name]
     qb, kb, vb = fa_inputs.make_qkv_for(w)
     O, L = run_gpu(qb, kb, vb, w.dtype, causal, w.scale)
     assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+    edge = sorted(set(range(min(256, w.S))) | set(range(max(0, w.S - 256), w.S)))
+    for b in range(w.B):
+        for h in range(w.H):
+            Oref, Lref = attention_rows(qb, kb, vb, w.dtype, causal, w.scale, b, h, edge)
+            what = f"{name} causal={causal} b{b} h{h} first/last block"
+            assert_close(O[b, edge, h, :], L[b, h, edge], Oref, Lref, w.dtype, what)
+            assert_bare_tolerance(O[b, edge, h, :], Oref, w.dtype, what)
     rng = np.random.default_rng(123)
     heads = [(0, 0), (w.B - 1, w.H - 1)] + [(int(rng.integers(w.B)), int(rng.integers(w.H)))
                                             for _ in range(4)]

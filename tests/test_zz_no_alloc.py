@@ -4,11 +4,14 @@ memory themselves (for example a latency-critical loop that must not pay for
 cudaMalloc's implicit synchronisation, or code whose device memory belongs to
 an allocator it cannot reach).
 
-The test calls the entry point through the C-ABI and compares its output
-with fa_fwd_splitkv (caller-provided workspace) on the same inputs, within
-the parity tolerances, for two calls in a row with different inputs (the
-second call runs on the scratch the first one left behind).  It is collected
-last so that a failure here stops a `-x` run only after every other test.
+The tests call the entry point through the C-ABI and compare its output
+with fa_fwd_splitkv (caller-provided workspace) and with the fp64 oracle on
+the same inputs, within the parity tolerances: two calls in a row with
+different inputs (the second call runs on the scratch the first one left
+behind), and three calls queued back to back on one stream with no wait
+between them (each call's main kernel may start while the previous call's
+merge still reads the array).  They are collected last so that a failure
+here stops a `-x` run only after every other test.
 """
 import ctypes
 
@@ -16,6 +19,7 @@ import numpy as np
 import pytest
 
 import fa_inputs
+from oracle import attention_reference
 
 from gpu_common import lse_tol, o_tol
 
@@ -38,8 +42,20 @@ def lib():
 
 
 def _inputs(B, H, S, D, dtype, seed):
-    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dtype, "stress", seed)
-    return tuple(fa_inputs.to_torch(x, dtype).cuda() for x in (qb, kb, vb))
+    """Device tensors and the 16-bit host bits they hold (for the oracle)."""
+    bits = fa_inputs.make_qkv(B, H, S, D, dtype, "stress", seed)
+    return tuple(fa_inputs.to_torch(x, dtype).cuda() for x in bits), bits
+
+
+def _check(o, lse, o_ref, l_ref, bits, dtype, causal, scale, what):
+    """o, lse against the caller-workspace result and against the oracle."""
+    O, Oref = o.double().cpu().numpy(), o_ref.double().cpu().numpy()
+    L, Lref = lse.double().cpu().numpy(), l_ref.double().cpu().numpy()
+    assert np.all(np.abs(O - Oref) <= o_tol(Oref, dtype)), f"{what}: O differs from fa_fwd_splitkv"
+    assert np.all(np.abs(L - Lref) <= lse_tol(Lref)), f"{what}: LSE differs from fa_fwd_splitkv"
+    Oo, Lo = attention_reference(*bits, dtype, causal, scale)
+    assert np.all(np.abs(O - Oo) <= o_tol(Oo, dtype)), f"{what}: O differs from the oracle"
+    assert np.all(np.abs(L - Lo) <= lse_tol(Lo)), f"{what}: LSE differs from the oracle"
 
 
 def _with_workspace(q, k, v, causal, scale, code):
@@ -85,15 +101,40 @@ def test_static_scratch_matches_caller_workspace(lib, B, H, S, D, dtype, causal)
     code = fa.FA_F16 if dtype == "f16" else fa.FA_BF16
     scale = D ** -0.5
     for call, seed in enumerate((101, 202)):     # two calls in a row
-        q, k, v = _inputs(B, H, S, D, dtype, seed + S)
+        (q, k, v), bits = _inputs(B, H, S, D, dtype, seed + S)
         o_ref, l_ref = _with_workspace(q, k, v, causal, scale, code)
         rc, o, lse = _static(lib, q, k, v, causal, scale, code)
         assert rc == fa.FA_OK, f"call {call}: status {rc}"
         torch.cuda.synchronize()
-        O, Oref = o.double().cpu().numpy(), o_ref.double().cpu().numpy()
-        L, Lref = lse.double().cpu().numpy(), l_ref.double().cpu().numpy()
-        assert np.all(np.abs(O - Oref) <= o_tol(Oref, dtype)), f"call {call}: O differs"
-        assert np.all(np.abs(L - Lref) <= lse_tol(Lref)), f"call {call}: LSE differs"
+        _check(o, lse, o_ref, l_ref, bits, dtype, causal, scale, f"call {call}")
+    assert fa.fa_device_status(clear=False) == fa.FA_OK
+
+
+@pytest.mark.parametrize("B,H,S,D,dtype,causal", [
+    (1, 1, 3000, 40, "f16", True),      # some query tiles see no key of a split
+    (1, 1, 4096, 64, "f16", False),
+])
+def test_static_calls_back_to_back(lib, B, H, S, D, dtype, causal):
+    """Three static calls with different inputs queued on one stream with no
+    wait between them, then one synchronisation: each result must be that
+    call's own (a call's merge must finish reading the shared array before
+    the next call's main kernel writes it)."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    assert fa.fa_splitkv_launches(B, H, S, D, causal) == 2   # the split path runs
+    code = fa.FA_F16 if dtype == "f16" else fa.FA_BF16
+    scale = D ** -0.5
+    cases = [_inputs(B, H, S, D, dtype, seed) for seed in (303, 404, 505)]
+    refs = [_with_workspace(*qkv, causal, scale, code) for qkv, _ in cases]
+    torch.cuda.synchronize()
+    outs = []
+    for qkv, _ in cases:
+        rc, o, lse = _static(lib, *qkv, causal, scale, code)
+        assert rc == fa.FA_OK, rc
+        outs.append((o, lse))
+    torch.cuda.synchronize()
+    for n, ((o, lse), (o_ref, l_ref), (_, bits)) in enumerate(zip(outs, refs, cases)):
+        _check(o, lse, o_ref, l_ref, bits, dtype, causal, scale, f"queued call {n}")
     assert fa.fa_device_status(clear=False) == fa.FA_OK
 
 
