@@ -782,23 +782,26 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             auto full_bar = [&](int i) { return bar_addr(&bars->kv_full[i % NS]); };
             auto full_par = [&](int i) { return static_cast<uint32_t>((i / NS) & 1); };
             auto slot_addr = [&](int i) { return sbase + L::kOffKV + (i % NS) * L::kKVBytes; };
+            // descriptors as low words over one shared high word (SBO 1024,
+            // 128-byte swizzle); the start address field counts 16 bytes
+            const uint32_t desc_hi = ptx::sdesc_sw128_hi(1024);
             auto issue_s = [&](int t, int ring) {
-                const uint64_t a0 = ptx::sdesc_sw128(sbase + L::kOffQ + t * L::kQBytes, 16, 1024);
-                const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), 16, 1024);
+                const uint32_t a0 = ptx::sdesc_sw128_lo(sbase + L::kOffQ + t * L::kQBytes, 16);
+                const uint32_t b0 = ptx::sdesc_sw128_lo(slot_addr(ring), 16);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-                    ptx::mma_ss_warp(tmem + t * kBN, a0 + (oa >> 4), b0 + (ob >> 4), kIdescQK, kk > 0);
+                    ptx::mma_ss_warp_lo(tmem + t * kBN, a0 + (oa >> 4), b0 + (ob >> 4), desc_hi, kIdescQK, kk > 0);
                 }
                 ptx::tc_commit_warp(bar_addr(&bars->s_full[t]));
             };
             auto issue_pv = [&](int t, int ring, bool acc) {
-                const uint64_t b0 = ptx::sdesc_sw128(slot_addr(ring), kBN * 128, 1024);
+                const uint32_t b0 = ptx::sdesc_sw128_lo(slot_addr(ring), kBN * 128);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    ptx::mma_ts_warp(tmem + 2 * kBN + t * D, tmem + p_col(t, kk),
-                                     b0 + ((kk * 16 * 128) >> 4), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                    ptx::mma_ts_warp_lo(tmem + 2 * kBN + t * D, tmem + p_col(t, kk), b0 + ((kk * 16 * 128) >> 4),
+                                        desc_hi, kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
                 ptx::tc_commit_warp(bar_addr(&bars->o_done[t]));
             };
@@ -1070,23 +1073,25 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     auto exp_pass = [&](float mc) {
                         const float2 c2 = make_float2(c, c);
                         const float2 nmc2 = make_float2(-mc, -mc);
-                        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                        float2 sum2[1] = {make_float2(0.f, 0.f)};
+                        // 16 columns at a time (registers are short with two
+                        // threads per row)
 #pragma unroll
-                        for (int q = 0; q < kHalf / 32; ++q) {
-                            uint32_t pk[16];
+                        for (int q = 0; q < kHalf / 16; ++q) {
+                            uint32_t pk[8];
                             uint32_t dw[4] = {};   // dropout draws of 8 of these keys
 #pragma unroll
-                            for (int kq = 0; kq < 16; ++kq) {
+                            for (int kq = 0; kq < 8; ++kq) {
                                 const float2 x = __ffma2_rn(
-                                    make_float2(__uint_as_float(s[q * 32 + 2 * kq]),
-                                                __uint_as_float(s[q * 32 + 2 * kq + 1])),
+                                    make_float2(__uint_as_float(s[q * 16 + 2 * kq]),
+                                                __uint_as_float(s[q * 16 + 2 * kq + 1])),
                                     c2, nmc2);
                                 const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
-                                sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
+                                sum2[0] = __fadd2_rn(sum2[0], pp);
                                 // (one block at a time: two threads share a row here
                                 // and registers are short)
                                 if constexpr (FEAT == kDropout)
-                                    if ((kq & 3) == 0) drop_words<1>(p, kv0 + q * 32 + 2 * kq, row, it, dw);
+                                    if ((kq & 3) == 0) drop_words<1>(p, kv0 + q * 16 + 2 * kq, row, it, dw);
                                 pk[kq] = pack_p<FEAT, BF16>(p, pp, dw[kq & 3]);
                             }
                             if (!p_free && ok) {
@@ -1096,10 +1101,9 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                                 if (ok) ptx::tc_fence_after_sync();
                                 p_free = true;
                             }
-                            if (ok) ptx::tmem_st_32x32b_x16(tP + q * 16, pk);
+                            if (ok) ptx::tmem_st_32x32b_x8(tP + q * 8, pk);
                         }
-                        const float2 s2 = __fadd2_rn(sum2[0], sum2[1]);
-                        sum = s2.x + s2.y;
+                        sum = sum2[0].x + sum2[0].y;
                     };
 
                     // this tile's row max (the RS threads of a row swap their parts)
@@ -1187,6 +1191,12 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 }
             }
 
+            // With two threads per row registers are short: the epilogue
+            // decodes its item again instead of keeping these fields live
+            // through the key loop (the opaque copy of w stops the compiler
+            // from reusing the first decode).  Packed batches read their
+            // offsets from global memory, so they keep the first decode.
+            const WorkItem ie = (kRowSplit > 1 && FEAT != kPacked) ? decode_item<FEAT>(p, ptx::opaque(w)) : it;
             // ------------------------------------------------------- epilogue
             // O_t is read out of TMEM (and waited for) before this thread's first
             // P_t arrival of the next item, which the next item's first P_t V
@@ -1211,11 +1221,11 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 if (n_tiles == 0 && !wait_phase(qbar, ki & 1, abort_flag)) return;
                 ptx::mbar_arrive(bar_addr(&bars->q_empty));
             };
-            if (it.partial && r0 < it.S) {
+            if (ie.partial && r0 < ie.S) {
                 // partial result: o~ stays unnormalised (fp32), m and l go
                 // beside it; a tile that saw no key of this split records l = 0
                 const int ntq = (p.S + kBM - 1) / kBM;
-                const size_t slot = partial_slot(it.bh, ntq, r0 / kBM, p.max_splits, it.split);
+                const size_t slot = partial_slot(ie.bh, ntq, r0 / kBM, p.max_splits, ie.split);
                 float* ml = p.ws_ml + slot * (2 * kBM);
                 float4* po = reinterpret_cast<float4*>(p.ws_o + slot * static_cast<size_t>(kBM * D));
                 if (eok && n_tiles > 0) {
@@ -1246,7 +1256,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 // one thread stores it; rows past S are dropped by the store.
                 // The last tile of a packed sequence is stored row by row
                 // instead (the rows after it belong to the next sequence).
-                const bool direct = kDirectO || (FEAT == kPacked && r0 + kBM > it.S);
+                const bool direct = kDirectO || (FEAT == kPacked && r0 + kBM > ie.S);
                 uint8_t* stage = smem + L::kOffStage + t * L::kQBytes;
                 if (!kStageInQ && !direct && ki > 0) {
                     // the previous item's store must have read the staging buffer
@@ -1258,7 +1268,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 // row of O: batch tb (0 when packed) of S rows, then the
                 // sequence start `base` (0 unless packed)
                 uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +
-                                 ((static_cast<size_t>(it.tb) * p.S + it.base + row) * p.H + it.h) * p.d_head;
+                                 ((static_cast<size_t>(ie.tb) * p.S + ie.base + row) * p.H + ie.h) * p.d_head;
                 if (eok) {
                     ptx::tc_fence_after_sync();
 #pragma unroll
@@ -1280,7 +1290,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                             v.w = pack2<BF16>(__uint_as_float(o[u * 8 + 6]) * inv_l,
                                               __uint_as_float(o[u * 8 + 7]) * inv_l);
                             if (direct) {
-                                if (row < it.S && cc * 8 < p.d_head) *reinterpret_cast<uint4*>(orow + cc * 8) = v;
+                                if (row < ie.S && cc * 8 < p.d_head) *reinterpret_cast<uint4*>(orow + cc * 8) = v;
                             } else {
                                 const int box = cc >> 3;
                                 const int phys = (cc & 7) ^ (r & 7);
@@ -1295,8 +1305,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     all_ok = ptx::named_barrier_and(tile_bar, kTileThreads, eok);
                     if (all_ok && store_thread) {
                         for (int cch = 0; cch < kChunks; ++cch)
-                            ptx::tma_store_4d(&tmO, ptx::smem_addr(stage + cch * (kBM * 128)), cch * 64, it.h,
-                                              it.base + r0, it.tb);
+                            ptx::tma_store_4d(&tmO, ptx::smem_addr(stage + cch * (kBM * 128)), cch * 64, ie.h,
+                                              ie.base + r0, ie.tb);
                         ptx::bulk_commit_group();
                     }
                 }
@@ -1305,11 +1315,11 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     if (!direct) ptx::bulk_wait_group_read_all();
                     ptx::mbar_arrive(bar_addr(&bars->q_empty));
                 }
-                if (eok && hf == 0 && p.lse != nullptr && row < it.S) {
+                if (eok && hf == 0 && p.lse != nullptr && row < ie.S) {
                     // LSE = scale * m + ln l = ln2 * (m * scale * log2e + log2 l)
                     const size_t li = FEAT == kPacked
-                                          ? static_cast<size_t>(it.h) * p.total + it.base + row
-                                          : static_cast<size_t>(it.bh) * p.S + row;
+                                          ? static_cast<size_t>(ie.h) * p.total + ie.base + row
+                                          : static_cast<size_t>(ie.bh) * p.S + row;
                     p.lse[li] = (m_use * c + log2f(l_row)) * 0.69314718055994530942f;
                 }
             } else if (kStageInQ && store_thread) {

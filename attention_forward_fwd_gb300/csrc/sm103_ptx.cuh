@@ -173,6 +173,13 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) 
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* r) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -273,6 +280,38 @@ __device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// The same two issue forms with each shared-memory descriptor given as its low
+// word (start address and leading byte offset, which vary per K step) and
+// one high word shared by both operands (stride byte offset, version and
+// swizzle, fixed for the kernel): 32-bit values keep the issuing warp's
+// unrolled loops within a small register budget.
+__host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo_bytes) {
+    return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ void mma_ss_warp_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred E, P1;\n\t.reg .b64 DA, DB;\n\t"
+        "mov.b64 DA, {%1, %3};\n\tmov.b64 DB, {%2, %3};\n\t"
+        "elect.sync _|E, 0xffffffff;\n\tsetp.ne.b32 P1, %5, 0;\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %4, P1;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_warp_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred E, P1;\n\t.reg .b64 DB;\n\t"
+        "mov.b64 DB, {%2, %3};\n\t"
+        "elect.sync _|E, 0xffffffff;\n\tsetp.ne.b32 P1, %5, 0;\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], DB, %4, P1;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -330,6 +369,13 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// The value of x, hidden from the optimiser (it cannot reuse a computation
+// made from x before this point).
+__device__ __forceinline__ int opaque(int x) {
+    asm volatile("" : "+r"(x));
+    return x;
 }
 
 // ----------------------------------------------------------------- math
