@@ -199,10 +199,21 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             if (!(ok = wait_warp(bar(&bars->kv_full[0]), static_cast<uint32_t>(i & 1)))) return;
             ptx::tc_fence_after_sync();
             const uint32_t d = tmem + ((i & 1) ? kWideS1 : 0u);
+            if constexpr (FA_MMA_BATCH != 0) {
+                // four K steps (one 64-column box) per election
+                const uint32_t hi = ptx::sdesc_sw128_hi(1024);
+                const uint32_t qlo = ptx::sdesc_sw128_lo(sbase + WideSmem::kOffQ, 16);
+                const uint32_t klo = ptx::sdesc_sw128_lo(slot0, 16);
 #pragma unroll
-            for (int kk = 0; kk < kWideD / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-                ptx::mma_ss_warp(d, qd + (off >> 4), kd + (off >> 4), kIdescQK, kk > 0);
+                for (int c = 0; c < kWideAtoms; ++c)
+                    ptx::mma_ss_x4_lo(d, qlo + c * (kBM * 128 / 16), klo + c * (kBN * 128 / 16), hi, 2u,
+                                      kIdescQK, c > 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < kWideD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                    ptx::mma_ss_warp(d, qd + (off >> 4), kd + (off >> 4), kIdescQK, kk > 0);
+                }
             }
             ptx::tc_commit_warp(bar(&bars->s_full[i & 1]));
             ptx::tc_commit_warp(bar(&bars->kv_empty[0]));
@@ -220,10 +231,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             if (!(ok = wait_warp(bar(&bars->kv_full[1]), par))) break;
             ptx::tc_fence_after_sync();
             const uint32_t pa = tmem + ((j & 1) ? kWideS1 : 0u);
+            if constexpr (FA_MMA_BATCH != 0) {
+                const uint32_t hi = ptx::sdesc_sw128_hi(1024);
+                const uint32_t vlo = ptx::sdesc_sw128_lo(slot0 + kWideTileBytes, kBN * 128);
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-                ptx::mma_ts_warp(tmem + kBN, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), kIdescPV,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kBN / 16; kk += 4)
+                    ptx::mma_ts_x4_lo(tmem + kBN, pa + kk * 8, vlo + kk * (16 * 128 / 16), hi, 8u,
+                                      16u * 128u / 16u, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    ptx::mma_ts_warp(tmem + kBN, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), kIdescPV,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
+            }
             ptx::tc_commit_warp(bar(&bars->kv_empty[1]));
             ptx::tc_commit_warp(bar(&bars->o_done));
             if (j + 1 == n_tiles) ptx::tc_commit_warp(bar(&bars->o_last));

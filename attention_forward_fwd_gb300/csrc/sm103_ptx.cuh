@@ -312,6 +312,52 @@ __device__ __forceinline__ void mma_ts_warp_lo(uint32_t d_tmem, uint32_t a_tmem,
         : "memory");
 }
 
+// Four K=16 steps issued under one elect.sync (the per-instruction election
+// and predicate set-up are paid once).  SS form: both descriptors (low words
+// over the shared high word) advance by `step` 16-byte units per K step, the
+// first step accumulates iff `acc_first`, the others always.
+__device__ __forceinline__ void mma_ss_x4_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                             uint32_t step, uint32_t idesc, uint32_t acc_first) {
+    asm volatile(
+        "{\n\t.reg .pred E, P1, T;\n\t.reg .b64 DA, DB;\n\t.reg .b32 A1, B1;\n\t"
+        "setp.ne.b32 P1, %6, 0;\n\tsetp.eq.b32 T, %6, %6;\n\t"
+        "elect.sync _|E, 0xffffffff;\n\t"
+        "mov.b64 DA, {%1, %3};\n\tmov.b64 DB, {%2, %3};\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %4, P1;\n\t"
+        "add.u32 A1, %1, %5;\n\tadd.u32 B1, %2, %5;\n\t"
+        "mov.b64 DA, {A1, %3};\n\tmov.b64 DB, {B1, %3};\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %4, T;\n\t"
+        "add.u32 A1, A1, %5;\n\tadd.u32 B1, B1, %5;\n\t"
+        "mov.b64 DA, {A1, %3};\n\tmov.b64 DB, {B1, %3};\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %4, T;\n\t"
+        "add.u32 A1, A1, %5;\n\tadd.u32 B1, B1, %5;\n\t"
+        "mov.b64 DA, {A1, %3};\n\tmov.b64 DB, {B1, %3};\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %4, T;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(step), "r"(acc_first)
+        : "memory");
+}
+
+// TS form of the same: A from tensor memory advancing by `a_step` columns,
+// B's descriptor low word by `b_step` 16-byte units per K step.
+__device__ __forceinline__ void mma_ts_x4_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                             uint32_t a_step, uint32_t b_step, uint32_t idesc,
+                                             uint32_t acc_first) {
+    asm volatile(
+        "{\n\t.reg .pred E, P1, T;\n\t.reg .b64 DB;\n\t.reg .b32 A1, B1;\n\t"
+        "setp.ne.b32 P1, %7, 0;\n\tsetp.eq.b32 T, %7, %7;\n\t"
+        "elect.sync _|E, 0xffffffff;\n\t"
+        "mov.b64 DB, {%2, %3};\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], DB, %4, P1;\n\t"
+        "add.u32 A1, %1, %5;\n\tadd.u32 B1, %2, %6;\n\tmov.b64 DB, {B1, %3};\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], [A1], DB, %4, T;\n\t"
+        "add.u32 A1, A1, %5;\n\tadd.u32 B1, B1, %6;\n\tmov.b64 DB, {B1, %3};\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], [A1], DB, %4, T;\n\t"
+        "add.u32 A1, A1, %5;\n\tadd.u32 B1, B1, %6;\n\tmov.b64 DB, {B1, %3};\n\t"
+        "@E tcgen05.mma.cta_group::1.kind::f16 [%0], [A1], DB, %4, T;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(a_step), "r"(b_step), "r"(acc_first)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
