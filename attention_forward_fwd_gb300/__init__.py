@@ -15,7 +15,7 @@ from .build import LIB_PATH, build  # noqa: F401
 
 __all__ = ["fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
            "fa_device_status", "fa_last_device_status", "attention_forward",
-           "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_launches",
+           "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_launches", "fa_split_plan",
            "fa_fwd_gqa", "fa_fwd_gqa_splitkv", "fa_fwd_varlen", "attention_forward_varlen",
            "fa_fwd_local", "fa_fwd_dropout",
            "FaError", "library", "EXPORTED_SYMBOLS", "FA_F16", "FA_BF16"]
@@ -27,7 +27,8 @@ FA_F16, FA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
                     "fa_device_status", "fa_last_device_status", "fa_splitkv_workspace_size",
                     "fa_splitkv_launches", "fa_fwd_splitkv", "fa_fwd_gqa", "fa_fwd_gqa_splitkv",
-                    "fa_fwd_varlen", "fa_fwd_local", "fa_selftest_timeout", "fa_fwd_dropout")
+                    "fa_fwd_varlen", "fa_fwd_local", "fa_selftest_timeout", "fa_fwd_dropout",
+                    "fa_split_plan")
 
 _LIB = None
 
@@ -63,6 +64,8 @@ def library() -> ctypes.CDLL:
         lib.fa_splitkv_workspace_size.restype = i
         lib.fa_splitkv_launches.argtypes = [i, i, i, i, i]
         lib.fa_splitkv_launches.restype = i
+        lib.fa_split_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(i), i, ctypes.POINTER(i)]
+        lib.fa_split_plan.restype = i
         lib.fa_fwd_splitkv.argtypes = sig + [i, vp, ctypes.c_size_t, vp]
         lib.fa_fwd_splitkv.restype = i
         gsig = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i]   # ..., B, H, H_kv, S, D, causal, scale, dtype
@@ -129,6 +132,19 @@ def fa_splitkv_workspace_size(B, H, S, D, causal) -> int:
 
 def fa_splitkv_launches(B, H, S, D, causal) -> int:
     return int(library().fa_splitkv_launches(int(B), int(H), int(S), int(D), int(bool(causal))))
+
+
+def fa_split_plan(B, H, S, D, causal, sms):
+    """(splits of each 256-row query block, work items per head) of the split
+    plan for this shape on a GPU with `sms` SMs (host only, no CUDA call)."""
+    nqb = (int(S) + 255) // 256
+    arr = (ctypes.c_int * max(nqb, 1))()
+    items = ctypes.c_int(0)
+    rc = library().fa_split_plan(int(B), int(H), int(S), int(D), int(bool(causal)), int(sms), arr,
+                                 nqb, ctypes.byref(items))
+    if rc < 1:
+        raise FaError(rc, "fa_split_plan")
+    return list(arr[:nqb]), items.value
 
 
 def fa_fwd_splitkv(Q, K, V, O, LSE, B, H, S, D, causal, scale, dtype, workspace,

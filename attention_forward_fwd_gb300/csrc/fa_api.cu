@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "fa_fwd_kernel.cuh"
 #include "fa_fwd_wide.cuh"
@@ -104,12 +105,23 @@ static_assert(sizeof(fa::FwdParams) + 4 * sizeof(CUtensorMap) <= 4096, "kernel p
 bool supported_dim(int D) { return D >= 8 && D <= fa::kWideD && D % 8 == 0; }
 int kernel_dim(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : fa::kWideD; }
 
-// How the keys of each query block are split over CTAs.
+// How the keys of each query block are split over CTAs: the splits of every
+// query block and the work items of one head in the order the kernel visits
+// them (the same for every head).
 struct SplitPlan {
-    int chunk = 0;          // key tiles per split (0: no split)
-    int max_splits = 1;     // splits of the longest query block
+    int chunk = 0;          // nonzero: split mode
+    int max_splits = 1;     // splits of the most split query block
     int ctas_per_head = 0;  // work items per head
+    uint8_t ns[fa::kMaxSplitBlocks] = {};       // splits of each query block
+    uint32_t item[fa::kMaxSplitItems] = {};     // (block, split, splits) per item
 };
+
+SplitPlan no_split(int S) {
+    SplitPlan plan;
+    plan.ctas_per_head = (S + fa::kQTiles * fa::kBM - 1) / (fa::kQTiles * fa::kBM);
+    std::fill(plan.ns, plan.ns + fa::kMaxSplitBlocks, uint8_t{1});
+    return plan;
+}
 
 long long ctas_per_head_for(int S, bool causal, int chunk) {
     const int nqb = (S + fa::kQTiles * fa::kBM - 1) / (fa::kQTiles * fa::kBM);
@@ -118,35 +130,159 @@ long long ctas_per_head_for(int S, bool causal, int chunk) {
     return n;
 }
 
-// Split the keys only when one CTA per query block leaves most of the SMs
-// idle; then take the smallest chunk (>= 2 key tiles) whose grid still fits in
-// one wave of `sms` CTAs.
-SplitPlan plan_split(int B, int H, int S, int D, bool causal, int sms) {
-    SplitPlan plan;
-    if (kernel_dim(D) > 128) return plan;   // the wide kernel does not split
+// Fills the item list of a plan from its per-block splits: items longest
+// first (each split's key tiles), the splits of a block together, ties in
+// the unsplit order (heaviest query block first when causal).  Returns false
+// if the head has too many items for the kernel's table.
+bool order_items(SplitPlan& plan, int S, bool causal) {
+    const int nqb = (S + fa::kQTiles * fa::kBM - 1) / (fa::kQTiles * fa::kBM);
+    struct Piece { int len, visit, qb, split, n; };
+    Piece pieces[fa::kMaxSplitItems];
+    int np = 0;
+    plan.max_splits = 1;
+    for (int v = 0; v < nqb; ++v) {
+        const int qb = causal ? nqb - 1 - v : v;
+        const int T = fa::key_tiles_for_block(qb, S, causal);
+        const int n = std::max(1, static_cast<int>(plan.ns[qb]));
+        const int c = (T + n - 1) / n;
+        plan.max_splits = std::max(plan.max_splits, n);
+        for (int sp = 0; sp < n; ++sp) {
+            if (np == fa::kMaxSplitItems) return false;
+            pieces[np++] = Piece{std::min(T, (sp + 1) * c) - sp * c, v, qb, sp, n};
+        }
+    }
+    std::stable_sort(pieces, pieces + np, [](const Piece& a, const Piece& b) { return a.len > b.len; });
+    for (int y = 0; y < np; ++y)
+        plan.item[y] = static_cast<uint32_t>(pieces[y].qb) | (static_cast<uint32_t>(pieces[y].split) << 8) |
+                       (static_cast<uint32_t>(pieces[y].n) << 20);
+    plan.ctas_per_head = np;
+    return true;
+}
+
+// Makespan, in key-tile steps, of the kernel's static schedule (item w of
+// round k goes to CTA w mod G, every other round in reverse; items are
+// numbered y * BH + bh) when every item costs its key tiles plus `per_item`,
+// plus `merge` when some block is split.
+double simulate_plan(const SplitPlan& plan, int S, bool causal, long long bh, int sms, double per_item,
+                     double merge) {
+    int len[fa::kMaxSplitItems];
+    bool split = false;
+    for (int y = 0; y < plan.ctas_per_head; ++y) {
+        const uint32_t e = plan.item[y];
+        const int qb = static_cast<int>(e & 0xffu), sp = static_cast<int>((e >> 8) & 0xfffu);
+        const int n = std::max(1, static_cast<int>(e >> 20));
+        const int T = fa::key_tiles_for_block(qb, S, causal);
+        const int c = (T + n - 1) / n;
+        len[y] = std::min(T, (sp + 1) * c) - sp * c;
+        split = split || n > 1;
+    }
+    const long long items = bh * plan.ctas_per_head;
+    const long long G = std::min<long long>(items, sms);
+    std::vector<double> load(static_cast<size_t>(G), 0.0);
+    for (long long w = 0; w < items; ++w) {
+        const long long k = w / G, c = w % G;
+        load[static_cast<size_t>((k & 1) ? G - 1 - c : c)] += len[w / bh] + per_item;
+    }
+    return *std::max_element(load.begin(), load.end()) + (split ? merge : 0.0);
+}
+
+// Split the keys only when one CTA per query block leaves SMs idle:
+// * less than three quarters of a wave: the smallest uniform chunk (>= 2
+//   key tiles) whose grid still fits in one wave of `sms` CTAs;
+// * one to four waves with a ragged last one: the per-block splits whose
+//   simulated schedule (simulate_plan) is shortest, if it beats the unsplit
+//   schedule by 8 % or more.  Candidates split every block above a key-tile
+//   cap, or the m lightest or heaviest blocks into 2-4 pieces (only with
+//   `multiwave`).
+SplitPlan plan_split_uncached(int B, int H, int S, int D, bool causal, int sms, bool multiwave) {
+    SplitPlan plan = no_split(S);
+    if (kernel_dim(D) > 128 || sms <= 0) return plan;   // the wide kernel does not split
     const int rows_per_cta = fa::kQTiles * fa::kBM;
     const int nqb = (S + rows_per_cta - 1) / rows_per_cta;
     const int nkv_all = (S + fa::kBN - 1) / fa::kBN;
-    plan.ctas_per_head = nqb;
-    const long long base = static_cast<long long>(B) * H * nqb;
-    if (sms <= 0 || base * 4 >= static_cast<long long>(sms) * 3 || nkv_all <= 2 ||
-        nqb > fa::kMaxSplitBlocks)
-        return plan;
-    int lo = 2, hi = nkv_all;   // grid size is non-increasing in the chunk
-    if (static_cast<long long>(B) * H * ctas_per_head_for(S, causal, hi) > sms) return plan;
-    while (lo < hi) {
-        const int mid = (lo + hi) / 2;
-        if (static_cast<long long>(B) * H * ctas_per_head_for(S, causal, mid) <= sms) hi = mid;
-        else lo = mid + 1;
+    const long long bh = static_cast<long long>(B) * H;
+    const long long base = bh * nqb;
+    if (nkv_all <= 2 || nqb > fa::kMaxSplitBlocks) return plan;
+    int T[fa::kMaxSplitBlocks];
+    for (int qb = 0; qb < nqb; ++qb) T[qb] = fa::key_tiles_for_block(qb, S, causal);
+    auto with_splits = [&](auto ns_of) {
+        SplitPlan cand;
+        cand.chunk = 1;
+        for (int qb = 0; qb < nqb; ++qb)
+            cand.ns[qb] = static_cast<uint8_t>(std::max(1, std::min({ns_of(qb), T[qb], 255})));
+        if (!order_items(cand, S, causal)) cand.chunk = 0;
+        return cand;
+    };
+    if (base * 4 < static_cast<long long>(sms) * 3) {
+        int lo = 2, hi = nkv_all;   // grid size is non-increasing in the chunk
+        if (bh * ctas_per_head_for(S, causal, hi) > sms) return plan;
+        while (lo < hi) {
+            const int mid = (lo + hi) / 2;
+            if (bh * ctas_per_head_for(S, causal, mid) <= sms) hi = mid;
+            else lo = mid + 1;
+        }
+        if ((nkv_all + lo - 1) / lo <= 1) return plan;
+        SplitPlan cand = with_splits([&](int qb) { return (T[qb] + lo - 1) / lo; });
+        return cand.chunk ? cand : plan;
     }
-    const int max_splits = (nkv_all + lo - 1) / lo;
-    if (max_splits <= 1 || ctas_per_head_for(S, causal, lo) > fa::kMaxSplitItems) return plan;
-    plan.chunk = lo;
-    plan.max_splits = max_splits;
-    plan.ctas_per_head = static_cast<int>(ctas_per_head_for(S, causal, lo));
-    return plan;
+    if (!multiwave || base <= sms || base > 4LL * sms) return plan;
+    // cost of an item beyond its key tiles and of the merge, in key steps
+    // (measured: the D = 64 key step is about half as long as the D = 128 one)
+    const double per_item = kernel_dim(D) == 64 ? 1.5 : 1.0;
+    const double merge = kernel_dim(D) == 64 ? 3.0 : 1.5;
+    if (!order_items(plan, S, causal)) return no_split(S);
+    const double t0 = simulate_plan(plan, S, causal, bh, sms, per_item, merge);
+    SplitPlan best = plan;
+    double t_best = t0;
+    auto consider = [&](const SplitPlan& cand) {
+        if (!cand.chunk || cand.max_splits <= 1) return;
+        const double t = simulate_plan(cand, S, causal, bh, sms, per_item, merge);
+        if (t < t_best) {
+            t_best = t;
+            best = cand;
+        }
+    };
+    int tmax = 0;
+    for (int qb = 0; qb < nqb; ++qb) tmax = std::max(tmax, T[qb]);
+    for (int cap = 1; cap < tmax; ++cap) consider(with_splits([&](int qb) { return (T[qb] + cap - 1) / cap; }));
+    int by_len[fa::kMaxSplitBlocks];   // blocks lightest first
+    for (int qb = 0; qb < nqb; ++qb) by_len[qb] = qb;
+    std::stable_sort(by_len, by_len + nqb, [&](int a, int b) { return T[a] < T[b]; });
+    for (int m = 1; m < nqb; ++m) {
+        for (int n = 2; n <= 4; ++n) {
+            bool light[fa::kMaxSplitBlocks] = {};
+            for (int i = 0; i < m; ++i) light[by_len[i]] = true;
+            consider(with_splits([&](int qb) { return light[qb] ? n : 1; }));
+            consider(with_splits([&](int qb) { return light[qb] ? 1 : n; }));
+        }
+    }
+    if (t_best > 0.92 * t0) return no_split(S);
+    return best;
 }
 
+// Plans are cached per shape (host threads may call concurrently).
+SplitPlan plan_split(int B, int H, int S, int D, bool causal, int sms, bool multiwave = true) {
+    struct Entry { int B, H, S, kd, causal, sms; bool multiwave; SplitPlan plan; };
+    static std::mutex mu;
+    static Entry cache[32];
+    static int used = 0, next = 0;
+    const int kd = kernel_dim(D);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i) {
+            const Entry& e = cache[i];
+            if (e.B == B && e.H == H && e.S == S && e.kd == kd && e.causal == int(causal) && e.sms == sms &&
+                e.multiwave == multiwave)
+                return e.plan;
+        }
+    }
+    const SplitPlan plan = plan_split_uncached(B, H, S, D, causal, sms, multiwave);
+    std::lock_guard<std::mutex> lock(mu);
+    cache[next] = Entry{B, H, S, kd, int(causal), sms, multiwave, plan};
+    next = (next + 1) % 32;
+    used = std::max(used, next == 0 ? 32 : next);
+    return plan;
+}
 
 size_t workspace_bytes_for(const SplitPlan& plan, int B, int H, int S, int D_head) {
     if (plan.chunk == 0) return 0;
@@ -223,16 +359,8 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.ws_o = plan.chunk ? static_cast<float*>(workspace) : nullptr;
     p.ws_ml = plan.chunk ? static_cast<float*>(workspace) + o_floats : nullptr;
     if (plan.chunk) {
-        // (visit index, split, splits) of each item of a head, in visit order
-        const bool c = causal != 0;
-        int y = 0;
-        for (int i = 0; i < p.nqb; ++i) {
-            const int qb = c ? (p.nqb - 1 - i) : i;
-            const int ns = (fa::key_tiles_for_block(qb, S, c) + plan.chunk - 1) / plan.chunk;
-            for (int sp = 0; sp < ns; ++sp, ++y)
-                p.split_item[y] = static_cast<uint32_t>(i) | (static_cast<uint32_t>(sp) << 8) |
-                                  (static_cast<uint32_t>(ns) << 20);
-        }
+        std::copy(plan.item, plan.item + plan.ctas_per_head, p.split_item);
+        std::copy(plan.ns, plan.ns + fa::kMaxSplitBlocks, p.block_splits);
     }
     // one CTA per SM, each running its share of the work items (at most one
     // CTA per item)
@@ -458,6 +586,18 @@ int fa_splitkv_launches(int B, int H, int S, int D, int causal) {
     return plan_split(B, H, S, D, causal != 0, num_sms()).chunk ? 2 : 1;
 }
 
+int fa_split_plan(int B, int H, int S, int D, int causal, int sms, int* splits, int max_blocks,
+                  int* items_per_head) {
+    if (B < 1 || H < 1 || S < 1 || D < 1 || sms < 1 || (splits == nullptr && max_blocks > 0))
+        return FA_ERR_INVALID_ARG;
+    const SplitPlan plan = plan_split(B, H, S, D, causal != 0, sms);
+    const int nqb = (S + fa::kQTiles * fa::kBM - 1) / (fa::kQTiles * fa::kBM);
+    for (int qb = 0; qb < std::min(nqb, max_blocks); ++qb)
+        splits[qb] = plan.chunk && qb < fa::kMaxSplitBlocks ? plan.ns[qb] : 1;
+    if (items_per_head != nullptr) *items_per_head = plan.ctas_per_head;
+    return plan.chunk ? plan.max_splits : 1;
+}
+
 int fa_fwd_gqa_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
                        int H, int H_kv, int S, int D, int causal, float scale, int dtype,
                        void* workspace, size_t workspace_bytes, fa_stream_t stream) {
@@ -590,7 +730,9 @@ extern "C" int fa_fwd_splitkv_static(const void* Q, const void* K, const void* V
     if (v != FA_OK) return v;
     const int sms = num_sms();
     if (sms <= 0) return FA_ERR_CUDA;
-    const SplitPlan plan = plan_split(B, H, S, D, causal != 0, sms);
+    // the one-wave plans only: the multi-wave ones need more scratch than the
+    // array holds for the shapes they serve
+    const SplitPlan plan = plan_split(B, H, S, D, causal != 0, sms, false);
     const size_t need = workspace_bytes_for(plan, B, H, S, D);
     if (need > kStaticWorkspaceBytes) return FA_ERR_UNSUPPORTED;
     // looked up on every call (free after the first), so that the first call

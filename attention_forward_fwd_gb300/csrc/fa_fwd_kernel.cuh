@@ -145,22 +145,23 @@ struct FwdParams {
     int items;
     float scale_log2;   // scale * log2(e)
     float* lse;         // [B, H, S] fp32 or nullptr
-    // Split over keys (0 = off).  With kv_chunk > 0 the CTAs of one head are
-    // the (query block, split) pairs, heaviest blocks first when causal; split
-    // s of a query block covers key tiles [s*kv_chunk, (s+1)*kv_chunk).  A
-    // block with more than one split writes partial results (see
-    // PartialLayout) that fa_combine_kernel merges.
+    // Split over keys (kv_chunk = 0: off).  In split mode the work items of a
+    // head are (query block, split) pairs in the order of split_item; query
+    // block qb with T key tiles and n splits gives split s the key tiles
+    // [s*c, min(T, (s+1)*c)), c = ceil(T / n).  A block with more than one
+    // split writes partial results (see partial_slot) that fa_combine_kernel
+    // merges.
     int nqb;            // query blocks of kQTiles*kBM rows per head
-    int kv_chunk;       // key tiles per split, 0 = no split
-    int max_splits;     // splits of the longest query block
+    int kv_chunk;       // nonzero: split mode
+    int max_splits;     // splits of the most split query block
     float* ws_o;        // partial o~ tiles (fp32)
     float* ws_ml;       // partial (m * scale * log2e, l) per row
     // split mode: item y of a head is split (split_item[y] >> 8) & 0xfff of
-    // the (split_item[y] & 0xff)-th query block visited (heaviest first when
-    // causal), which has split_item[y] >> 20 splits.  One table entry per
-    // item: the decode takes one load, not a search (a chain of dependent
-    // parameter loads is slow right after launch).
+    // query block split_item[y] & 0xff, which has split_item[y] >> 20 splits.
+    // One table entry per item: the decode takes one load, not a search (a
+    // chain of dependent parameter loads is slow right after launch).
     uint32_t split_item[kMaxSplitItems];
+    uint8_t block_splits[kMaxSplitBlocks];   // splits of each query block
 };
 
 // Workspace of the split-over-keys path.  One partial slot per (b*H + h,
@@ -333,12 +334,12 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
         it.split = 0;
     } else {
         const uint32_t e = p.split_item[y];
-        const int lo = static_cast<int>(e & 0xffu);
-        qb = causal ? (p.nqb - 1 - lo) : lo;
+        qb = static_cast<int>(e & 0xffu);
         nsplit = static_cast<int>(e >> 20);
         it.split = static_cast<int>((e >> 8) & 0xfffu);
-        it.jb = it.split * p.kv_chunk;
-        je = it.jb + p.kv_chunk;
+        const int chunk = (key_tiles_for_block(qb, it.S, causal) + nsplit - 1) / nsplit;
+        it.jb = it.split * chunk;
+        je = it.jb + chunk;
     }
     it.q0 = qb * (kQTiles * kBM);
     it.nkv0 = max(0, min(je, key_tiles_for(it.q0, it.S, causal)) - it.jb);
@@ -1408,8 +1409,7 @@ __global__ void __launch_bounds__(kCombineThreads) fa_combine_kernel(const FwdPa
     constexpr int kPerTile = kBM / kRows;               // CTAs per query tile
     const int qt = blockIdx.x / kPerTile;
     const int bh = blockIdx.y;
-    const bool causal = p.causal != 0;
-    const int ns = (key_tiles_for_block(qt / kQTiles, p.S, causal) + p.kv_chunk - 1) / p.kv_chunk;
+    const int ns = p.block_splits[qt / kQTiles];
     // the next kernel in the stream may start its set-up now (it waits for
     // this grid before touching memory)
     ptx::launch_dependents();

@@ -106,13 +106,15 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
 
 /*
  * Split over keys (for shapes whose B * H * ceil(S / 256) query blocks leave
- * most SMs idle).  The keys of each query block are divided among several
- * CTAs; each writes a partial result (unnormalised fp32 output rows, the row
- * max and the row sum) to `workspace`, and a second kernel, launched on the
- * same stream as a programmatic dependent of the first, merges them with the
- * same exp(m_old - m_new) rescaling that the online softmax uses across key
- * tiles (page "CuTe 详解：以 FlashAttention-2 拆解 Layout、TiledCopy 与 TiledMMA",
- * section 沿 C fragment 做 Online Softmax).
+ * SMs idle: less than three quarters of a wave, or one to four waves with a
+ * ragged last one).  The keys of some or all query blocks are divided among
+ * several CTAs; each writes a partial result (unnormalised fp32 output rows,
+ * the row max and the row sum) to `workspace`, and a second kernel, launched
+ * on the same stream as a programmatic dependent of the first, merges them
+ * with the same exp(m_old - m_new) rescaling that the online softmax uses
+ * across key tiles (page "CuTe 详解：以 FlashAttention-2 拆解 Layout、TiledCopy
+ * 与 TiledMMA", section 沿 C fragment 做 Online Softmax).  Which blocks are
+ * split, and how many ways, is fixed per shape (fa_split_plan).
  *
  * fa_splitkv_workspace_size: bytes of device workspace fa_fwd_splitkv needs
  * for this shape on the current device (0 when the shape is not split).
@@ -126,6 +128,19 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
  */
 int fa_splitkv_workspace_size(int B, int H, int S, int D, int causal, size_t* bytes);
 int fa_splitkv_launches(int B, int H, int S, int D, int causal);
+
+/*
+ * The split plan fa_fwd_splitkv uses for a shape on a GPU with `sms` SMs
+ * (host only; no CUDA call).  splits[qb] receives the number of CTAs that
+ * share the keys of query block qb (256 query rows; blocks 0 .. nblocks-1,
+ * nblocks = ceil(S / 256)), for qb < min(nblocks, max_blocks); *items_per_head
+ * (may be NULL) the work items of one head.  Returns the largest entry
+ * (1 = not split), or FA_ERR_INVALID_ARG for sizes below 1 or a NULL
+ * `splits` with max_blocks > 0.  Not part of the attention computation; the
+ * pages have no counterpart.
+ */
+int fa_split_plan(int B, int H, int S, int D, int causal, int sms, int* splits, int max_blocks,
+                  int* items_per_head);
 int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
                    int B, int H, int S, int D, int causal, float scale, int dtype,
                    void* workspace, size_t workspace_bytes, fa_stream_t stream);

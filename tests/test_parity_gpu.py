@@ -105,6 +105,23 @@ def test_split_kv_path_is_taken_and_exact(S, D, dtype, causal):
     _full_case(1, 1, S, D, dtype, "stress", 30 + S, causal, split_kv=True)
 
 
+@pytest.mark.parametrize("B,H,S,D,dtype,dist", [(1, 40, 1000, 64, "f16", "normal"),
+                                                  (1, 40, 900, 128, "bf16", "stress"),
+                                                  (3, 8, 1999, 64, "f16", "stress")])
+def test_multiwave_split_is_taken_and_exact(B, H, S, D, dtype, dist):
+    """One to two waves of query blocks with a ragged last one: some blocks
+    are split over CTAs (the plan the host simulation picks), the rest run
+    whole in the same launch, and the merge leaves the unsplit blocks alone;
+    every element matches the oracle."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    splits, items = fa.fa_split_plan(B, H, S, D, False, sms)
+    assert max(splits) > 1 and min(splits) == 1 and B * H * items > sms
+    assert _splits(B, H, S, D, False)
+    _full_case(B, H, S, D, dtype, dist, 40 + S, False, split_kv=True)
+
+
 def test_split_kv_workspace_checks():
     import torch
     import attention_forward_fwd_gb300 as fa
