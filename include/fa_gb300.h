@@ -257,8 +257,13 @@ int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* L
  * The scratch is one device array inside this library, 24 MiB (25,165,824
  * bytes), reserved on every GPU that loads the library until the process
  * exits.  This call allocates nothing and calls no allocating routine.
- *   - A shape whose split needs more than 24 MiB (fa_splitkv_workspace_size)
- *     is rejected with FA_ERR_UNSUPPORTED before anything is launched; shapes
+ *   - It splits only the shapes whose query blocks fill less than three
+ *     quarters of a wave (the one-wave plans); shapes that fa_fwd_splitkv
+ *     would split over several waves run unsplit here, with the same result.
+ *   - A shape whose one-wave split needs more than 24 MiB (what
+ *     fa_splitkv_workspace_size reports for it, since such shapes are never
+ *     multi-wave) is rejected with FA_ERR_UNSUPPORTED before anything is
+ *     launched; shapes
  *     that are not split need no scratch and always run.  On a 152-SM GB300
  *     every split of D <= 64, and of D <= 128 without the causal mask, fits
  *     (at most about 20 MiB); the longest causal splits of 64 < D <= 128 (up
