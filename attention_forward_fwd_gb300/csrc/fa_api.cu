@@ -179,9 +179,16 @@ double simulate_plan(const SplitPlan& plan, int S, bool causal, long long bh, in
     const long long items = bh * plan.ctas_per_head;
     const long long G = std::min<long long>(items, sms);
     std::vector<double> load(static_cast<size_t>(G), 0.0);
-    for (long long w = 0; w < items; ++w) {
-        const long long k = w / G, c = w % G;
-        load[static_cast<size_t>((k & 1) ? G - 1 - c : c)] += len[w / bh] + per_item;
+    long long c = 0, k = 0;   // item w = y * bh + i goes to round k = w / G, slot c = w % G
+    for (int y = 0; y < plan.ctas_per_head; ++y) {
+        const double cost = len[y] + per_item;
+        for (long long i = 0; i < bh; ++i) {
+            load[static_cast<size_t>((k & 1) ? G - 1 - c : c)] += cost;
+            if (++c == G) {
+                c = 0;
+                ++k;
+            }
+        }
     }
     return *std::max_element(load.begin(), load.end()) + (split ? merge : 0.0);
 }
@@ -192,8 +199,9 @@ double simulate_plan(const SplitPlan& plan, int S, bool causal, long long bh, in
 // * one to four waves with a ragged last one: the per-block splits whose
 //   simulated schedule (simulate_plan) is shortest, if it beats the unsplit
 //   schedule by 8 % or more.  Candidates split every block above a key-tile
-//   cap, or the m lightest or heaviest blocks into 2-4 pieces (only with
-//   `multiwave`).
+//   cap, or the m lightest or heaviest blocks into 2-4 pieces (m on a grid
+//   of at most ~16 values; only with `multiwave`).  Planned once per shape
+//   (cached below): at most ~2 ms of host time for the largest shapes.
 SplitPlan plan_split_uncached(int B, int H, int S, int D, bool causal, int sms, bool multiwave) {
     SplitPlan plan = no_split(S);
     if (kernel_dim(D) > 128 || sms <= 0) return plan;   // the wide kernel does not split
@@ -234,8 +242,14 @@ SplitPlan plan_split_uncached(int B, int H, int S, int D, bool causal, int sms, 
     const double t0 = simulate_plan(plan, S, causal, bh, sms, per_item, merge);
     SplitPlan best = plan;
     double t_best = t0;
+    // candidates that cannot beat the best so far (their work spread evenly
+    // over the CTAs already takes longer) are not simulated
     auto consider = [&](const SplitPlan& cand) {
         if (!cand.chunk || cand.max_splits <= 1) return;
+        double work = 0.0;
+        for (int qb = 0; qb < nqb; ++qb) work += T[qb] + per_item * cand.ns[qb];
+        const long long items = bh * cand.ctas_per_head;
+        if (work * bh / static_cast<double>(std::min<long long>(items, sms)) + merge >= t_best) return;
         const double t = simulate_plan(cand, S, causal, bh, sms, per_item, merge);
         if (t < t_best) {
             t_best = t;
@@ -244,11 +258,19 @@ SplitPlan plan_split_uncached(int B, int H, int S, int D, bool causal, int sms, 
     };
     int tmax = 0;
     for (int qb = 0; qb < nqb; ++qb) tmax = std::max(tmax, T[qb]);
-    for (int cap = 1; cap < tmax; ++cap) consider(with_splits([&](int qb) { return (T[qb] + cap - 1) / cap; }));
+    int prev_ns0 = -1, prev_nsl = -1;   // (caps that split like the previous one are skipped)
+    for (int cap = 1; cap < tmax; ++cap) {
+        const int ns0 = (T[0] + cap - 1) / cap, nsl = (T[nqb - 1] + cap - 1) / cap;
+        if (ns0 == prev_ns0 && nsl == prev_nsl && T[0] == T[nqb - 1]) continue;
+        prev_ns0 = ns0;
+        prev_nsl = nsl;
+        consider(with_splits([&](int qb) { return (T[qb] + cap - 1) / cap; }));
+    }
     int by_len[fa::kMaxSplitBlocks];   // blocks lightest first
     for (int qb = 0; qb < nqb; ++qb) by_len[qb] = qb;
     std::stable_sort(by_len, by_len + nqb, [&](int a, int b) { return T[a] < T[b]; });
-    for (int m = 1; m < nqb; ++m) {
+    const int m_step = std::max(1, (nqb - 1) / 16);   // at most ~16 block counts
+    for (int m = 1; m < nqb; m += m_step) {
         for (int n = 2; n <= 4; ++n) {
             bool light[fa::kMaxSplitBlocks] = {};
             for (int i = 0; i < m; ++i) light[by_len[i]] = true;
