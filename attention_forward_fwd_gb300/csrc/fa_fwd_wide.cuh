@@ -38,10 +38,20 @@ constexpr uint32_t kWideS1 = 384;         // column of the second S/P buffer
 constexpr long long kWideL2Share = 16ll << 20;
 constexpr long long kWideL2ShareCausal = 32ll << 20;
 
+// K tiles are loaded and released one 64-column box at a time: box c of
+// K(j+1) is loaded as soon as the four K steps of S(j) that read box c of
+// K(j) have run, so the load overlaps the rest of S(j) (1: on; 0: the whole
+// tile at once).
+#ifndef FA_WIDE_KBOX
+#define FA_WIDE_KBOX 1
+#endif
+
 struct WideBars {
     uint64_t q_full;
-    uint64_t kv_full[2];    // slot 0: K(j), slot 1: V(j)
+    uint64_t kv_full[2];    // slot 0: K(j) (whole-tile mode), slot 1: V(j)
     uint64_t kv_empty[2];
+    uint64_t kbox_full[kWideAtoms];    // per-box mode: box c of K(j) landed
+    uint64_t kbox_empty[kWideAtoms];   // ... and read by S(j)
     uint64_t s_full[2];     // S(j) complete in buffer j % 2 (and every MMA before it)
     // P(j) stored in buffer j % 2 by the 128 softmax threads.  One barrier
     // per buffer: S(j+1) is issued before the MMA warp waits for P(j), so the
@@ -114,6 +124,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             ptx::mbar_init(bar(&bars->kv_full[s]), 1);
             ptx::mbar_init(bar(&bars->kv_empty[s]), 1);
         }
+        for (int c = 0; c < kWideAtoms; ++c) {
+            ptx::mbar_init(bar(&bars->kbox_full[c]), 1);
+            ptx::mbar_init(bar(&bars->kbox_empty[c]), 1);
+        }
         ptx::mbar_init(bar(&bars->s_full[0]), 1);
         ptx::mbar_init(bar(&bars->s_full[1]), 1);
         ptx::mbar_init(bar(&bars->p_full[0]), kBM);
@@ -160,9 +174,25 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         // empty barrier).
         bool ok = true;
         int nk = 0, nv = 0;   // K / V tiles issued
+        int nkb[kWideAtoms] = {};   // per-box mode: boxes of K issued
         auto load_k = [&](int i) {
-            if (i > 0 && !(ok = wait_warp(bar(&bars->kv_empty[0]), static_cast<uint32_t>((i - 1) & 1)))) return;
-            if (lane == 0) load_tile(&tmK, slot0, bar(&bars->kv_full[0]), hkv, i * kBN);
+            if constexpr (FA_WIDE_KBOX != 0) {
+#pragma unroll 1
+                for (int c = 0; c < kWideAtoms; ++c) {
+                    const uint32_t full = bar(&bars->kbox_full[c]);
+                    if (i > 0 &&
+                        !(ok = wait_warp(bar(&bars->kbox_empty[c]), static_cast<uint32_t>((i - 1) & 1))))
+                        return;
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(full, kWideTileBytes / kWideAtoms);
+                        ptx::tma_load_4d(slot0 + c * (kBN * 128), &tmK, full, c * 64, hkv, i * kBN, b);
+                    }
+                    ++nkb[c];
+                }
+            } else {
+                if (i > 0 && !(ok = wait_warp(bar(&bars->kv_empty[0]), static_cast<uint32_t>((i - 1) & 1)))) return;
+                if (lane == 0) load_tile(&tmK, slot0, bar(&bars->kv_full[0]), hkv, i * kBN);
+            }
             ++nk;
         };
         auto load_v = [&](int i) {
@@ -181,7 +211,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             // let every copy this warp started land before the CTA exits
             // (only the last of each slot can still be in flight)
             wait_warp(bar(&bars->q_full), 0, false);
-            if (nk > 0) wait_warp(bar(&bars->kv_full[0]), static_cast<uint32_t>((nk - 1) & 1), false);
+            if (FA_WIDE_KBOX == 0 && nk > 0)
+                wait_warp(bar(&bars->kv_full[0]), static_cast<uint32_t>((nk - 1) & 1), false);
+            for (int c = 0; c < kWideAtoms; ++c)
+                if (FA_WIDE_KBOX != 0 && nkb[c] > 0)
+                    wait_warp(bar(&bars->kbox_full[c]), static_cast<uint32_t>((nkb[c] - 1) & 1), false);
             if (nv > 0) wait_warp(bar(&bars->kv_full[1]), static_cast<uint32_t>((nv - 1) & 1), false);
         }
     } else if (warp == 4) {
@@ -196,9 +230,26 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         // S(i) into buffer i % 2: Q K(i)^T over the 256 columns, K=16 steps
         // through the four 64-column boxes (32 bytes per step inside a box)
         auto issue_s = [&](int i) {
+            const uint32_t d = tmem + ((i & 1) ? kWideS1 : 0u);
+            if constexpr (FA_WIDE_KBOX != 0) {
+                // box by box: wait for box c of K(i), run its four K steps, and
+                // hand the box back to the producer once they have run
+                const uint32_t hi = ptx::sdesc_sw128_hi(1024);
+                const uint32_t qlo = ptx::sdesc_sw128_lo(sbase + WideSmem::kOffQ, 16);
+                const uint32_t klo = ptx::sdesc_sw128_lo(slot0, 16);
+#pragma unroll
+                for (int c = 0; c < kWideAtoms; ++c) {
+                    if (!(ok = wait_warp(bar(&bars->kbox_full[c]), static_cast<uint32_t>(i & 1)))) return;
+                    ptx::tc_fence_after_sync();
+                    ptx::mma_ss_x4_lo(d, qlo + c * (kBM * 128 / 16), klo + c * (kBN * 128 / 16), hi, 2u,
+                                      kIdescQK, c > 0 ? 1u : 0u);
+                    ptx::tc_commit_warp(bar(&bars->kbox_empty[c]));
+                }
+                ptx::tc_commit_warp(bar(&bars->s_full[i & 1]));
+                return;
+            }
             if (!(ok = wait_warp(bar(&bars->kv_full[0]), static_cast<uint32_t>(i & 1)))) return;
             ptx::tc_fence_after_sync();
-            const uint32_t d = tmem + ((i & 1) ? kWideS1 : 0u);
             if constexpr (FA_MMA_BATCH != 0) {
                 // four K steps (one 64-column box) per election
                 const uint32_t hi = ptx::sdesc_sw128_hi(1024);
