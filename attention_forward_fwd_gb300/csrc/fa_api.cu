@@ -105,6 +105,21 @@ static_assert(sizeof(fa::FwdParams) + 4 * sizeof(CUtensorMap) <= 4096, "kernel p
 bool supported_dim(int D) { return D >= 8 && D <= fa::kWideD && D % 8 == 0; }
 int kernel_dim(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : fa::kWideD; }
 
+// Cost model of the multi-wave split plans (plan_split_uncached), in key
+// steps: an item's cost beyond its key tiles, and the merge's.
+#ifndef FA_PLAN_ITEM_D64
+#define FA_PLAN_ITEM_D64 1.5
+#endif
+#ifndef FA_PLAN_MERGE_D64
+#define FA_PLAN_MERGE_D64 3.0
+#endif
+#ifndef FA_PLAN_ITEM_D128
+#define FA_PLAN_ITEM_D128 1.0
+#endif
+#ifndef FA_PLAN_MERGE_D128
+#define FA_PLAN_MERGE_D128 1.5
+#endif
+
 // How the keys of each query block are split over CTAs: the splits of every
 // query block and the work items of one head in the order the kernel visits
 // them (the same for every head).
@@ -236,8 +251,8 @@ SplitPlan plan_split_uncached(int B, int H, int S, int D, bool causal, int sms, 
     if (!multiwave || base <= sms || base > 4LL * sms) return plan;
     // cost of an item beyond its key tiles and of the merge, in key steps
     // (measured: the D = 64 key step is about half as long as the D = 128 one)
-    const double per_item = kernel_dim(D) == 64 ? 1.5 : 1.0;
-    const double merge = kernel_dim(D) == 64 ? 3.0 : 1.5;
+    const double per_item = kernel_dim(D) == 64 ? FA_PLAN_ITEM_D64 : FA_PLAN_ITEM_D128;
+    const double merge = kernel_dim(D) == 64 ? FA_PLAN_MERGE_D64 : FA_PLAN_MERGE_D128;
     if (!order_items(plan, S, causal)) return no_split(S);
     const double t0 = simulate_plan(plan, S, causal, bh, sms, per_item, merge);
     SplitPlan best = plan;
