@@ -270,31 +270,57 @@ class _Driver:
         self._check(self._wait(stream, ev, 0), "cuStreamWaitEvent")
 
 
+# A head's query rows are taken in blocks of two mirrored chunks (chunk k and
+# chunk n-1-k of n = CPU_CHUNKS), so that under the causal mask every block
+# holds about the same work.
+CPU_CHUNKS = 16
+
+
+def _row_flops(rows: np.ndarray, S: int, D: int, causal: bool) -> float:
+    """Counted FLOPs of query rows `rows` of one head: the workload's
+    convention (4 S^2 D, half when causal) shared out over the rows, in
+    proportion to the keys each row sees; all S rows sum to it exactly."""
+    if causal:
+        return 4.0 * D * S / (S + 1) * float(np.sum(rows + 1))
+    return 4.0 * D * S * len(rows)
+
+
+def _row_blocks(S: int):
+    c = -(-S // CPU_CHUNKS)
+    chunks = [np.arange(a, min(S, a + c)) for a in range(0, S, c)]
+    n = len(chunks)
+    return [np.concatenate([chunks[k], chunks[n - 1 - k]]) if k != n - 1 - k else chunks[k]
+            for k in range((n + 1) // 2)], c
+
+
 def cpu_baseline(w: fa_inputs.Workload, budget_s: float = 15.0, inputs=None):
-    """Time the fp64 oracle on a bounded sample of the workload: whole heads
-    (all rows, every mask mode of the workload) one after another, cycling
-    over the workload's heads, until ``budget_s`` seconds are spent (at least
-    one head)."""
+    """Time the fp64 oracle on a bounded sample of the workload: blocks of
+    query rows (two mirrored chunks of S / CPU_CHUNKS rows of one head, every
+    mask mode of the workload) one after another, cycling over the blocks of
+    every head, until ``budget_s`` seconds are spent (at least one block)."""
     from oracle import attention_rows
     qb, kb, vb = inputs if inputs is not None else fa_inputs.make_qkv_for(w)
+    blocks, chunk = _row_blocks(w.S)
+    order = [(b, h, rows) for b in range(w.B) for h in range(w.H) for rows in blocks]
     flops = 0.0
-    heads = 0
-    rows = np.arange(w.S)
-    order = [(b, h) for b in range(w.B) for h in range(w.H)]
+    done = 0
     t0 = time.perf_counter()
     while True:
-        b, h = order[heads % len(order)]
+        b, h, rows = order[done % len(order)]
         for causal in w.modes:
             attention_rows(qb, kb, vb, w.dtype, causal, w.scale, b, h, rows)
-            flops += fa_inputs.attention_flops(1, 1, w.S, w.D, causal)
-        heads += 1
+            flops += _row_flops(rows, w.S, w.D, causal)
+        done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    heads = len({(b, h) for b, h, _ in order[:min(done, len(order))]})
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{heads} (b,h) heads of {w.name} ({w.B * w.H} in the workload), all "
-                      f"{w.S} rows, modes {['causal' if c else 'non-causal' for c in w.modes]}; "
+            "sample": f"{done} row blocks of {w.name} (rows of two mirrored {chunk}-row chunks of one "
+                      f"(b,h) head, {len(blocks)} blocks per head; {heads} of the workload's "
+                      f"{w.B * w.H} heads touched), modes "
+                      f"{['causal' if c else 'non-causal' for c in w.modes]}; "
                       f"fp64 numpy, BLAS threads = cores; {dt:.1f} s"}
 
 

@@ -11,6 +11,7 @@ import json
 import os
 import types
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -95,13 +96,26 @@ def test_theoretical_peak_arithmetic(monkeypatch):
     assert bench._theoretical(1.0, {"sm_max_mhz": None, "sm_mhz": 0}, 0)["at_max_clock"] is None
 
 
-def test_cpu_baseline_takes_at_least_one_whole_head():
+def test_cpu_baseline_takes_at_least_one_row_block():
     bench = _bench()
     w = bench.fa_inputs.WORKLOADS["s256"]
     out = bench.cpu_baseline(w, budget_s=0.0)
     assert out["kind"] == "oracle" and out["unit"] == "TFLOP/s"
     assert out["value"] > 0 and out["cores"] >= 1
-    assert out["sample"].startswith("1 (b,h) heads of s256")
+    assert out["sample"].startswith("1 row blocks of s256")
+
+
+@pytest.mark.parametrize("S", [1, 7, 256, 1999, 8192])
+@pytest.mark.parametrize("causal", [False, True])
+def test_cpu_baseline_row_blocks_cover_each_row_once_and_sum_to_the_convention(S, causal):
+    """The row blocks of a head partition its rows, and their counted FLOPs
+    add up to the convention for the whole head (4 S^2 D, half causal)."""
+    bench = _bench()
+    blocks, _ = bench._row_blocks(S)
+    rows = np.sort(np.concatenate(blocks))
+    assert np.array_equal(rows, np.arange(S))
+    total = sum(bench._row_flops(r, S, 64, causal) for r in blocks)
+    assert total == pytest.approx(bench.fa_inputs.attention_flops(1, 1, S, 64, causal), rel=1e-12)
 
 
 def test_one_thread_oracle_sample_and_cpu_model():
