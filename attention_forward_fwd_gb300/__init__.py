@@ -21,7 +21,7 @@ __all__ = ["fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
            "FaError", "library", "EXPORTED_SYMBOLS", "FA_F16", "FA_BF16"]
 
 (FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT,
- FA_ERR_BAD_SEQLENS) = range(6)
+ FA_ERR_BAD_SEQLENS, FA_ERR_DEVICE_CHECK) = range(7)
 FA_F16, FA_BF16 = 0, 1
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_status_string",
@@ -46,47 +46,65 @@ def library() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with "
                                "attention_forward_fwd_gb300.build()")
-        lib = ctypes.CDLL(LIB_PATH)
-        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        sig = [vp, vp, vp, vp, vp, i, i, i, i, i, f]
-        lib.fa_fwd.argtypes = sig + [i, vp]
-        lib.fa_fwd_f16.argtypes = sig + [vp]
-        lib.fa_fwd_bf16.argtypes = sig + [vp]
-        for fn in (lib.fa_fwd, lib.fa_fwd_f16, lib.fa_fwd_bf16):
-            fn.restype = i
-        lib.fa_status_string.argtypes = [i]
-        lib.fa_status_string.restype = ctypes.c_char_p
-        lib.fa_device_status.argtypes = [i]
-        lib.fa_device_status.restype = i
-        lib.fa_last_device_status.argtypes = [vp]
-        lib.fa_last_device_status.restype = i
-        lib.fa_splitkv_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
-        lib.fa_splitkv_workspace_size.restype = i
-        lib.fa_splitkv_launches.argtypes = [i, i, i, i, i]
-        lib.fa_splitkv_launches.restype = i
-        lib.fa_split_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(i), i, ctypes.POINTER(i)]
-        lib.fa_split_plan.restype = i
-        lib.fa_fwd_splitkv.argtypes = sig + [i, vp, ctypes.c_size_t, vp]
-        lib.fa_fwd_splitkv.restype = i
-        gsig = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i]   # ..., B, H, H_kv, S, D, causal, scale, dtype
-        lib.fa_fwd_gqa.argtypes = gsig + [vp]
-        lib.fa_fwd_gqa.restype = i
-        lib.fa_fwd_gqa_splitkv.argtypes = gsig + [vp, ctypes.c_size_t, vp]
-        lib.fa_fwd_gqa_splitkv.restype = i
-        # Q, K, V, O, LSE, cu_seqlens, B, max_seqlen, total, H, H_kv, D, causal, scale, dtype, stream
-        lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
-        lib.fa_fwd_varlen.restype = i
-        # ..., B, H, H_kv, S, D, causal, window_left, window_right, scale, dtype, stream
-        lib.fa_fwd_local.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
-        lib.fa_fwd_local.restype = i
-        lib.fa_selftest_timeout.argtypes = [vp, vp, vp, vp, i, i, i, vp]
-        # ..., B, H, H_kv, S, D, causal, p_drop, seed, scale, dtype, stream
-        lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_double,
-                                       ctypes.c_ulonglong, f, i, vp]
-        lib.fa_fwd_dropout.restype = i
-        lib.fa_selftest_timeout.restype = i
-        _LIB = lib
+        _LIB = _declare(ctypes.CDLL(LIB_PATH))
     return _LIB
+
+
+_DEBUG_LIB = None
+
+
+def debug_library() -> ctypes.CDLL:
+    """Build (if needed) and load libfa_gb300_debug.so: the same C-ABI with
+    the device-side invariant checks, which report FA_ERR_DEVICE_CHECK
+    through its own fa_device_status.  A separate library with a status word
+    of its own; for tests."""
+    global _DEBUG_LIB
+    if _DEBUG_LIB is None:
+        _DEBUG_LIB = _declare(ctypes.CDLL(build(debug=True)))
+    return _DEBUG_LIB
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Argument and result types of every exported function."""
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    sig = [vp, vp, vp, vp, vp, i, i, i, i, i, f]
+    lib.fa_fwd.argtypes = sig + [i, vp]
+    lib.fa_fwd_f16.argtypes = sig + [vp]
+    lib.fa_fwd_bf16.argtypes = sig + [vp]
+    for fn in (lib.fa_fwd, lib.fa_fwd_f16, lib.fa_fwd_bf16):
+        fn.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_device_status.argtypes = [i]
+    lib.fa_device_status.restype = i
+    lib.fa_last_device_status.argtypes = [vp]
+    lib.fa_last_device_status.restype = i
+    lib.fa_splitkv_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_splitkv_workspace_size.restype = i
+    lib.fa_splitkv_launches.argtypes = [i, i, i, i, i]
+    lib.fa_splitkv_launches.restype = i
+    lib.fa_split_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(i), i, ctypes.POINTER(i)]
+    lib.fa_split_plan.restype = i
+    lib.fa_fwd_splitkv.argtypes = sig + [i, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_splitkv.restype = i
+    gsig = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i]   # ..., B, H, H_kv, S, D, causal, scale, dtype
+    lib.fa_fwd_gqa.argtypes = gsig + [vp]
+    lib.fa_fwd_gqa.restype = i
+    lib.fa_fwd_gqa_splitkv.argtypes = gsig + [vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_gqa_splitkv.restype = i
+    # Q, K, V, O, LSE, cu_seqlens, B, max_seqlen, total, H, H_kv, D, causal, scale, dtype, stream
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_varlen.restype = i
+    # ..., B, H, H_kv, S, D, causal, window_left, window_right, scale, dtype, stream
+    lib.fa_fwd_local.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_local.restype = i
+    lib.fa_selftest_timeout.argtypes = [vp, vp, vp, vp, i, i, i, vp]
+    # ..., B, H, H_kv, S, D, causal, p_drop, seed, scale, dtype, stream
+    lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_double,
+                                   ctypes.c_ulonglong, f, i, vp]
+    lib.fa_fwd_dropout.restype = i
+    lib.fa_selftest_timeout.restype = i
+    return lib
 
 
 def fa_status_string(status: int) -> str:

@@ -17,6 +17,9 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
+# the same sources with the device-side invariant checks (FA_DEBUG = 1)
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libfa_gb300_debug.so")
+DEBUG_FLAGS = ["-DFA_DEBUG=1"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMPILE_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC"]
 
@@ -39,14 +42,14 @@ def _sources():
 STAMP_PATH = LIB_PATH + ".sha256"
 
 
-def source_hash() -> str:
+def source_hash(debug: bool = False) -> str:
     """SHA-256 over the library's sources (names and contents), the compile
     command's flags and this machine's architecture: the stamp a built
     library must carry to be reused."""
     import hashlib
     import platform
     h = hashlib.sha256()
-    h.update(" ".join(ARCH_FLAGS + COMPILE_FLAGS).encode())
+    h.update(" ".join(ARCH_FLAGS + COMPILE_FLAGS + (DEBUG_FLAGS if debug else [])).encode())
     h.update(platform.machine().encode())
     for path in _sources():
         with open(path, "rb") as f:
@@ -54,14 +57,16 @@ def source_hash() -> str:
     return h.hexdigest()
 
 
-def needs_build() -> bool:
+def needs_build(debug: bool = False) -> bool:
     """True unless the library exists and its stamp matches the sources (file
     times are not trusted: a copied tree can carry a library newer than
     sources it was not built from)."""
-    if not (os.path.exists(LIB_PATH) and os.path.exists(STAMP_PATH)):
+    lib = DEBUG_LIB_PATH if debug else LIB_PATH
+    stamp = lib + ".sha256"
+    if not (os.path.exists(lib) and os.path.exists(stamp)):
         return True
-    with open(STAMP_PATH) as f:
-        return f.read().strip() != source_hash()
+    with open(stamp) as f:
+        return f.read().strip() != source_hash(debug)
 
 
 # Registers per thread the attention kernel must launch with, by its last
@@ -103,19 +108,21 @@ def check_launch_registers(ptxas_log: str) -> None:
         raise RuntimeError("no fa_fwd_kernel register report in the ptxas output")
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
     """Compile the library unless it exists with the stamp of the current
-    sources."""
-    if not force and not needs_build():
-        return LIB_PATH
+    sources; ``debug`` builds libfa_gb300_debug.so, the same sources with the
+    device-side invariant checks (FA_DEBUG = 1)."""
+    lib = DEBUG_LIB_PATH if debug else LIB_PATH
+    if not force and not needs_build(debug):
+        return lib
     out_dir = os.path.join(ROOT, "_build")
     os.makedirs(out_dir, exist_ok=True)
-    tmp = LIB_PATH + ".tmp"
-    stamp = source_hash()
-    cmd = [_nvcc(), *ARCH_FLAGS, *COMPILE_FLAGS, "-Xptxas", "-v", "-I", INCLUDE,
-           "-o", tmp, os.path.join(CSRC, "fa_api.cu")]
+    tmp = lib + ".tmp"
+    stamp = source_hash(debug)
+    cmd = [_nvcc(), *ARCH_FLAGS, *COMPILE_FLAGS, *(DEBUG_FLAGS if debug else []), "-Xptxas", "-v",
+           "-I", INCLUDE, "-o", tmp, os.path.join(CSRC, "fa_api.cu")]
     res = subprocess.run(cmd, capture_output=True, text=True)
-    with open(os.path.join(out_dir, "ptxas.txt"), "w") as f:
+    with open(os.path.join(out_dir, "ptxas_debug.txt" if debug else "ptxas.txt"), "w") as f:
         f.write(" ".join(cmd) + "\n" + res.stdout + res.stderr)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stderr[-4000:]}")
@@ -124,12 +131,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     except RuntimeError:
         os.remove(tmp)
         raise
-    os.replace(tmp, LIB_PATH)
-    with open(STAMP_PATH, "w") as f:
+    os.replace(tmp, lib)
+    with open(lib + ".sha256", "w") as f:
         f.write(stamp + "\n")
     if verbose:
         print(res.stderr)
-    return LIB_PATH
+    return lib
 
 
 if __name__ == "__main__":

@@ -95,6 +95,10 @@ int num_sms() {
 // The kernel's parameters (four tensor maps and FwdParams) must fit the 4 KiB
 // of a launch's parameter space.
 static_assert(sizeof(fa::FwdParams) + 4 * sizeof(CUtensorMap) <= 4096, "kernel parameters too large");
+// the device status word carries the host's codes
+static_assert(fa::kStatusTimeout == FA_ERR_TIMEOUT && fa::kStatusBadSeqlens == FA_ERR_BAD_SEQLENS &&
+                  fa::kStatusDeviceCheck == FA_ERR_DEVICE_CHECK,
+              "device status codes");
 
 // Head dimensions the library takes: multiples of 8 up to 256 (the row
 // strides of the tensor maps must be multiples of 16 bytes).  D = 64, 128
@@ -676,6 +680,7 @@ const char* fa_status_string(int status) {
         case FA_ERR_CUDA: return "CUDA runtime or driver error";
         case FA_ERR_TIMEOUT: return "a device-side wait timed out";
         case FA_ERR_BAD_SEQLENS: return "a sequence offset was out of range (that sequence was skipped)";
+        case FA_ERR_DEVICE_CHECK: return "a device-side invariant check failed (debug build)";
         default: return "unknown status";
     }
 }

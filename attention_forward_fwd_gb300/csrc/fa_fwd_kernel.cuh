@@ -95,8 +95,23 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 constexpr int kStatusTimeout = 4;
 constexpr int kStatusBadSeqlens = 5;   // a sequence offset was out of range (sequence skipped)
 
+constexpr int kStatusDeviceCheck = 6;   // a device-side invariant check failed (FA_DEBUG builds)
+
 // Device status word: 0, or the status of the first wait that ran out.
 __device__ int g_fa_device_status;
+
+// Builds with FA_DEBUG = 1 check invariants on the device (work-item bounds,
+// the tensor-memory allocation, the roles' tile counts, row sums); a failed
+// check records kStatusDeviceCheck in the status word -- the kernel does not
+// trap -- and the results are those of the build without the checks.
+#ifndef FA_DEBUG
+#define FA_DEBUG 0
+#endif
+__device__ __forceinline__ void debug_check(bool cond) {
+    if constexpr (FA_DEBUG != 0) {
+        if (!cond) atomicCAS(&g_fa_device_status, 0, kStatusDeviceCheck);
+    }
+}
 
 // query blocks per head, and work items per head, beyond which the keys are
 // never split
@@ -210,6 +225,9 @@ struct Barriers {
     uint64_t drain[kQTiles];
     uint32_t tmem_base;
     int abort;
+    // FA_DEBUG: tiles each role saw (producer ring, each issuer's ring, S per
+    // query tile as issued and as read by the softmax)
+    int dbg[7];
     // the RS threads of a row swap partial row maxima (double-buffered over
     // key tiles) and, at the end of an item, partial row sums (double-buffered
     // over items)
@@ -364,6 +382,14 @@ __device__ __forceinline__ WorkItem decode_item(const FwdParams& p, int w) {
     }
     it.nkv = max(it.nkv0, it.nkv1);
     it.partial = nsplit > 1;
+    if constexpr (FA_DEBUG != 0) {
+        // key tiles [jb, jb + nkv) inside the sequence, each query tile's
+        // range inside the item's, and the split fields in range
+        const int tiles = (it.S + kBN - 1) / kBN;
+        debug_check(it.jb >= 0 && it.s0 >= 0 && it.s1 >= 0 && it.s0 <= it.nkv0 && it.s1 <= it.nkv1 &&
+                    (it.nkv == 0 || (it.jb + it.nkv <= tiles && it.q0 < it.S)));
+        if (p.kv_chunk > 0) debug_check(qb < p.nqb && nsplit >= 1 && it.split < nsplit);
+    }
     return it;
 }
 
@@ -559,6 +585,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             ptx::mbar_init(bar_addr(&bars->drain[t]), 1);
         }
         bars->abort = 0;
+        for (int d = 0; d < 7; ++d) bars->dbg[d] = 0;
         ptx::fence_barrier_init();
         ptx::tma_prefetch_map(&tmQ);
         ptx::tma_prefetch_map(&tmK);
@@ -590,6 +617,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
+    debug_check((tmem & 0xffffu) == 0u);   // all 512 columns, from column 0
     // The next kernel in the stream (the combine launch of the split path, or
     // the next call) may be scheduled as soon as every CTA of this grid is
     // running; it waits for this grid to finish before touching memory.
@@ -649,6 +677,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 }
                 ++ki;
             }
+            if (FA_DEBUG && lane == 0) bars->dbg[0] = static_cast<int>(gi);
             if (*abort_flag) {
                 // Let every copy this warp started land before the CTA exits.
                 wait_warp(qbar, k_q & 1, false);
@@ -734,6 +763,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             };
 
             int gi0 = 0;       // ring position of the item's first tile, modulo 2*NS
+            int ring_total = 0;   // ring items seen, all items (FA_DEBUG count)
             uint32_t gs = 0;   // S_t tiles issued, all items (parities only)
             bool ok = true;
             int ki = 0;   // items with key tiles so far
@@ -794,6 +824,11 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     }
                 }
                 gi0 = (gi0 + 2 * nkv) % (2 * NS);
+                ring_total += 2 * nkv;
+            }
+            if (FA_DEBUG && lane == 0) {
+                bars->dbg[1 + t] = ring_total;
+                bars->dbg[3 + t] = static_cast<int>(gs);
             }
             // Every MMA of this issuer must be complete before TMEM is freed.
             ptx::tc_commit_warp(bar_addr(&bars->drain[t]));
@@ -857,6 +892,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
             };
 
             int gi0 = 0;                   // ring position of the item's K0, modulo 2*NS
+            int ring_total = 0;            // ring items seen, all items (FA_DEBUG count)
             uint32_t gs[kQTiles] = {0, 0};  // S_t tiles issued per query tile (parities only)
             bool ok = true;
             int ki = 0;   // items with key tiles so far
@@ -922,6 +958,12 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                 gs[0] += max(0, nkv0 - s0);
                 gs[1] += max(0, nkv1 - s1);
                 gi0 = (gi0 + 2 * nkv) % (2 * NS);
+                ring_total += 2 * nkv;
+            }
+            if (FA_DEBUG && lane == 0) {
+                bars->dbg[1] = bars->dbg[2] = ring_total;
+                bars->dbg[3] = static_cast<int>(gs[0]);
+                bars->dbg[4] = static_cast<int>(gs[1]);
             }
             // Every MMA must be complete before TMEM is freed.
             ptx::tc_commit_warp(bar_addr(&bars->drain[0]));
@@ -1313,6 +1355,8 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
                     if (store_thread) ptx::bulk_wait_group_read_all();
                     ptx::named_barrier_sync(tile_bar, kTileThreads);
                 }
+                // a stored row saw at least one key (its own, or key 0)
+                if (eok && row < ie.S) debug_check(l_row > 0.f);
                 float inv_l = 1.f / l_row;
                 if constexpr (FEAT == kDropout) inv_l *= p.drop_inv_keep;   // kept P scaled by 1 / (1 - p)
                 // row of O: batch tb (0 when packed) of S rows, then the
@@ -1381,10 +1425,14 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
         }
         // every O store must be complete before the CTA exits
         if (store_thread) ptx::bulk_wait_group_all();
+        if (FA_DEBUG && store_thread) bars->dbg[5 + t] = static_cast<int>(gs0);
     }
 
     ptx::tc_fence_before_sync();
     __syncthreads();
+    if (FA_DEBUG && threadIdx.x == 0 && !*abort_flag)
+        debug_check(bars->dbg[0] == bars->dbg[1] && bars->dbg[1] == bars->dbg[2] &&
+                    bars->dbg[3] == bars->dbg[5] && bars->dbg[4] == bars->dbg[6]);
     if (warp == kMmaWarp) {
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem, kTmemCols);
@@ -1415,6 +1463,7 @@ __global__ void __launch_bounds__(kCombineThreads) fa_combine_kernel(const FwdPa
     const int qt = blockIdx.x / kPerTile;
     const int bh = blockIdx.y;
     const int ns = p.block_splits[qt / kQTiles];
+    debug_check(ns >= 1 && ns <= p.max_splits);
     // the next kernel in the stream may start its set-up now (it waits for
     // this grid before touching memory)
     ptx::launch_dependents();

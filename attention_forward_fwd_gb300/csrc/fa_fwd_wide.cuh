@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int qt = causal ? (ntq - 1 - y) : y;
     const int r0 = qt * kBM;
     const int n_tiles = key_tiles_for(r0, p.S, causal);   // >= 1 (key 0 is always visible)
+    debug_check(qt >= 0 && qt < ntq && bh < bhn && n_tiles >= 1);
 
     if (threadIdx.x == 32 * 5) {
         ptx::mbar_init(bar(&bars->q_full), 1);

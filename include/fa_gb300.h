@@ -59,6 +59,12 @@
  *                       sequence offset out of range; nothing of that
  *                       sequence was read or written (its O / LSE rows are
  *                       left as they were)
+ *   FA_ERR_DEVICE_CHECK reported by fa_device_status() and
+ *                       fa_last_device_status() of a library built with
+ *                       FA_DEBUG = 1 only: a device-side invariant check
+ *                       failed (work-item bounds, the tensor-memory
+ *                       allocation, the tile counts of the kernel's roles,
+ *                       a stored row's sum); the kernel does not trap
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -79,7 +85,8 @@ typedef enum {
     FA_ERR_UNSUPPORTED = 2,
     FA_ERR_CUDA = 3,
     FA_ERR_TIMEOUT = 4,
-    FA_ERR_BAD_SEQLENS = 5
+    FA_ERR_BAD_SEQLENS = 5,
+    FA_ERR_DEVICE_CHECK = 6
 } fa_status_t;
 
 typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype_t;

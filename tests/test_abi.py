@@ -40,8 +40,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(5):
-        assert fa.fa_status_string(code)
+    texts = [fa.fa_status_string(code) for code in range(7)]
+    assert all(texts) and len(set(texts)) == 7 and "unknown status" not in texts
+    assert fa.fa_status_string(fa.FA_ERR_DEVICE_CHECK).startswith("a device-side invariant check")
     assert fa.fa_status_string(99) == "unknown status"
 
 
