@@ -515,6 +515,8 @@ def run_ours(args, w):
             "e2e": e2e,
             "wall_s_timed_region": t_wall}
     line["pages_protocol"] = pages_protocol(step, stream, dev, flops_step)
+    # which kernel sources produced the line (the hash the traffic table is keyed on)
+    line["kernel_sha"] = _kernel_sha()
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
         line["cpu_baseline"]["cpu_model"] = _cpu_model()
