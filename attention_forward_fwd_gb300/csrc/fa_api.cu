@@ -221,9 +221,33 @@ double simulate_plan(const SplitPlan& plan, int S, bool causal, long long bh, in
 //   cap, or the m lightest or heaviest blocks into 2-4 pieces (m on a grid
 //   of at most ~16 values; only with `multiwave`).  Planned once per shape
 //   (cached below): at most ~2 ms of host time for the largest shapes.
-SplitPlan plan_split_uncached(int B, int H, int S, int D, bool causal, int sms, bool multiwave) {
+// The wide kernel (D > 128, one CTA per 128-row query tile): when the
+// tiles fill less than three quarters of a wave, every tile's keys are
+// divided into the same number of chunks (at most the merge kernel's
+// register-held splits), so that the CTAs come close to one per SM.
+SplitPlan plan_split_wide(int B, int H, int S, int sms) {
     SplitPlan plan = no_split(S);
-    if (kernel_dim(D) > 128 || sms <= 0) return plan;   // the wide kernel does not split
+    const long long tiles = static_cast<long long>(B) * H * ((S + fa::kBM - 1) / fa::kBM);
+    const int max_kt = (S + fa::kBN - 1) / fa::kBN;
+    const int nqb = (S + fa::kQTiles * fa::kBM - 1) / (fa::kQTiles * fa::kBM);
+    if (sms <= 0 || tiles * 4 >= static_cast<long long>(sms) * 3 || max_kt < 2 || nqb > fa::kMaxSplitBlocks)
+        return plan;
+    int ns = static_cast<int>(std::min<long long>(std::min<long long>(fa::kCombineMaxSplits, max_kt), sms / tiles));
+    if (ns < 2) return plan;
+    const int chunk = (max_kt + ns - 1) / ns;
+    ns = (max_kt + chunk - 1) / chunk;
+    if (ns < 2) return plan;
+    plan.chunk = chunk;
+    plan.max_splits = ns;
+    plan.ctas_per_head = ((S + fa::kBM - 1) / fa::kBM) * ns;
+    std::fill(plan.ns, plan.ns + nqb, static_cast<uint8_t>(ns));
+    return plan;
+}
+
+SplitPlan plan_split_uncached(int B, int H, int S, int D, bool causal, int sms, bool multiwave) {
+    if (kernel_dim(D) > 128) return plan_split_wide(B, H, S, sms);
+    SplitPlan plan = no_split(S);
+    if (sms <= 0) return plan;
     const int rows_per_cta = fa::kQTiles * fa::kBM;
     const int nqb = (S + rows_per_cta - 1) / rows_per_cta;
     const int nkv_all = (S + fa::kBN - 1) / fa::kBN;
@@ -345,6 +369,27 @@ struct Options {
     int drop_first_q = 0;              // test support: the first Q load is withheld
 };
 
+// Merge the partials of a split call (fa_combine_kernel), launched as a
+// programmatic dependent of the main kernel: the launch gap is hidden.
+template <int D, bool BF16>
+int launch_combine(const fa::FwdParams& p, void* O, int B, int H, size_t ntq, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    constexpr int kPerTile = fa::kBM / (fa::kCombineThreads / (D / 8));
+    cfg.gridDim = dim3(static_cast<unsigned>(ntq * kPerTile),
+                       static_cast<unsigned>(B) * static_cast<unsigned>(H));
+    cfg.blockDim = dim3(fa::kCombineThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fa::fa_combine_kernel<D, BF16>, p, O) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
 template <int D, bool BF16, int NS, int RS, int FEAT>
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
            int S, int Dh, int causal, float scale, cudaStream_t stream, const SplitPlan& plan,
@@ -425,22 +470,7 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     if (cudaLaunchKernelEx(&mcfg, kern, mq, mk, mv, mo, p) != cudaSuccess) return FA_ERR_CUDA;
     if (plan.chunk == 0) return FA_OK;
 
-    // merge the partials; programmatic dependent launch hides the launch gap
-    cudaLaunchConfig_t cfg = {};
-    constexpr int kPerTile = fa::kBM / (fa::kCombineThreads / (D / 8));
-    cfg.gridDim = dim3(static_cast<unsigned>(ntq * kPerTile),
-                       static_cast<unsigned>(B) * static_cast<unsigned>(H));
-    cfg.blockDim = dim3(fa::kCombineThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, fa::fa_combine_kernel<D, BF16>, p, O) != cudaSuccess)
-        return FA_ERR_CUDA;
-    return FA_OK;
+    return launch_combine<D, BF16>(p, O, B, H, ntq, stream);
 }
 
 int validate(const void* Q, const void* K, const void* V, void* O, const float* LSE, int B, int H,
@@ -467,7 +497,8 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
 // dependent launch as the main kernel.
 template <bool BF16>
 int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
-                int Hkv, int S, int Dh, int causal, float scale, cudaStream_t stream, const Options& opt) {
+                int Hkv, int S, int Dh, int causal, float scale, cudaStream_t stream, const SplitPlan& plan,
+                void* workspace, const Options& opt) {
     auto kern = fa::fa_fwd_wide_kernel<BF16>;
     constexpr int kSmem = fa::WideSmem::kAlloc;
     static std::once_flag once[64];
@@ -493,7 +524,19 @@ int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE
     p.lse = LSE;
     p.drop_first_q = opt.drop_first_q;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-    const long long ctas = static_cast<long long>(B) * H * ((S + fa::kBM - 1) / fa::kBM);
+    const size_t ntq = (S + fa::kBM - 1) / fa::kBM;
+    // split over keys: max_splits CTAs per query tile, partials in the
+    // workspace, merged by fa_combine_kernel
+    p.kv_chunk = plan.chunk;
+    p.max_splits = plan.chunk ? plan.max_splits : 1;
+    p.nqb = (S + fa::kQTiles * fa::kBM - 1) / (fa::kQTiles * fa::kBM);
+    if (plan.chunk) {
+        const size_t o_floats = static_cast<size_t>(B) * H * ntq * plan.max_splits * fa::kBM * fa::kWideD;
+        p.ws_o = static_cast<float*>(workspace);
+        p.ws_ml = static_cast<float*>(workspace) + o_floats;
+        std::copy(plan.ns, plan.ns + fa::kMaxSplitBlocks, p.block_splits);
+    }
+    const long long ctas = static_cast<long long>(B) * H * ntq * p.max_splits;
     if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -505,7 +548,9 @@ int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE
     cfg.stream = stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) != cudaSuccess) return FA_ERR_CUDA;
+    if (plan.chunk == 0) return FA_OK;
+    return launch_combine<fa::kWideD, BF16>(p, O, B, H, ntq, stream);
 }
 
 int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
@@ -526,9 +571,10 @@ int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, i
                             : FA_ONE(D_, BF16_, NS_, RS_, fa::kPlain))
     const int kd = kernel_dim(D);
     if (kd > 128) {
-        if (feat != fa::kPlain || plan.chunk != 0) return FA_ERR_UNSUPPORTED;
-        return dtype == FA_F16 ? launch_wide<false>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, opt)
-                               : launch_wide<true>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, opt);
+        if (feat != fa::kPlain) return FA_ERR_UNSUPPORTED;
+        return dtype == FA_F16
+                   ? launch_wide<false>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt)
+                   : launch_wide<true>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt);
     }
     if (dtype == FA_F16) {
         if (kd == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);

@@ -105,7 +105,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const long long kv_head_bytes = max(1ll, 4ll * p.S * p.d_head / p.kv_group);
     const int group = static_cast<int>(max(
         1ll, min(static_cast<long long>(bhn), (causal ? kWideL2ShareCausal : kWideL2Share) / kv_head_bytes)));
-    const int x = static_cast<int>(blockIdx.x);
+    // split over keys (kv_chunk > 0): CTA blockIdx.x runs split s = blockIdx.x
+    // % max_splits of query tile x = blockIdx.x / max_splits, the key tiles
+    // [s * kv_chunk, (s + 1) * kv_chunk) of its range (possibly none)
+    const int nsplit = p.kv_chunk > 0 ? p.max_splits : 1;
+    const int x = static_cast<int>(blockIdx.x) / nsplit;
+    const int split = static_cast<int>(blockIdx.x) - x * nsplit;
     const int g0 = (x / (group * ntq)) * group;   // first head of x's group
     const int gsize = min(group, bhn - g0);
     const int local = x - g0 * ntq;               // in [0, gsize * ntq)
@@ -116,8 +121,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int hkv = h / p.kv_group;
     const int qt = causal ? (ntq - 1 - y) : y;
     const int r0 = qt * kBM;
-    const int n_tiles = key_tiles_for(r0, p.S, causal);   // >= 1 (key 0 is always visible)
-    debug_check(qt >= 0 && qt < ntq && bh < bhn && n_tiles >= 1);
+    const int n_all = key_tiles_for(r0, p.S, causal);   // >= 1 (key 0 is always visible)
+    const int jb = split * p.kv_chunk;                  // first key tile of this CTA
+    const int n_tiles = p.kv_chunk > 0 ? max(0, min(n_all, jb + p.kv_chunk) - jb) : n_all;
+    debug_check(qt >= 0 && qt < ntq && bh < bhn && n_all >= 1 && (p.kv_chunk > 0 || n_tiles >= 1) &&
+                split < nsplit);
 
     if (threadIdx.x == 32 * 5) {
         ptx::mbar_init(bar(&bars->q_full), 1);
@@ -166,7 +174,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             for (int c = 0; c < kWideAtoms; ++c)
                 ptx::tma_load_4d(dst + c * (kBM * 128), map, full, c * 64, head, row0, b);
         };
-        if (lane == 0) {
+        if (lane == 0 && n_tiles > 0) {
             if (!p.drop_first_q) load_tile(&tmQ, q_dst, bar(&bars->q_full), h, r0);
         }
         // K(j+1) is needed before V(j) (the MMA order is S(j+1), P V(j)):
@@ -186,23 +194,23 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         return;
                     if (lane == 0) {
                         ptx::mbar_arrive_expect_tx(full, kWideTileBytes / kWideAtoms);
-                        ptx::tma_load_4d(slot0 + c * (kBN * 128), &tmK, full, c * 64, hkv, i * kBN, b);
+                        ptx::tma_load_4d(slot0 + c * (kBN * 128), &tmK, full, c * 64, hkv, (jb + i) * kBN, b);
                     }
                     ++nkb[c];
                 }
             } else {
                 if (i > 0 && !(ok = wait_warp(bar(&bars->kv_empty[0]), static_cast<uint32_t>((i - 1) & 1)))) return;
-                if (lane == 0) load_tile(&tmK, slot0, bar(&bars->kv_full[0]), hkv, i * kBN);
+                if (lane == 0) load_tile(&tmK, slot0, bar(&bars->kv_full[0]), hkv, (jb + i) * kBN);
             }
             ++nk;
         };
         auto load_v = [&](int i) {
             if (i > 0 && !(ok = wait_warp(bar(&bars->kv_empty[1]), static_cast<uint32_t>((i - 1) & 1)))) return;
-            if (lane == 0) load_tile(&tmV, slot0 + kWideTileBytes, bar(&bars->kv_full[1]), hkv, i * kBN);
+            if (lane == 0) load_tile(&tmV, slot0 + kWideTileBytes, bar(&bars->kv_full[1]), hkv, (jb + i) * kBN);
             ++nv;
         };
-        load_k(0);
-        if (ok) load_v(0);
+        if (n_tiles > 0) load_k(0);
+        if (ok && n_tiles > 0) load_v(0);
         if (ok && n_tiles > 1) load_k(1);
         for (int j = 1; j < n_tiles && ok; ++j) {
             if (j + 1 < n_tiles) load_k(j + 1);
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         if (*abort_flag) {
             // let every copy this warp started land before the CTA exits
             // (only the last of each slot can still be in flight)
-            wait_warp(bar(&bars->q_full), 0, false);
+            if (n_tiles > 0) wait_warp(bar(&bars->q_full), 0, false);
             if (FA_WIDE_KBOX == 0 && nk > 0)
                 wait_warp(bar(&bars->kv_full[0]), static_cast<uint32_t>((nk - 1) & 1), false);
             for (int c = 0; c < kWideAtoms; ++c)
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
         constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, kWideD, BF16, true);
         const uint32_t slot0 = sbase + WideSmem::kOffKV;
-        bool ok = wait_warp(bar(&bars->q_full), 0);
+        bool ok = n_tiles == 0 || wait_warp(bar(&bars->q_full), 0);
         const uint64_t qd = ptx::sdesc_sw128(sbase + WideSmem::kOffQ, 16, 1024);
         const uint64_t kd = ptx::sdesc_sw128(slot0, 16, 1024);
         const uint64_t vd = ptx::sdesc_sw128(slot0 + kWideTileBytes, kBN * 128, 1024);
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             ptx::tc_commit_warp(bar(&bars->s_full[i & 1]));
             ptx::tc_commit_warp(bar(&bars->kv_empty[0]));
         };
-        if (ok) issue_s(0);
+        if (ok && n_tiles > 0) issue_s(0);
         for (int j = 0; j < n_tiles && ok; ++j) {
             const uint32_t par = static_cast<uint32_t>(j & 1);
             if (j + 1 < n_tiles) {
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             ptx::tmem_ld_wait();
             ptx::reg_fence<kBN>(s);
             // keys past the end and, on the diagonal tile, keys after the row
-            const int kv0 = j * kBN;
+            const int kv0 = (jb + j) * kBN;
             const int last = causal ? min(p.S - 1, row) : (p.S - 1);
             if (kv0 + kBN - 1 > last || kv0 + kBN > p.S) {
 #pragma unroll
@@ -391,9 +399,35 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             ptx::mbar_arrive(bar(&bars->p_full[j & 1]));
         }
         // ---------------------------------------------------------- epilogue
-        ok = ok && wait_phase(bar(&bars->o_last), 0, abort_flag);
+        ok = ok && (n_tiles == 0 || wait_phase(bar(&bars->o_last), 0, abort_flag));
         ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
+        if (p.kv_chunk > 0) {
+            // partial result of this split (the layout of fa_fwd_kernel's split
+            // path: o~ as [D/4][128] float4, then m (log2 units) and l per
+            // row); a split with no key records l = 0 and m = -inf
+            const size_t slot = partial_slot(bh, ntq, qt, p.max_splits, split);
+            float* ml = p.ws_ml + slot * (2 * kBM);
+            float4* po = reinterpret_cast<float4*>(p.ws_o + slot * static_cast<size_t>(kBM * kWideD));
+            if (ok && n_tiles > 0) {
+                ptx::tc_fence_after_sync();
+#pragma unroll 1
+                for (int q = 0; q < kWideD / 32; ++q) {
+                    uint32_t o[32];
+                    ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence<32>(o);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        po[(q * 8 + u) * kBM + r] = make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
+                                                                __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]));
+                }
+                ml[r] = m_use * c;
+                ml[kBM + r] = l;
+            } else if (ok) {
+                ml[r] = -INFINITY;
+                ml[kBM + r] = 0.f;
+            }
+        } else if (ok) {
             ptx::tc_fence_after_sync();
             const float inv_l = 1.f / l;
             uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +

@@ -31,8 +31,10 @@
  *                cores do that padded work (a D = 96 call costs a D = 128 one).
  *                D > 128 has a kernel of its own (one 128-row query tile per
  *                CTA): the plain and grouped-K/V calls take it (the split
- *                entry points run it unsplit, with no workspace); the packed,
- *                windowed and dropout calls return FA_ERR_UNSUPPORTED there.
+ *                entry points divide every tile's keys into the same number
+ *                of chunks when the tiles fill less than three quarters of
+ *                the SMs); the packed, windowed and dropout calls return
+ *                FA_ERR_UNSUPPORTED there.
  *   LSE        : contiguous fp32 [B, H, S], or NULL to skip writing it.
  *
  * Ownership and ordering: the library keeps no pointer after a call returns

@@ -122,6 +122,20 @@ def test_multiwave_split_is_taken_and_exact(B, H, S, D, dtype, dist):
     _full_case(B, H, S, D, dtype, dist, 40 + S, False, split_kv=True)
 
 
+@pytest.mark.parametrize("S,D,dtype,causal,dist", [(1000, 256, "bf16", False, "normal"),
+                                                    (1000, 256, "f16", True, "stress"),
+                                                    (2500, 192, "bf16", True, "normal"),
+                                                    (4096, 256, "bf16", True, "normal"),
+                                                    (300, 136, "f16", False, "normal")])
+def test_wide_split_is_taken_and_exact(S, D, dtype, causal, dist):
+    """D > 128 with two heads: every query tile's keys are divided over
+    several CTAs of the wide kernel (causal: the later chunks of the early
+    tiles see no key and are skipped by the merge), and every element
+    matches the oracle."""
+    assert _splits(1, 2, S, D, causal)
+    _full_case(1, 2, S, D, dtype, dist, 50 + S + D, causal, split_kv=True)
+
+
 def test_split_kv_workspace_checks():
     import torch
     import attention_forward_fwd_gb300 as fa

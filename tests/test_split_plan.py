@@ -52,6 +52,24 @@ def test_one_head_splits_into_one_wave(causal):
         assert splits == [8] * 16     # 32 key tiles in chunks of 4: 128 CTAs
 
 
+@pytest.mark.parametrize("S", [1000, 4096])
+@pytest.mark.parametrize("causal", [False, True])
+def test_wide_kernel_splits_every_tile_alike(S, causal):
+    """D > 128 (one CTA per 128-row query tile): B1 H2 leaves most SMs idle,
+    so every tile's keys are divided into the same number of chunks (at most
+    16, the merge kernel's register-held splits), filling at most one wave;
+    a shape that fills the SMs is not split."""
+    splits, items = fa.fa_split_plan(1, 2, S, 256, causal, SMS)
+    ntq, max_kt = (S + 127) // 128, (S + 127) // 128
+    ns = splits[0]
+    assert 2 <= ns <= 16 and set(splits) == {ns}
+    assert items == ntq * ns and 2 * items <= SMS
+    chunk = math.ceil(max_kt / ns)
+    assert math.ceil(max_kt / chunk) == ns      # no split past the last key tile
+    full, items_full = fa.fa_split_plan(2, 16, 4096, 256, causal, SMS)
+    assert set(full) == {1} and items_full == (4096 + 255) // 256
+
+
 def test_ragged_last_wave_is_split():
     """B3 H8 S1999 non-causal: 192 equal blocks on 152 SMs leave a second
     wave of 40; splitting some blocks shortens the schedule."""
