@@ -509,9 +509,12 @@ int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE
         attr_err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     });
     if (attr_err[dev] != cudaSuccess) return FA_ERR_CUDA;
+    // packed variable-length tensors are one batch of `total` rows
+    const int mb = opt.cu_seqlens ? 1 : B;
+    const int ms = opt.cu_seqlens ? opt.total : S;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, Q, BF16, B, S, H, Dh, fa::kBM) || !make_map(&mk, K, BF16, B, S, Hkv, Dh, fa::kBN) ||
-        !make_map(&mv, V, BF16, B, S, Hkv, Dh, fa::kBN))
+    if (!make_map(&mq, Q, BF16, mb, ms, H, Dh, fa::kBM) || !make_map(&mk, K, BF16, mb, ms, Hkv, Dh, fa::kBN) ||
+        !make_map(&mv, V, BF16, mb, ms, Hkv, Dh, fa::kBN))
         return FA_ERR_CUDA;
     fa::FwdParams p = {};
     p.B = B;
@@ -522,6 +525,10 @@ int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE
     p.kv_group = H / Hkv;
     p.o_ptr = O;
     p.lse = LSE;
+    p.cu_seqlens = opt.cu_seqlens;
+    p.total = opt.total;
+    p.win_left = opt.win_left;
+    p.win_right = opt.win_right;
     p.drop_first_q = opt.drop_first_q;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     const size_t ntq = (S + fa::kBM - 1) / fa::kBM;
@@ -571,7 +578,8 @@ int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, i
                             : FA_ONE(D_, BF16_, NS_, RS_, fa::kPlain))
     const int kd = kernel_dim(D);
     if (kd > 128) {
-        if (feat != fa::kPlain) return FA_ERR_UNSUPPORTED;
+        // plain, grouped, packed and windowed calls; packed and windowed ones unsplit
+        if (feat == fa::kDropout || (feat != fa::kPlain && plan.chunk != 0)) return FA_ERR_UNSUPPORTED;
         return dtype == FA_F16
                    ? launch_wide<false>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt)
                    : launch_wide<true>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt);

@@ -121,11 +121,32 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int hkv = h / p.kv_group;
     const int qt = causal ? (ntq - 1 - y) : y;
     const int r0 = qt * kBM;
-    const int n_all = key_tiles_for(r0, p.S, causal);   // >= 1 (key 0 is always visible)
-    const int jb = split * p.kv_chunk;                  // first key tile of this CTA
-    const int n_tiles = p.kv_chunk > 0 ? max(0, min(n_all, jb + p.kv_chunk) - jb) : n_all;
-    debug_check(qt >= 0 && qt < ntq && bh < bhn && n_all >= 1 && (p.kv_chunk > 0 || n_tiles >= 1) &&
-                split < nsplit);
+    // The item's sequence: S_b rows from row `base` of batch `tb` of the
+    // tensors.  Packed batches (cu_seqlens) are one batch of `total` rows,
+    // sequence b rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (at most S); their
+    // offsets are read after the previous kernel in the stream has finished.
+    int S_b = p.S, base = 0, tb = b;
+    if (p.cu_seqlens != nullptr) {
+        ptx::grid_dependency_wait();
+        const int a = p.cu_seqlens[b];
+        const int e = p.cu_seqlens[b + 1];
+        const bool bad = !(a >= 0 && e >= a && e <= p.total && e - a <= p.S);
+        if (bad && qt == 0 && h == 0 && split == 0 && threadIdx.x == 0)
+            atomicCAS(&g_fa_device_status, 0, kStatusBadSeqlens);
+        S_b = bad ? 0 : e - a;
+        base = bad ? 0 : a;
+        tb = 0;
+    }
+    // key tiles [lo, hi) that the tile's rows see: up to the diagonal when
+    // causal, and within [row - win_left, row + win_right] for a local window
+    int lo = 0, hi = key_tiles_for(r0, S_b, causal);   // 0 past the sequence's end
+    if (p.win_left >= 0) lo = min(hi, max(0, r0 - p.win_left) / kBN);
+    if (p.win_right >= 0) hi = min(hi, (r0 + kBM - 1 + p.win_right) / kBN + 1);
+    const int n_all = max(0, hi - lo);
+    const int jb = lo + split * p.kv_chunk;             // first key tile of this CTA
+    const int n_tiles = p.kv_chunk > 0 ? max(0, min(hi, jb + p.kv_chunk) - jb) : n_all;
+    debug_check(qt >= 0 && qt < ntq && bh < bhn && (n_all >= 1 || r0 >= S_b) && split < nsplit &&
+                (p.kv_chunk == 0 || (p.cu_seqlens == nullptr && p.win_left < 0 && p.win_right < 0)));
 
     if (threadIdx.x == 32 * 5) {
         ptx::mbar_init(bar(&bars->q_full), 1);
@@ -172,7 +193,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int head, int row0) {
             ptx::mbar_arrive_expect_tx(full, kWideTileBytes);
             for (int c = 0; c < kWideAtoms; ++c)
-                ptx::tma_load_4d(dst + c * (kBM * 128), map, full, c * 64, head, row0, b);
+                ptx::tma_load_4d(dst + c * (kBM * 128), map, full, c * 64, head, base + row0, tb);
         };
         if (lane == 0 && n_tiles > 0) {
             if (!p.drop_first_q) load_tile(&tmQ, q_dst, bar(&bars->q_full), h, r0);
@@ -194,7 +215,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         return;
                     if (lane == 0) {
                         ptx::mbar_arrive_expect_tx(full, kWideTileBytes / kWideAtoms);
-                        ptx::tma_load_4d(slot0 + c * (kBN * 128), &tmK, full, c * 64, hkv, (jb + i) * kBN, b);
+                        ptx::tma_load_4d(slot0 + c * (kBN * 128), &tmK, full, c * 64, hkv, base + (jb + i) * kBN, tb);
                     }
                     ++nkb[c];
                 }
@@ -333,13 +354,16 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             for (int q = 0; q < kBN / 32; ++q) ptx::tmem_ld_32x32b_x32(tS + q * 32, s + q * 32);
             ptx::tmem_ld_wait();
             ptx::reg_fence<kBN>(s);
-            // keys past the end and, on the diagonal tile, keys after the row
+            // keys outside [first, last] are masked: past the sequence, after
+            // the row (causal) or outside the window
             const int kv0 = (jb + j) * kBN;
-            const int last = causal ? min(p.S - 1, row) : (p.S - 1);
-            if (kv0 + kBN - 1 > last || kv0 + kBN > p.S) {
+            int last = causal ? min(S_b - 1, row) : (S_b - 1);
+            if (p.win_right >= 0) last = min(last, row + p.win_right);
+            const int first = p.win_left >= 0 ? row - p.win_left : -1;
+            if (kv0 + kBN - 1 > last || kv0 < first) {
 #pragma unroll
                 for (int kq = 0; kq < kBN; ++kq)
-                    if (kv0 + kq > last) s[kq] = __float_as_uint(-INFINITY);
+                    if (kv0 + kq > last || kv0 + kq < first) s[kq] = __float_as_uint(-INFINITY);
             }
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -374,7 +398,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                     ptx::tmem_st_32x32b_x32(tO + q * 32, o);
                 }
             }
-            const float mc = m_use * c;
+            // (a row whose keys so far all lie outside its window has no
+            // reference yet: its p are 0)
+            const float mc = (m_use == -INFINITY) ? 0.f : m_use * c;
             const float2 c2 = make_float2(c, c);
             const float2 nmc2 = make_float2(-mc, -mc);
             float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -427,11 +453,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 ml[r] = -INFINITY;
                 ml[kBM + r] = 0.f;
             }
-        } else if (ok) {
+        } else if (ok && n_tiles > 0) {
             ptx::tc_fence_after_sync();
             const float inv_l = 1.f / l;
+            // row of O: batch tb (0 when packed) of S rows, then the sequence
+            // start `base` (0 unless packed)
             uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +
-                             ((static_cast<size_t>(b) * p.S + row) * p.H + h) * p.d_head;
+                             ((static_cast<size_t>(tb) * p.S + base + row) * p.H + h) * p.d_head;
 #pragma unroll 1
             for (int q = 0; q < kWideD / 32; ++q) {
                 uint32_t o[32];
@@ -446,11 +474,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                     v.y = pack2<BF16>(__uint_as_float(o[u * 8 + 2]) * inv_l, __uint_as_float(o[u * 8 + 3]) * inv_l);
                     v.z = pack2<BF16>(__uint_as_float(o[u * 8 + 4]) * inv_l, __uint_as_float(o[u * 8 + 5]) * inv_l);
                     v.w = pack2<BF16>(__uint_as_float(o[u * 8 + 6]) * inv_l, __uint_as_float(o[u * 8 + 7]) * inv_l);
-                    if (row < p.S && col < p.d_head) *reinterpret_cast<uint4*>(orow + col) = v;
+                    if (row < S_b && col < p.d_head) *reinterpret_cast<uint4*>(orow + col) = v;
                 }
             }
-            if (p.lse != nullptr && row < p.S)
-                p.lse[static_cast<size_t>(bh) * p.S + row] = (m_use * c + log2f(l)) * 0.69314718055994530942f;
+            if (p.lse != nullptr && row < S_b) {
+                const size_t li = p.cu_seqlens != nullptr ? static_cast<size_t>(h) * p.total + base + row
+                                                          : static_cast<size_t>(bh) * p.S + row;
+                p.lse[li] = (m_use * c + log2f(l)) * 0.69314718055994530942f;
+            }
         }
     }
 

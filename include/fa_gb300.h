@@ -33,8 +33,8 @@
  *                CTA): the plain and grouped-K/V calls take it (the split
  *                entry points divide every tile's keys into the same number
  *                of chunks when the tiles fill less than three quarters of
- *                the SMs); the packed, windowed and dropout calls return
- *                FA_ERR_UNSUPPORTED there.
+ *                the SMs), and so do the packed and windowed calls
+ *                (unsplit); dropout calls return FA_ERR_UNSUPPORTED there.
  *   LSE        : contiguous fp32 [B, H, S], or NULL to skip writing it.
  *
  * Ownership and ordering: the library keeps no pointer after a call returns
@@ -276,8 +276,8 @@ int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* L
  *     that are not split need no scratch and always run.  On a 152-SM GB300
  *     every split of D <= 64, and of D <= 128 without the causal mask, fits
  *     (at most about 20 MiB); the longest causal splits of 64 < D <= 128 (up
- *     to about 38 MiB, e.g. B = H = 1, S = 4096) are rejected.  D > 128 is
- *     never split.
+ *     to about 38 MiB, e.g. B = H = 1, S = 4096) are rejected.  Every split
+ *     of D > 128 fits (at most one CTA per SM, 132 KiB of partials each).
  *   - The first call on a device looks up the array's device address on that
  *     device (with it current); make that first call before any stream
  *     capture on the device.

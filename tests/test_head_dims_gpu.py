@@ -73,10 +73,11 @@ def test_output_stays_inside_the_tensor(D, split_kv):
                  f"guarded D{D}")
 
 
-@pytest.mark.parametrize("D", [32, 96])
+@pytest.mark.parametrize("D", [32, 96, 192, 256])
 def test_packed_batch_row_stores(D):
     """Packed sequences whose last tiles are stored row by row, with the
-    next sequence's rows right after them."""
+    next sequence's rows right after them (D > 128: the wide kernel, which
+    stores every row itself)."""
     import torch
     import attention_forward_fwd_gb300 as fa
     dtype = _dtype(D)
@@ -176,18 +177,30 @@ def test_wide_peaky_scores_and_guard_bands(dtype):
     assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), Oref, Lref, dtype, "stress D256")
 
 
-def test_wide_unsupported_variants_are_rejected():
+def test_wide_dropout_is_rejected():
     import torch
     import attention_forward_fwd_gb300 as fa
     q = torch.zeros((1, 256, 2, 256), dtype=torch.float16, device="cuda")
     with pytest.raises(fa.FaError):
-        fa.attention_forward(q, q, q, window=(64, -1))
-    with pytest.raises(fa.FaError):
         fa.attention_forward(q, q, q, dropout_p=0.1)
-    cu = torch.tensor([0, 100, 256], dtype=torch.int32, device="cuda")
-    with pytest.raises(fa.FaError):
-        fa.attention_forward_varlen(q[0], q[0], q[0], cu, 156)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("D,window,causal,H_kv", [(256, (300, -1), True, 3), (192, (200, 150), False, 1),
+                                                   (256, (0, 0), False, 3), (136, (129, 40), True, 1)])
+def test_wide_window(D, window, causal, H_kv):
+    """Sliding windows on the wide kernel (D > 128): key-tile ranges per query
+    tile, rows whose first tiles lie wholly outside their window, grouped
+    K/V heads; every element against the oracle."""
+    import attention_forward_fwd_gb300 as fa
+    dtype = "bf16"
+    B, H, S = 2, 3, 1100
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, dtype, "normal", 160 + D + window[0], h_kv=H_kv)
+    q, k, v = (fa_inputs.to_torch(x, dtype).cuda() for x in (qb, kb, vb))
+    o, lse = fa.attention_forward(q, k, v, causal=causal, scale=D ** -0.5, window=window)
+    Oref, Lref = attention_reference(qb, kb, vb, dtype, causal, D ** -0.5, window=window)
+    assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), Oref, Lref, dtype,
+                 f"window {window} D{D} causal={causal}")
 
 
 def test_wide_full_size_sampled_rows():
