@@ -263,7 +263,7 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
 
     q, k, v must be contiguous fp16 or bf16 tensors on the same CUDA device;
     H_kv must divide H (query head h uses K/V head h // (H / H_kv)); D is a
-    multiple of 8 up to 256 (above 128 without dropout).
+    multiple of 8 up to 256.
     ``out`` / ``lse`` may be preallocated ([B, S, H, D] same dtype; [B, H, S]
     fp32), on q's device.  Work is enqueued on ``stream`` (a torch stream or
     a raw handle; default: the current stream) and not waited for.  ``split_kv`` lets the library split the keys of each

@@ -495,11 +495,11 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
 
 // D in (128, 256]: one CTA per (head, 128-row query tile), programmatic
 // dependent launch as the main kernel.
-template <bool BF16>
+template <bool BF16, bool DROP>
 int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
                 int Hkv, int S, int Dh, int causal, float scale, cudaStream_t stream, const SplitPlan& plan,
                 void* workspace, const Options& opt) {
-    auto kern = fa::fa_fwd_wide_kernel<BF16>;
+    auto kern = fa::fa_fwd_wide_kernel<BF16, DROP>;
     constexpr int kSmem = fa::WideSmem::kAlloc;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
@@ -530,6 +530,10 @@ int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE
     p.win_left = opt.win_left;
     p.win_right = opt.win_right;
     p.drop_first_q = opt.drop_first_q;
+    p.drop_seed_lo = static_cast<uint32_t>(opt.seed & 0xffffffffull);
+    p.drop_seed_hi = static_cast<uint32_t>(opt.seed >> 32);
+    p.drop_threshold = opt.drop_threshold;
+    p.drop_inv_keep = opt.drop_inv_keep;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     const size_t ntq = (S + fa::kBM - 1) / fa::kBM;
     // split over keys: max_splits CTAs per query tile, partials in the
@@ -578,11 +582,14 @@ int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, i
                             : FA_ONE(D_, BF16_, NS_, RS_, fa::kPlain))
     const int kd = kernel_dim(D);
     if (kd > 128) {
-        // plain, grouped, packed and windowed calls; packed and windowed ones unsplit
-        if (feat == fa::kDropout || (feat != fa::kPlain && plan.chunk != 0)) return FA_ERR_UNSUPPORTED;
-        return dtype == FA_F16
-                   ? launch_wide<false>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt)
-                   : launch_wide<true>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt);
+        // every variant; only plain calls are split over keys
+        if (feat != fa::kPlain && plan.chunk != 0) return FA_ERR_UNSUPPORTED;
+        const bool drop = feat == fa::kDropout;
+        if (dtype == FA_F16)
+            return drop ? launch_wide<false, true>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt)
+                        : launch_wide<false, false>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt);
+        return drop ? launch_wide<true, true>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt)
+                    : launch_wide<true, false>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt);
     }
     if (dtype == FA_F16) {
         if (kd == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);

@@ -82,7 +82,10 @@ struct WideSmem {
 // group run at about the same
 // time, so each head's K / V comes from DRAM about once, where an order over
 // all heads at once read every head's prefix again in every wave of CTAs.
-template <bool BF16>
+// DROP: attention dropout (the draws of fa_fwd_kernel's dropout variant:
+// Philox4x32-10 blocks with counter (key / 8, row, head, batch) and the seed
+// as key, sixteen-bit draws; kept P scaled by 1 / (1 - p) in the epilogue).
+template <bool BF16, bool DROP>
 __global__ void __launch_bounds__(kWideThreads, 1)
     fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -407,6 +410,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
             for (int q = 0; q < kBN / 32; ++q) {
                 uint32_t pk[16];
+                uint32_t dw[16] = {};   // dropout draws of these 32 keys (two per word)
+                if constexpr (DROP)
+                    philox4x32_10<4>(static_cast<uint32_t>(kv0 + q * 32) >> 3, static_cast<uint32_t>(row),
+                                     static_cast<uint32_t>(h), static_cast<uint32_t>(b), p.drop_seed_lo,
+                                     p.drop_seed_hi, dw);
 #pragma unroll
                 for (int kq = 0; kq < 16; ++kq) {
                     const float2 xv = __ffma2_rn(make_float2(__uint_as_float(s[q * 32 + 2 * kq]),
@@ -414,7 +422,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                                                  c2, nmc2);
                     const float2 pp = make_float2(ptx::ex2_approx(xv.x), ptx::ex2_approx(xv.y));
                     sum2[kq & 1] = __fadd2_rn(sum2[kq & 1], pp);
-                    pk[kq] = pack2<BF16>(pp.x, pp.y);
+                    pk[kq] = pack_p<DROP ? kDropout : kPlain, BF16>(p, pp, dw[kq]);
                 }
                 ptx::tmem_st_32x32b_x16(tS + q * 16, pk);
             }
@@ -455,7 +463,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             }
         } else if (ok && n_tiles > 0) {
             ptx::tc_fence_after_sync();
-            const float inv_l = 1.f / l;
+            float inv_l = 1.f / l;
+            if constexpr (DROP) inv_l *= p.drop_inv_keep;   // kept P scaled by 1 / (1 - p)
             // row of O: batch tb (0 when packed) of S rows, then the sequence
             // start `base` (0 unless packed)
             uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +

@@ -33,8 +33,8 @@
  *                CTA): the plain and grouped-K/V calls take it (the split
  *                entry points divide every tile's keys into the same number
  *                of chunks when the tiles fill less than three quarters of
- *                the SMs), and so do the packed and windowed calls
- *                (unsplit); dropout calls return FA_ERR_UNSUPPORTED there.
+ *                the SMs), and so do the packed, windowed and dropout
+ *                calls (unsplit).
  *   LSE        : contiguous fp32 [B, H, S], or NULL to skip writing it.
  *
  * Ownership and ordering: the library keeps no pointer after a call returns

@@ -79,7 +79,7 @@ def _assert_dropout_close(O, L, Oref, Lref, A, dtype, what):
 
 @pytest.mark.parametrize("p", [0.1, 0.5, 0.9])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D,dtype", [(64, "f16"), (128, "bf16")])
+@pytest.mark.parametrize("D,dtype", [(64, "f16"), (128, "bf16"), (256, "bf16"), (192, "f16")])
 def test_dropout_matches_oracle(p, causal, D, dtype):
     """Several query and key tiles with a ragged tail, grouped K/V heads."""
     B, H, H_kv, S = 2, 4, 2, 333
@@ -91,7 +91,7 @@ def test_dropout_matches_oracle(p, causal, D, dtype):
     _assert_dropout_close(O, L, Oref, Lref, A, dtype, f"p={p} causal={causal} D{D}")
 
 
-@pytest.mark.parametrize("D,dtype", [(64, "f16"), (128, "bf16")])
+@pytest.mark.parametrize("D,dtype", [(64, "f16"), (128, "bf16"), (256, "bf16")])
 def test_dropout_peaky_scores_several_items_per_cta(D, dtype):
     """More work items than SMs and peaky scores (the reference max moves)."""
     B, H, S = 3, 8, 1999
@@ -102,7 +102,7 @@ def test_dropout_peaky_scores_several_items_per_cta(D, dtype):
     _assert_dropout_close(O, L, Oref, Lref, A, dtype, f"stress D{D}")
 
 
-@pytest.mark.parametrize("D,dtype", [(64, "f16"), (128, "bf16")])
+@pytest.mark.parametrize("D,dtype", [(64, "f16"), (128, "bf16"), (256, "bf16")])
 @pytest.mark.parametrize("causal", [False, True])
 def test_zero_probability_is_the_plain_forward_bit_for_bit(D, dtype, causal):
     import torch
@@ -126,7 +126,7 @@ def test_zero_probability_is_the_plain_forward_bit_for_bit(D, dtype, causal):
 
 # 1 / (1 - p) is a power of two for these p, so the read-back is exact
 @pytest.mark.parametrize("D,dtype,p", [(64, "f16", 0.5), (128, "bf16", 0.5), (128, "bf16", 0.75),
-                                       (64, "f16", 0.875)])
+                                       (64, "f16", 0.875), (256, "bf16", 0.5)])
 def test_mask_read_back_bit_exact(D, dtype, p):
     """Q = 0 makes every visible probability 1/S; a V whose key j carries a 1
     in column j - c*D only (block c) turns O(1 - p) S into the keep bits of

@@ -177,15 +177,6 @@ def test_wide_peaky_scores_and_guard_bands(dtype):
     assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), Oref, Lref, dtype, "stress D256")
 
 
-def test_wide_dropout_is_rejected():
-    import torch
-    import attention_forward_fwd_gb300 as fa
-    q = torch.zeros((1, 256, 2, 256), dtype=torch.float16, device="cuda")
-    with pytest.raises(fa.FaError):
-        fa.attention_forward(q, q, q, dropout_p=0.1)
-    torch.cuda.synchronize()
-
-
 @pytest.mark.parametrize("D,window,causal,H_kv", [(256, (300, -1), True, 3), (192, (200, 150), False, 1),
                                                    (256, (0, 0), False, 3), (136, (129, 40), True, 1)])
 def test_wide_window(D, window, causal, H_kv):
