@@ -2,6 +2,8 @@
 import numpy as np
 
 import fa_inputs
+from oracle import dropout_keep
+from oracle.attention import decode
 
 TOL_O = {"f16": 2e-3, "bf16": 8e-3}
 
@@ -73,3 +75,39 @@ def assert_bare_tolerance(O, Oref, dtype, what=""):
     assert sel.any(), f"{what}: no element with a half ulp below 1e-4"
     dO = np.abs(O - Oref)[sel]
     assert dO.max() <= TOL_O[dtype], f"{what}: max|dO| = {dO.max():.3e} on {sel.sum()} small elements"
+
+
+# Dropout: the kernel rounds each kept P_ij to 16 bits (unit roundoff U16)
+# before the 1 / (1 - p) scale, so element (i, d) may move by up to
+# U16 * sum_j keep_ij P_ij |V_jd| / (1 - p) on top of the forward's error
+# (twice that is allowed, for the exponential's own error).
+U16 = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}
+
+
+def abs_weights(qb, kb, vb, dtype, causal, scale, p, seed):
+    """A[b, i, h, d] = sum_j keep_bhij P_bhij |V_bjd| / (1 - p) in fp64 (the
+    oracle's probabilities and mask): the size of the sum whose terms the
+    16-bit rounding of P perturbs."""
+    q, k, v = decode(qb, dtype), decode(kb, dtype), decode(vb, dtype)
+    B, S, H, _ = q.shape
+    group = H // k.shape[2]
+    keep = dropout_keep(B, H, S, p, seed)
+    A = np.empty(q.shape[:3] + (v.shape[3],))
+    vis = np.tril(np.ones((S, S), dtype=bool)) if causal else np.ones((S, S), dtype=bool)
+    for b in range(B):
+        for h in range(H):
+            z = np.where(vis, scale * (q[b, :, h, :] @ k[b, :, h // group, :].T), -np.inf)
+            e = np.exp(z - z.max(axis=1, keepdims=True))
+            P = e / e.sum(axis=1, keepdims=True)
+            A[b, :, h, :] = (P * keep[b, h]) @ np.abs(v[b, :, h // group, :]) / (1.0 - p)
+    return A
+
+
+def assert_dropout_close(O, L, Oref, Lref, A, dtype, what):
+    assert np.all(np.isfinite(O)), f"{what}: non-finite O"
+    dO = np.abs(O - Oref)
+    bound = TOL_O[dtype] + half_ulp(Oref, dtype) + 2.0 * U16[dtype] * A
+    bad = dO > bound
+    assert not bad.any(), f"{what}: max|dO| = {dO.max():.3e} at {np.unravel_index(dO.argmax(), dO.shape)}"
+    dL = np.abs(L - Lref)
+    assert not (dL > lse_tol(Lref)).any(), f"{what}: |dLSE| = {dL.max():.3e}"

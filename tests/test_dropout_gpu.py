@@ -19,10 +19,7 @@ import fa_inputs
 from oracle import attention_reference_dropout, dropout_keep
 from oracle.attention import decode
 
-from gpu_common import half_ulp, lse_tol, TOL_O
-
-# unit roundoff of the 16-bit P
-U16 = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}
+from gpu_common import abs_weights as _abs_weights, assert_dropout_close as _assert_dropout_close
 
 pytestmark = pytest.mark.gpu
 
@@ -46,35 +43,6 @@ def _run(qb, kb, vb, dtype, causal, scale, p, seed):
     o, lse = fa.attention_forward(q, k, v, causal=causal, scale=scale, dropout_p=p, seed=seed)
     torch.cuda.synchronize()
     return o.double().cpu().numpy(), lse.double().cpu().numpy()
-
-
-def _abs_weights(qb, kb, vb, dtype, causal, scale, p, seed):
-    """A[b, i, h, d] = sum_j keep_bhij P_bhij |V_bjd| / (1 - p) in fp64 (the
-    oracle's probabilities and mask): the size of the sum whose terms the
-    16-bit rounding of P perturbs."""
-    q, k, v = decode(qb, dtype), decode(kb, dtype), decode(vb, dtype)
-    B, S, H, _ = q.shape
-    group = H // k.shape[2]
-    keep = dropout_keep(B, H, S, p, seed)
-    A = np.empty(q.shape[:3] + (v.shape[3],))
-    vis = np.tril(np.ones((S, S), dtype=bool)) if causal else np.ones((S, S), dtype=bool)
-    for b in range(B):
-        for h in range(H):
-            z = np.where(vis, scale * (q[b, :, h, :] @ k[b, :, h // group, :].T), -np.inf)
-            e = np.exp(z - z.max(axis=1, keepdims=True))
-            P = e / e.sum(axis=1, keepdims=True)
-            A[b, :, h, :] = (P * keep[b, h]) @ np.abs(v[b, :, h // group, :]) / (1.0 - p)
-    return A
-
-
-def _assert_dropout_close(O, L, Oref, Lref, A, dtype, what):
-    assert np.all(np.isfinite(O)), f"{what}: non-finite O"
-    dO = np.abs(O - Oref)
-    bound = TOL_O[dtype] + half_ulp(Oref, dtype) + 2.0 * U16[dtype] * A
-    bad = dO > bound
-    assert not bad.any(), f"{what}: max|dO| = {dO.max():.3e} at {np.unravel_index(dO.argmax(), dO.shape)}"
-    dL = np.abs(L - Lref)
-    assert not (dL > lse_tol(Lref)).any(), f"{what}: |dLSE| = {dL.max():.3e}"
 
 
 @pytest.mark.parametrize("p", [0.1, 0.5, 0.9])
