@@ -76,14 +76,15 @@ def test_varlen_equal_lengths_match_the_batched_call_bitwise(S, D, dtype):
         assert torch.equal(lv.view(H, B, S).permute(1, 0, 2), lse)
 
 
-def test_varlen_bad_offsets_are_reported_and_nothing_is_written_outside():
+@pytest.mark.parametrize("D", [64, 256])
+def test_varlen_bad_offsets_are_reported_and_nothing_is_written_outside(D):
     """A sequence reaching past the packed tensors, and one longer than
     max_seqlen, are skipped and reported; the rest is computed, nothing is
     written outside the tensors (guard bands), the skipped rows keep their
-    previous contents."""
+    previous contents (D = 256: the wide kernel)."""
     import torch
     import attention_forward_fwd_gb300 as fa
-    H, D, total = 2, 64, 400
+    H, total = 2, 400
     qb, kb, vb, _ = fa_inputs.make_varlen([total], H, D, "f16", "normal", 64)
     q, k, v = (fa_inputs.to_torch(x, "f16").cuda() for x in (qb, kb, vb))
     guard = 4096
@@ -94,12 +95,12 @@ def test_varlen_bad_offsets_are_reported_and_nothing_is_written_outside():
         lse = lbuf[64:64 + H * total].view(H, total)
         cu = torch.tensor(cu_list, dtype=torch.int32, device="cuda")
         fa.fa_device_status(clear=True)
-        fa.attention_forward_varlen(q, k, v, cu, ms, causal=True, out=o, lse=lse)
+        fa.attention_forward_varlen(q, k, v, cu, ms, causal=True, scale=D ** -0.5, out=o, lse=lse)
         assert fa.fa_device_status(clear=True) == fa.FA_ERR_BAD_SEQLENS
         assert torch.all(buf[:guard] == 7.0) and torch.all(buf[guard + total * H * D:] == 7.0)
         assert torch.all(lbuf[:64] == 3.0) and torch.all(lbuf[64 + H * total:] == 3.0)
         assert torch.all(o[100:] == 7.0) and torch.all(lse[:, 100:] == 3.0)
         good = np.array([0, 100], dtype=np.int32)
-        Oref, Lref = attention_reference_varlen(qb[:100], kb[:100], vb[:100], good, "f16", True, 0.125)
+        Oref, Lref = attention_reference_varlen(qb[:100], kb[:100], vb[:100], good, "f16", True, D ** -0.5)
         assert_close(o[:100].double().cpu().numpy(), lse[:, :100].double().cpu().numpy(), Oref, Lref,
-                     "f16", "varlen good part")
+                     "f16", f"varlen good part D{D}")
