@@ -70,6 +70,24 @@ def test_wide_kernel_splits_every_tile_alike(S, causal):
     assert set(full) == {1} and items_full == (4096 + 255) // 256
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_wide_splits_fit_the_static_scratch(causal):
+    """Every split plan of the wide kernel keeps at most one CTA per SM, so
+    its partials (128 x 256 fp32 values plus m and l per CTA) fit the static
+    entry point's 24 MiB scratch, whatever the shape."""
+    worst = 0
+    for B in (1, 2, 3):
+        for H in (1, 2, 3, 5, 8):
+            for S in (129, 256, 1000, 2048, 4096, 8192, 16384):
+                splits, items = fa.fa_split_plan(B, H, S, 256, causal, SMS)
+                if max(splits) == 1:
+                    continue
+                ctas = B * H * items
+                assert ctas <= SMS
+                worst = max(worst, ctas * (128 * 256 + 2 * 128) * 4)
+    assert 0 < worst <= 24 << 20
+
+
 def test_ragged_last_wave_is_split():
     """B3 H8 S1999 non-causal: 192 equal blocks on 152 SMs leave a second
     wave of 40; splitting some blocks shortens the schedule."""
