@@ -101,13 +101,12 @@ static_assert(fa::kStatusTimeout == FA_ERR_TIMEOUT && fa::kStatusBadSeqlens == F
               "device status codes");
 
 // Head dimensions the library takes: multiples of 8 up to 256 (the row
-// strides of the tensor maps must be multiples of 16 bytes).  D = 64, 128
-// and 256 run at full width; any other runs on the next kernel up, whose
+// strides of the tensor maps must be multiples of 16 bytes).  D = 64, 128,
+// 192 and 256 run at full width; any other runs on the next kernel up, whose
 // extra columns the tensor maps read as zeros.  D > 128 has a kernel of its
-// own (one query tile per CTA), without the key split or the packed,
-// windowed and dropout variants.
+// own (fa_fwd_wide_kernel, one query tile per CTA, at width 192 or 256).
 bool supported_dim(int D) { return D >= 8 && D <= fa::kWideD && D % 8 == 0; }
-int kernel_dim(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : fa::kWideD; }
+int kernel_dim(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : fa::wide_dim(D); }
 
 // Cost model of the multi-wave split plans (plan_split_uncached), in key
 // steps: an item's cost beyond its key tiles, and the merge's.
@@ -374,10 +373,11 @@ struct Options {
 template <int D, bool BF16>
 int launch_combine(const fa::FwdParams& p, void* O, int B, int H, size_t ntq, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    constexpr int kPerTile = fa::kBM / (fa::kCombineThreads / (D / 8));
+    constexpr int kThreads = fa::combine_threads(D);
+    constexpr int kPerTile = fa::kBM / (kThreads / (D / 8));
     cfg.gridDim = dim3(static_cast<unsigned>(ntq * kPerTile),
                        static_cast<unsigned>(B) * static_cast<unsigned>(H));
-    cfg.blockDim = dim3(fa::kCombineThreads);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -493,14 +493,14 @@ int validate(const void* Q, const void* K, const void* V, void* O, const float* 
     return FA_OK;
 }
 
-// D in (128, 256]: one CTA per (head, 128-row query tile), programmatic
-// dependent launch as the main kernel.
-template <bool BF16, bool DROP>
+// D in (128, 256]: one CTA per (head, 128-row query tile) at width 192 or
+// 256, programmatic dependent launch as the main kernel.
+template <int D, bool BF16, bool DROP>
 int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
                 int Hkv, int S, int Dh, int causal, float scale, cudaStream_t stream, const SplitPlan& plan,
                 void* workspace, const Options& opt) {
-    auto kern = fa::fa_fwd_wide_kernel<BF16, DROP>;
-    constexpr int kSmem = fa::WideSmem::kAlloc;
+    auto kern = fa::fa_fwd_wide_kernel<D, BF16, DROP>;
+    constexpr int kSmem = fa::WideSmem<D>::kAlloc;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
@@ -542,7 +542,7 @@ int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE
     p.max_splits = plan.chunk ? plan.max_splits : 1;
     p.nqb = (S + fa::kQTiles * fa::kBM - 1) / (fa::kQTiles * fa::kBM);
     if (plan.chunk) {
-        const size_t o_floats = static_cast<size_t>(B) * H * ntq * plan.max_splits * fa::kBM * fa::kWideD;
+        const size_t o_floats = static_cast<size_t>(B) * H * ntq * plan.max_splits * fa::kBM * D;
         p.ws_o = static_cast<float*>(workspace);
         p.ws_ml = static_cast<float*>(workspace) + o_floats;
         std::copy(plan.ns, plan.ns + fa::kMaxSplitBlocks, p.block_splits);
@@ -561,7 +561,7 @@ int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) != cudaSuccess) return FA_ERR_CUDA;
     if (plan.chunk == 0) return FA_OK;
-    return launch_combine<fa::kWideD, BF16>(p, O, B, H, ntq, stream);
+    return launch_combine<D, BF16>(p, O, B, H, ntq, stream);
 }
 
 int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Hkv,
@@ -585,11 +585,12 @@ int dispatch(const void* Q, const void* K, const void* V, void* O, float* LSE, i
         // every variant; only plain calls are split over keys
         if (feat != fa::kPlain && plan.chunk != 0) return FA_ERR_UNSUPPORTED;
         const bool drop = feat == fa::kDropout;
-        if (dtype == FA_F16)
-            return drop ? launch_wide<false, true>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt)
-                        : launch_wide<false, false>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt);
-        return drop ? launch_wide<true, true>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt)
-                    : launch_wide<true, false>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt);
+#define FA_WIDE(D_, BF16_)                                                                              \
+    (drop ? launch_wide<D_, BF16_, true>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt) \
+          : launch_wide<D_, BF16_, false>(Q, K, V, O, LSE, B, H, Hkv, S, D, causal, scale, st, plan, ws, opt))
+        if (dtype == FA_F16) return kd == 192 ? FA_WIDE(192, false) : FA_WIDE(256, false);
+        return kd == 192 ? FA_WIDE(192, true) : FA_WIDE(256, true);
+#undef FA_WIDE
     }
     if (dtype == FA_F16) {
         if (kd == 64) return FA_LAUNCH(64, false, kRingD64, kRowSplitD64);

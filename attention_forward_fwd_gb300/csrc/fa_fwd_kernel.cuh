@@ -1443,7 +1443,7 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
 // M = max_s m_s, l = sum_s l_s 2^(m_s - M), O = sum_s o~_s 2^(m_s - M) / l and
 // LSE = ln2 (M + log2 l) -- the same rescaling by alpha = exp(m_old - m_new)
 // as the online update of section 沿 C fragment 做 Online Softmax, applied
-// across splits instead of across tiles.  A CTA covers kCombineThreads / (D/8) rows of
+// across splits instead of across tiles.  A CTA covers combine_threads(D) / (D/8) rows of
 // one query tile of one (b, h); thread (r, c) produces the 8 outputs of row r,
 // columns [8c, 8c+8).  Launched as a programmatic dependent of the main
 // kernel: it waits for that grid to complete before reading its partials.
@@ -1454,12 +1454,16 @@ __global__ void __launch_bounds__(Roles<RS>::kThreads, 1)
 #endif
 constexpr int kCombineThreads = FA_COMBINE_THREADS;
 constexpr int kCombineMaxSplits = 16;   // weights kept in registers up to this
+// threads per CTA for width D: a whole number of rows of D / 8 chunks, and a
+// whole number of CTAs per 128-row tile (D = 192: 24 chunks, 8 rows)
+__host__ __device__ constexpr int combine_threads(int D) { return D == 192 ? 192 : kCombineThreads; }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kCombineThreads) fa_combine_kernel(const FwdParams p, void* O) {
+__global__ void __launch_bounds__(combine_threads(D)) fa_combine_kernel(const FwdParams p, void* O) {
     constexpr int kCols = D / 8;                        // 8-column chunks per row
-    constexpr int kRows = kCombineThreads / kCols;      // rows per CTA
+    constexpr int kRows = combine_threads(D) / kCols;   // rows per CTA
     constexpr int kPerTile = kBM / kRows;               // CTAs per query tile
+    static_assert(combine_threads(D) % kCols == 0 && kBM % kRows == 0, "combine CTA shape");
     const int qt = blockIdx.x / kPerTile;
     const int bh = blockIdx.y;
     const int ns = p.block_splits[qt / kQTiles];

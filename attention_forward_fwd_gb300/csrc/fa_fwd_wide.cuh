@@ -4,15 +4,16 @@
 // 拆解 Layout、TiledCopy 与 TiledMMA": S = Q K^T (section 先看全局), the online
 // softmax with the O correction (section 沿 C fragment 做 Online Softmax), the
 // second product P V (section V 的转置只发生在视图里) and the O + LSE epilogue
-// (section 第二次 GEMM 与输出 Epilogue)), laid out for a 256-wide head: one
-// 128-row query tile per CTA, so that its S (128 columns) and O (256 columns)
-// fit in tensor memory: S in two buffers (columns [0, 128) and [384, 512)),
-// P written over its S, O in [128, 384).  Shared memory holds the Q tile
-// (4 boxes of 64 columns, 64 KiB) and two 64 KiB slots: K(j) in one, V(j) in
-// the other.  The tensor pipe runs S(0), S(1), P V(0), S(2), P V(1), ...:
-// S(j+1) overlaps the softmax of tile j.  S(j) is issued after P V(j-2), so
-// when S(j) is complete the P V that last read its buffer is too; O may be
-// rescaled once P V(j-1) has reported on its own barrier.
+// (section 第二次 GEMM 与输出 Epilogue)), laid out for a wide head of D = 192
+// or 256 columns: one 128-row query tile per CTA, so that its S (128 columns)
+// and O (D columns) fit in tensor memory: S in two buffers (columns [0, 128)
+// and [384, 512)), P written over its S, O in [128, 128 + D).  Shared memory
+// holds the Q tile (D / 64 boxes of 64 columns) and two slots of the same
+// size: K(j) in one, V(j) in the other.  The tensor pipe runs S(0), S(1),
+// P V(0), S(2), P V(1), ...: S(j+1) overlaps the softmax of tile j.  S(j) is
+// issued after P V(j-2), so when S(j) is complete the P V that last read its
+// buffer is too; O may be rescaled once P V(j-1) has reported on its own
+// barrier.
 //
 // Warps 0-3: softmax, thread = query row = TMEM lane.  Warp 4: TMEM
 // allocation and MMA issue (converged warp, one elected lane).  Warp 5: TMA
@@ -25,12 +26,13 @@
 
 namespace fa {
 
-constexpr int kWideD = 256;
+constexpr int kWideD = 256;        // the widest head the library takes
 constexpr int kWideThreads = 192;
-constexpr int kWideAtoms = kWideD / 64;                 // 64-column boxes per row
-constexpr int kWideTileBytes = kBM * kWideD * 2;        // one 128 x 256 16-bit tile
-constexpr uint32_t kWideTmemCols = 512;   // S/P buffers [0, 128) and [384, 512), O [128, 384)
+constexpr int kWideAtoms = kWideD / 64;   // 64-column boxes per row, at most
+constexpr uint32_t kWideTmemCols = 512;   // S/P buffers [0, 128) and [384, 512), O [128, 128 + D)
 constexpr uint32_t kWideS1 = 384;         // column of the second S/P buffer
+// the kernel's width for a head of Dh columns (136 .. 256)
+__host__ __device__ constexpr int wide_dim(int Dh) { return Dh <= 192 ? 192 : 256; }
 // K and V bytes of the heads whose CTAs are ordered together (a share of the
 // 126 MB L2, leaving room for the next group and the Q / O traffic).  Causal
 // calls take larger groups: their query tiles differ in cost, and a group
@@ -68,10 +70,15 @@ struct WideBars {
     int abort;
 };
 
+template <int D>
 struct WideSmem {
+    static_assert(D == 192 || D == 256, "wide head widths");
+    static_assert(kBN + D <= static_cast<int>(kWideS1), "O overlaps the second S/P buffer");
+    static constexpr int kAtoms = D / 64;              // 64-column boxes per row
+    static constexpr int kTileBytes = kBM * D * 2;     // one 128 x D 16-bit tile
     static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kWideTileBytes;
-    static constexpr int kOffBar = kOffKV + 2 * kWideTileBytes;
+    static constexpr int kOffKV = kTileBytes;
+    static constexpr int kOffBar = kOffKV + 2 * kTileBytes;
     static constexpr int kAlloc = kOffBar + static_cast<int>(sizeof(WideBars)) + 1024;
     static_assert(kAlloc <= 232448, "shared memory beyond the 227 KiB a CTA may use");
 };
@@ -85,7 +92,7 @@ struct WideSmem {
 // DROP: attention dropout (the draws of fa_fwd_kernel's dropout variant:
 // Philox4x32-10 blocks with counter (key / 8, row, head, batch) and the seed
 // as key, sixteen-bit draws; kept P scaled by 1 / (1 - p) in the epilogue).
-template <bool BF16, bool DROP>
+template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(kWideThreads, 1)
     fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -93,7 +100,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = ptx::smem_addr(smem);
-    WideBars* bars = reinterpret_cast<WideBars*>(smem + WideSmem::kOffBar);
+    using L = WideSmem<D>;
+    constexpr int kAtoms = L::kAtoms;
+    constexpr int kTileBytes = L::kTileBytes;
+    WideBars* bars = reinterpret_cast<WideBars*>(smem + L::kOffBar);
     volatile int* abort_flag = &bars->abort;
     auto bar = [&](const uint64_t* b) { return ptx::smem_addr(b); };
     const int warp = threadIdx.x >> 5;
@@ -157,7 +167,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             ptx::mbar_init(bar(&bars->kv_full[s]), 1);
             ptx::mbar_init(bar(&bars->kv_empty[s]), 1);
         }
-        for (int c = 0; c < kWideAtoms; ++c) {
+        for (int c = 0; c < kAtoms; ++c) {
             ptx::mbar_init(bar(&bars->kbox_full[c]), 1);
             ptx::mbar_init(bar(&bars->kbox_empty[c]), 1);
         }
@@ -191,11 +201,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (warp == 5) {
         // ---------------------------------------------------- TMA producer
         ptx::grid_dependency_wait();   // the previous kernel may write Q, K, V
-        const uint32_t q_dst = sbase + WideSmem::kOffQ;
-        const uint32_t slot0 = sbase + WideSmem::kOffKV;
+        const uint32_t q_dst = sbase + L::kOffQ;
+        const uint32_t slot0 = sbase + L::kOffKV;
         auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int head, int row0) {
-            ptx::mbar_arrive_expect_tx(full, kWideTileBytes);
-            for (int c = 0; c < kWideAtoms; ++c)
+            ptx::mbar_arrive_expect_tx(full, kTileBytes);
+            for (int c = 0; c < kAtoms; ++c)
                 ptx::tma_load_4d(dst + c * (kBM * 128), map, full, c * 64, head, base + row0, tb);
         };
         if (lane == 0 && n_tiles > 0) {
@@ -207,17 +217,17 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         // empty barrier).
         bool ok = true;
         int nk = 0, nv = 0;   // K / V tiles issued
-        int nkb[kWideAtoms] = {};   // per-box mode: boxes of K issued
+        int nkb[kAtoms] = {};   // per-box mode: boxes of K issued
         auto load_k = [&](int i) {
             if constexpr (FA_WIDE_KBOX != 0) {
 #pragma unroll 1
-                for (int c = 0; c < kWideAtoms; ++c) {
+                for (int c = 0; c < kAtoms; ++c) {
                     const uint32_t full = bar(&bars->kbox_full[c]);
                     if (i > 0 &&
                         !(ok = wait_warp(bar(&bars->kbox_empty[c]), static_cast<uint32_t>((i - 1) & 1))))
                         return;
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(full, kWideTileBytes / kWideAtoms);
+                        ptx::mbar_arrive_expect_tx(full, kTileBytes / kAtoms);
                         ptx::tma_load_4d(slot0 + c * (kBN * 128), &tmK, full, c * 64, hkv, base + (jb + i) * kBN, tb);
                     }
                     ++nkb[c];
@@ -230,7 +240,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         };
         auto load_v = [&](int i) {
             if (i > 0 && !(ok = wait_warp(bar(&bars->kv_empty[1]), static_cast<uint32_t>((i - 1) & 1)))) return;
-            if (lane == 0) load_tile(&tmV, slot0 + kWideTileBytes, bar(&bars->kv_full[1]), hkv, (jb + i) * kBN);
+            if (lane == 0) load_tile(&tmV, slot0 + kTileBytes, bar(&bars->kv_full[1]), hkv, (jb + i) * kBN);
             ++nv;
         };
         if (n_tiles > 0) load_k(0);
@@ -246,7 +256,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             if (n_tiles > 0) wait_warp(bar(&bars->q_full), 0, false);
             if (FA_WIDE_KBOX == 0 && nk > 0)
                 wait_warp(bar(&bars->kv_full[0]), static_cast<uint32_t>((nk - 1) & 1), false);
-            for (int c = 0; c < kWideAtoms; ++c)
+            for (int c = 0; c < kAtoms; ++c)
                 if (FA_WIDE_KBOX != 0 && nkb[c] > 0)
                     wait_warp(bar(&bars->kbox_full[c]), static_cast<uint32_t>((nkb[c] - 1) & 1), false);
             if (nv > 0) wait_warp(bar(&bars->kv_full[1]), static_cast<uint32_t>((nv - 1) & 1), false);
@@ -254,24 +264,24 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     } else if (warp == 4) {
         // ------------------------------------------------------ MMA issue
         constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
-        constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, kWideD, BF16, true);
-        const uint32_t slot0 = sbase + WideSmem::kOffKV;
+        constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, D, BF16, true);
+        const uint32_t slot0 = sbase + L::kOffKV;
         bool ok = n_tiles == 0 || wait_warp(bar(&bars->q_full), 0);
-        const uint64_t qd = ptx::sdesc_sw128(sbase + WideSmem::kOffQ, 16, 1024);
+        const uint64_t qd = ptx::sdesc_sw128(sbase + L::kOffQ, 16, 1024);
         const uint64_t kd = ptx::sdesc_sw128(slot0, 16, 1024);
-        const uint64_t vd = ptx::sdesc_sw128(slot0 + kWideTileBytes, kBN * 128, 1024);
-        // S(i) into buffer i % 2: Q K(i)^T over the 256 columns, K=16 steps
-        // through the four 64-column boxes (32 bytes per step inside a box)
+        const uint64_t vd = ptx::sdesc_sw128(slot0 + kTileBytes, kBN * 128, 1024);
+        // S(i) into buffer i % 2: Q K(i)^T over the D columns, K=16 steps
+        // through the D / 64 boxes of 64 columns (32 bytes per step inside a box)
         auto issue_s = [&](int i) {
             const uint32_t d = tmem + ((i & 1) ? kWideS1 : 0u);
             if constexpr (FA_WIDE_KBOX != 0) {
                 // box by box: wait for box c of K(i), run its four K steps, and
                 // hand the box back to the producer once they have run
                 const uint32_t hi = ptx::sdesc_sw128_hi(1024);
-                const uint32_t qlo = ptx::sdesc_sw128_lo(sbase + WideSmem::kOffQ, 16);
+                const uint32_t qlo = ptx::sdesc_sw128_lo(sbase + L::kOffQ, 16);
                 const uint32_t klo = ptx::sdesc_sw128_lo(slot0, 16);
 #pragma unroll
-                for (int c = 0; c < kWideAtoms; ++c) {
+                for (int c = 0; c < kAtoms; ++c) {
                     if (!(ok = wait_warp(bar(&bars->kbox_full[c]), static_cast<uint32_t>(i & 1)))) return;
                     ptx::tc_fence_after_sync();
                     ptx::mma_ss_x4_lo(d, qlo + c * (kBM * 128 / 16), klo + c * (kBN * 128 / 16), hi, 2u,
@@ -286,15 +296,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             if constexpr (FA_MMA_BATCH != 0) {
                 // four K steps (one 64-column box) per election
                 const uint32_t hi = ptx::sdesc_sw128_hi(1024);
-                const uint32_t qlo = ptx::sdesc_sw128_lo(sbase + WideSmem::kOffQ, 16);
+                const uint32_t qlo = ptx::sdesc_sw128_lo(sbase + L::kOffQ, 16);
                 const uint32_t klo = ptx::sdesc_sw128_lo(slot0, 16);
 #pragma unroll
-                for (int c = 0; c < kWideAtoms; ++c)
+                for (int c = 0; c < kAtoms; ++c)
                     ptx::mma_ss_x4_lo(d, qlo + c * (kBM * 128 / 16), klo + c * (kBN * 128 / 16), hi, 2u,
                                       kIdescQK, c > 0 ? 1u : 0u);
             } else {
 #pragma unroll
-                for (int kk = 0; kk < kWideD / 16; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
                     ptx::mma_ss_warp(d, qd + (off >> 4), kd + (off >> 4), kIdescQK, kk > 0);
                 }
@@ -317,7 +327,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             const uint32_t pa = tmem + ((j & 1) ? kWideS1 : 0u);
             if constexpr (FA_MMA_BATCH != 0) {
                 const uint32_t hi = ptx::sdesc_sw128_hi(1024);
-                const uint32_t vlo = ptx::sdesc_sw128_lo(slot0 + kWideTileBytes, kBN * 128);
+                const uint32_t vlo = ptx::sdesc_sw128_lo(slot0 + kTileBytes, kBN * 128);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; kk += 4)
                     ptx::mma_ts_x4_lo(tmem + kBN, pa + kk * 8, vlo + kk * (16 * 128 / 16), hi, 8u,
@@ -341,7 +351,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         const int row = r0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
         const uint32_t tS0 = tmem + lane_off;            // S(j), then P(j) over it, buffer j % 2
-        const uint32_t tO = tmem + lane_off + kBN;       // O, 256 columns
+        const uint32_t tO = tmem + lane_off + kBN;       // O, D columns
         const float c = p.scale_log2;
         float m_use = -INFINITY;
         float l = 0.f;
@@ -391,7 +401,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 if (!ok) break;
                 ptx::tc_fence_after_sync();
 #pragma unroll 1
-                for (int q = 0; q < kWideD / 32; ++q) {
+                for (int q = 0; q < D / 32; ++q) {
                     uint32_t o[32];
                     ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
                     ptx::tmem_ld_wait();
@@ -441,11 +451,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             // row); a split with no key records l = 0 and m = -inf
             const size_t slot = partial_slot(bh, ntq, qt, p.max_splits, split);
             float* ml = p.ws_ml + slot * (2 * kBM);
-            float4* po = reinterpret_cast<float4*>(p.ws_o + slot * static_cast<size_t>(kBM * kWideD));
+            float4* po = reinterpret_cast<float4*>(p.ws_o + slot * static_cast<size_t>(kBM * D));
             if (ok && n_tiles > 0) {
                 ptx::tc_fence_after_sync();
 #pragma unroll 1
-                for (int q = 0; q < kWideD / 32; ++q) {
+                for (int q = 0; q < D / 32; ++q) {
                     uint32_t o[32];
                     ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
                     ptx::tmem_ld_wait();
@@ -470,7 +480,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +
                              ((static_cast<size_t>(tb) * p.S + base + row) * p.H + h) * p.d_head;
 #pragma unroll 1
-            for (int q = 0; q < kWideD / 32; ++q) {
+            for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
                 ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
                 ptx::tmem_ld_wait();

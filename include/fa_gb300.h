@@ -21,8 +21,8 @@
  * Memory layout (all buffers are caller-owned DEVICE memory):
  *   Q, K, V, O : contiguous [B, S, H, D], element type fp16 or bf16 (all four
  *                the same), D a multiple of 8 from 8 to 256; base addresses
- *                16-byte aligned.  D = 64, 128 and 256 run at full width; any
- *                other D runs on the kernel of the next of the three (the page
+ *                16-byte aligned.  D = 64, 128, 192 and 256 run at full
+ *                width; any other D runs on the next kernel up (the page
  *                "CuTe 详解：以 FlashAttention-2 拆解 Layout、TiledCopy 与
  *                TiledMMA" lists other head dimensions among a production
  *                FA2's needs, section 哪些结论可以迁移，哪些只是本例特例): its
@@ -30,7 +30,7 @@
  *                rest as zeros and the O stores leave it out, and the tensor
  *                cores do that padded work (a D = 96 call costs a D = 128 one).
  *                D > 128 has a kernel of its own (one 128-row query tile per
- *                CTA): the plain and grouped-K/V calls take it (the split
+ *                CTA, 192 or 256 columns wide): the plain and grouped-K/V calls take it (the split
  *                entry points divide every tile's keys into the same number
  *                of chunks when the tiles fill less than three quarters of
  *                the SMs), and so do the packed, windowed and dropout

@@ -62,6 +62,7 @@ SPLITKV = [
     (2, 4, 2, 777, 128, "bf16", False, "normal"),    # grouped K/V heads
     (2, 16, 16, 2048, 128, "bf16", True, "normal"),  # several items per CTA
     (1, 2, 1, 1500, 256, "bf16", True, "normal"),    # the wide kernel
+    (1, 3, 3, 900, 176, "f16", False, "normal"),     # the wide kernel at width 192
 ]
 
 

@@ -1,7 +1,7 @@
 """GPU parity for head dimensions other than 64 and 128 against the fp64
 oracle.  A head dimension D (a multiple of 8 up to 256) runs on the D = 64,
-D = 128 or D = 256 kernel, whose tensor maps cover only the D columns: the
-copies read the others as zeros and the O stores leave them out.  Every path that stores
+D = 128, D = 192 or D = 256 kernel, whose tensor maps cover only the D
+columns: the copies read the others as zeros and the O stores leave them out.  Every path that stores
 O is covered: the TMA store, the merge of split keys and the row-by-row
 stores of a packed sequence's last tile, with guard bands around O.
 Tolerances as in test_parity_gpu.py."""
@@ -51,7 +51,7 @@ def test_head_dims(D, causal, split_kv):
 
 
 @pytest.mark.parametrize("split_kv", [False, True], ids=["one-cta-per-block", "split-kv"])
-@pytest.mark.parametrize("D", [24, 96])
+@pytest.mark.parametrize("D", [24, 96, 176, 232])
 def test_output_stays_inside_the_tensor(D, split_kv):
     """O surrounded by guard bands: no column past D and no row past S is
     written (rows are D elements apart, not the kernel's width)."""
@@ -194,12 +194,13 @@ def test_wide_window(D, window, causal, H_kv):
                  f"window {window} D{D} causal={causal}")
 
 
-def test_wide_full_size_sampled_rows():
-    """B2 H16 S8192 D256 bf16, causal: sampled rows of a few heads."""
+@pytest.mark.parametrize("D", [192, 256])
+def test_wide_full_size_sampled_rows(D):
+    """B2 H16 S8192 bf16 at D = 192 and 256, causal: sampled rows of a few heads."""
     import torch
     import attention_forward_fwd_gb300 as fa
-    B, H, S, D = 2, 16, 8192, 256
-    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, "bf16", "normal", 151)
+    B, H, S = 2, 16, 8192
+    qb, kb, vb = fa_inputs.make_qkv(B, H, S, D, "bf16", "normal", 151 + D % 256)
     q, k, v = (fa_inputs.to_torch(x, "bf16").cuda() for x in (qb, kb, vb))
     o, lse = fa.attention_forward(q, k, v, causal=True, scale=D ** -0.5)
     torch.cuda.synchronize()
@@ -208,18 +209,19 @@ def test_wide_full_size_sampled_rows():
     for b, h in ((0, 0), (1, 15), (1, 4)):
         rows = np.sort(np.concatenate([rng.choice(S, 20, replace=False), [0, S - 1]]))
         Oref, Lref = attention_rows(qb, kb, vb, "bf16", True, D ** -0.5, b, h, rows)
-        assert_close(O[b, rows, h, :], L[b, h, rows], Oref, Lref, "bf16", f"D256 b={b} h={h}")
+        assert_close(O[b, rows, h, :], L[b, h, rows], Oref, Lref, "bf16", f"D{D} b={b} h={h}")
 
 
 @pytest.mark.parametrize("S", [1, 2, 127, 129, 255, 257, 383])
 @pytest.mark.parametrize("causal", [False, True])
-def test_wide_edge_lengths(S, causal):
+@pytest.mark.parametrize("D", [192, 256])
+def test_wide_edge_lengths(D, S, causal):
     """One key, tile boundaries and lengths that are not multiples of 8."""
-    D, dtype = 256, "f16"
-    qb, kb, vb = fa_inputs.make_qkv(1, 2, S, D, dtype, "stress", 160 + S)
+    dtype = "f16"
+    qb, kb, vb = fa_inputs.make_qkv(1, 2, S, D, dtype, "stress", 160 + S + D)
     O, L = run_gpu(qb, kb, vb, dtype, causal, D ** -0.5)
     Oref, Lref = attention_reference(qb, kb, vb, dtype, causal, D ** -0.5)
-    assert_close(O, L, Oref, Lref, dtype, f"D256 S{S} causal={causal}")
+    assert_close(O, L, Oref, Lref, dtype, f"D{D} S{S} causal={causal}")
 
 
 def test_wide_many_heads_one_wave_and_more():
