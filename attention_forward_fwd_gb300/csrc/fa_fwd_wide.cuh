@@ -8,8 +8,9 @@
 // or 256 columns: one 128-row query tile per CTA, so that its S (128 columns)
 // and O (D columns) fit in tensor memory: S in two buffers (columns [0, 128)
 // and [384, 512)), P written over its S, O in [128, 128 + D).  Shared memory
-// holds the Q tile (D / 64 boxes of 64 columns) and two slots of the same
-// size: K(j) in one, V(j) in the other.  The tensor pipe runs S(0), S(1),
+// holds the Q tile (D / 64 boxes of 64 columns) and slots of the same size:
+// one for K(j) and one for V(j) at D = 256, two for V at D = 192 (V(j+1)
+// then loads while P V(j-1) runs).  The tensor pipe runs S(0), S(1),
 // P V(0), S(2), P V(1), ...: S(j+1) overlaps the softmax of tile j.  S(j) is
 // issued after P V(j-2), so when S(j) is complete the P V that last read its
 // buffer is too; O may be rescaled once P V(j-1) has reported on its own
@@ -50,8 +51,8 @@ constexpr long long kWideL2ShareCausal = 32ll << 20;
 
 struct WideBars {
     uint64_t q_full;
-    uint64_t kv_full[2];    // slot 0: K(j) (whole-tile mode), slot 1: V(j)
-    uint64_t kv_empty[2];
+    uint64_t kv_full[3];    // slot 0: K(j) (whole-tile mode), slots 1, 2: V(j)
+    uint64_t kv_empty[3];
     uint64_t kbox_full[kWideAtoms];    // per-box mode: box c of K(j) landed
     uint64_t kbox_empty[kWideAtoms];   // ... and read by S(j)
     uint64_t s_full[2];     // S(j) complete in buffer j % 2 (and every MMA before it)
@@ -76,9 +77,11 @@ struct WideSmem {
     static_assert(kBN + D <= static_cast<int>(kWideS1), "O overlaps the second S/P buffer");
     static constexpr int kAtoms = D / 64;              // 64-column boxes per row
     static constexpr int kTileBytes = kBM * D * 2;     // one 128 x D 16-bit tile
+    // V slots: V(j) waits for P V(j - kVSlots) to have read its slot
+    static constexpr int kVSlots = D == 192 ? 2 : 1;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kTileBytes;
-    static constexpr int kOffBar = kOffKV + 2 * kTileBytes;
+    static constexpr int kOffKV = kTileBytes;          // K, then the V slots
+    static constexpr int kOffBar = kOffKV + (1 + kVSlots) * kTileBytes;
     static constexpr int kAlloc = kOffBar + static_cast<int>(sizeof(WideBars)) + 1024;
     static_assert(kAlloc <= 232448, "shared memory beyond the 227 KiB a CTA may use");
 };
@@ -103,6 +106,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     using L = WideSmem<D>;
     constexpr int kAtoms = L::kAtoms;
     constexpr int kTileBytes = L::kTileBytes;
+    constexpr int kVSlots = L::kVSlots;
     WideBars* bars = reinterpret_cast<WideBars*>(smem + L::kOffBar);
     volatile int* abort_flag = &bars->abort;
     auto bar = [&](const uint64_t* b) { return ptx::smem_addr(b); };
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
     if (threadIdx.x == 32 * 5) {
         ptx::mbar_init(bar(&bars->q_full), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < 3; ++s) {
             ptx::mbar_init(bar(&bars->kv_full[s]), 1);
             ptx::mbar_init(bar(&bars->kv_empty[s]), 1);
         }
@@ -211,10 +215,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         if (lane == 0 && n_tiles > 0) {
             if (!p.drop_first_q) load_tile(&tmQ, q_dst, bar(&bars->q_full), h, r0);
         }
-        // K(j+1) is needed before V(j) (the MMA order is S(j+1), P V(j)):
-        // K(0), V(0), K(1), then K(j+1), V(j).  Tile i of a slot waits for
-        // the slot's previous tile to be consumed (completion i of its
-        // empty barrier).
+        // K(j+1) is needed before V(j) (the MMA order is S(j+1), P V(j)).
+        // One V slot: K(0), V(0), K(1), then K(j+1), V(j).  Two: K(j), V(j),
+        // the order in which their slots are released (V(j) waits for
+        // P V(j-2), which runs before S(j), which K(j+1) waits for).  A tile
+        // waits for the previous tile of its slot to be consumed.
         bool ok = true;
         int nk = 0, nv = 0;   // K / V tiles issued
         int nkb[kAtoms] = {};   // per-box mode: boxes of K issued
@@ -239,16 +244,27 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             ++nk;
         };
         auto load_v = [&](int i) {
-            if (i > 0 && !(ok = wait_warp(bar(&bars->kv_empty[1]), static_cast<uint32_t>((i - 1) & 1)))) return;
-            if (lane == 0) load_tile(&tmV, slot0 + kTileBytes, bar(&bars->kv_full[1]), hkv, (jb + i) * kBN);
+            const int vs = i % kVSlots;
+            if (i >= kVSlots && !(ok = wait_warp(bar(&bars->kv_empty[1 + vs]),
+                                                 static_cast<uint32_t>((i / kVSlots - 1) & 1))))
+                return;
+            if (lane == 0)
+                load_tile(&tmV, slot0 + (1 + vs) * kTileBytes, bar(&bars->kv_full[1 + vs]), hkv, (jb + i) * kBN);
             ++nv;
         };
-        if (n_tiles > 0) load_k(0);
-        if (ok && n_tiles > 0) load_v(0);
-        if (ok && n_tiles > 1) load_k(1);
-        for (int j = 1; j < n_tiles && ok; ++j) {
-            if (j + 1 < n_tiles) load_k(j + 1);
-            if (ok) load_v(j);
+        if constexpr (kVSlots == 2) {
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                load_k(j);
+                if (ok) load_v(j);
+            }
+        } else {
+            if (n_tiles > 0) load_k(0);
+            if (ok && n_tiles > 0) load_v(0);
+            if (ok && n_tiles > 1) load_k(1);
+            for (int j = 1; j < n_tiles && ok; ++j) {
+                if (j + 1 < n_tiles) load_k(j + 1);
+                if (ok) load_v(j);
+            }
         }
         if (*abort_flag) {
             // let every copy this warp started land before the CTA exits
@@ -259,7 +275,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             for (int c = 0; c < kAtoms; ++c)
                 if (FA_WIDE_KBOX != 0 && nkb[c] > 0)
                     wait_warp(bar(&bars->kbox_full[c]), static_cast<uint32_t>((nkb[c] - 1) & 1), false);
-            if (nv > 0) wait_warp(bar(&bars->kv_full[1]), static_cast<uint32_t>((nv - 1) & 1), false);
+            // the last V tile of each slot: tile i went to slot i % kVSlots as
+            // its (i / kVSlots)-th
+            for (int i = max(0, nv - kVSlots); i < nv; ++i)
+                wait_warp(bar(&bars->kv_full[1 + i % kVSlots]), static_cast<uint32_t>((i / kVSlots) & 1), false);
         }
     } else if (warp == 4) {
         // ------------------------------------------------------ MMA issue
@@ -269,7 +288,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         bool ok = n_tiles == 0 || wait_warp(bar(&bars->q_full), 0);
         const uint64_t qd = ptx::sdesc_sw128(sbase + L::kOffQ, 16, 1024);
         const uint64_t kd = ptx::sdesc_sw128(slot0, 16, 1024);
-        const uint64_t vd = ptx::sdesc_sw128(slot0 + kTileBytes, kBN * 128, 1024);
+        const uint64_t vd0 = ptx::sdesc_sw128(slot0 + kTileBytes, kBN * 128, 1024);
         // S(i) into buffer i % 2: Q K(i)^T over the D columns, K=16 steps
         // through the D / 64 boxes of 64 columns (32 bytes per step inside a box)
         auto issue_s = [&](int i) {
@@ -314,7 +333,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         };
         if (ok && n_tiles > 0) issue_s(0);
         for (int j = 0; j < n_tiles && ok; ++j) {
-            const uint32_t par = static_cast<uint32_t>(j & 1);
             if (j + 1 < n_tiles) {
                 issue_s(j + 1);
                 if (!ok) break;
@@ -322,12 +340,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             // O (+)= P(j) V(j): P from the first 64 columns of S(j)'s buffer,
             // V MN-major (64-column boxes 128*128 bytes apart)
             if (!(ok = wait_warp(bar(&bars->p_full[j & 1]), static_cast<uint32_t>((j >> 1) & 1)))) break;
-            if (!(ok = wait_warp(bar(&bars->kv_full[1]), par))) break;
+            const int vs = j % kVSlots;
+            if (!(ok = wait_warp(bar(&bars->kv_full[1 + vs]), static_cast<uint32_t>((j / kVSlots) & 1)))) break;
             ptx::tc_fence_after_sync();
             const uint32_t pa = tmem + ((j & 1) ? kWideS1 : 0u);
+            const uint32_t vslot = slot0 + (1 + vs) * kTileBytes;
             if constexpr (FA_MMA_BATCH != 0) {
                 const uint32_t hi = ptx::sdesc_sw128_hi(1024);
-                const uint32_t vlo = ptx::sdesc_sw128_lo(slot0 + kTileBytes, kBN * 128);
+                const uint32_t vlo = ptx::sdesc_sw128_lo(vslot, kBN * 128);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; kk += 4)
                     ptx::mma_ts_x4_lo(tmem + kBN, pa + kk * 8, vlo + kk * (16 * 128 / 16), hi, 8u,
@@ -335,10 +355,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             } else {
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    ptx::mma_ts_warp(tmem + kBN, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), kIdescPV,
+                    ptx::mma_ts_warp(tmem + kBN, pa + kk * 8, vd0 + ((vs * kTileBytes + kk * 16 * 128) >> 4), kIdescPV,
                                      (j > 0 || kk > 0) ? 1u : 0u);
             }
-            ptx::tc_commit_warp(bar(&bars->kv_empty[1]));
+            ptx::tc_commit_warp(bar(&bars->kv_empty[1 + vs]));
             ptx::tc_commit_warp(bar(&bars->o_done));
             if (j + 1 == n_tiles) ptx::tc_commit_warp(bar(&bars->o_last));
         }
