@@ -513,8 +513,9 @@ int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE
     const int mb = opt.cu_seqlens ? 1 : B;
     const int ms = opt.cu_seqlens ? opt.total : S;
     CUtensorMap mq, mk, mv;
+    // V is copied in pieces of kVRows keys
     if (!make_map(&mq, Q, BF16, mb, ms, H, Dh, fa::kBM) || !make_map(&mk, K, BF16, mb, ms, Hkv, Dh, fa::kBN) ||
-        !make_map(&mv, V, BF16, mb, ms, Hkv, Dh, fa::kBN))
+        !make_map(&mv, V, BF16, mb, ms, Hkv, Dh, fa::WideSmem<D>::kVRows))
         return FA_ERR_CUDA;
     fa::FwdParams p = {};
     p.B = B;

@@ -7,20 +7,27 @@
 // (section 第二次 GEMM 与输出 Epilogue)), laid out for a wide head of D = 192
 // or 256 columns: one 128-row query tile per CTA, so that its S (128 columns)
 // and O (D columns) fit in tensor memory: S in two buffers (columns [0, 128)
-// and [384, 512)), P written over its S, O in [128, 128 + D).  Shared memory
-// holds the Q tile (D / 64 boxes of 64 columns) and slots of the same size:
-// one for K(j) and one for V(j) at D = 256, two for V at D = 192 (V(j+1)
-// then loads while P V(j-1) runs).  The tensor pipe runs S(0), S(1),
-// P V(0), S(2), P V(1), ...: S(j+1) overlaps the softmax of tile j.  S(j) is
-// issued after P V(j-2), so when S(j) is complete the P V that last read its
-// buffer is too; O may be rescaled once P V(j-1) has reported on its own
-// barrier.
+// and [384, 512)), P written over its S, O in [128, 128 + D).  The tensor
+// pipe runs S(0), S(1), P V(0), S(2), P V(1), ...: S(j+1) overlaps the
+// softmax of tile j.  S(j) is issued after P V(j-2), so when S(j) is
+// complete the P V that last read its buffer is too; O may be rescaled once
+// P V(j-1) has reported on its own barrier.
+//
+// Shared memory holds the Q tile (D / 64 boxes of 64 columns) and two rings:
+// K as 128-key x 64-column boxes (16 KiB; S(j) reads box c of K(j) in its
+// K steps 4c .. 4c+3 and releases it after them), V as pieces of 128 or 64
+// keys x D columns (P V(j) reads a piece in the K steps over its keys).  A
+// copy is issued as soon as the slot it goes to is released, several key
+// tiles ahead of its use: a copy from L2 under load takes about as long as
+// two of the MMAs.
 //
 // Warps 0-3: softmax, thread = query row = TMEM lane.  Warp 4: TMEM
-// allocation and MMA issue (converged warp, one elected lane).  Warp 5: TMA
-// producer (lane 0 issues).  Every wait is bounded (wait_phase); after a
-// timeout each role stops, the producer waits (bounded) for its copies, the
-// MMA warp for its MMAs, and the CTA frees its tensor memory and exits.
+// allocation and MMA issue (converged warp, one elected lane).  Warp 5: Q
+// and K copies, warp 6: V copies (lane 0 issues; each in the order the MMAs
+// release their slots, neither waiting on the other's).  Every wait is
+// bounded (wait_phase); after a timeout each role stops, the copy warps wait
+// (bounded) for their copies, the MMA warp for its MMAs, and the CTA frees
+// its tensor memory and exits.
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
@@ -28,8 +35,10 @@
 namespace fa {
 
 constexpr int kWideD = 256;        // the widest head the library takes
-constexpr int kWideThreads = 192;
-constexpr int kWideAtoms = kWideD / 64;   // 64-column boxes per row, at most
+constexpr int kWideThreads = 224;  // softmax warps 0-3, MMA warp 4, copy warps 5 (Q, K) and 6 (V)
+constexpr int kWideBoxBytes = kBN * 128;   // one 128-key x 64-column box of K
+constexpr int kWideMaxKSlots = 6;
+constexpr int kWideMaxVSlots = 3;
 constexpr uint32_t kWideTmemCols = 512;   // S/P buffers [0, 128) and [384, 512), O [128, 128 + D)
 constexpr uint32_t kWideS1 = 384;         // column of the second S/P buffer
 // the kernel's width for a head of Dh columns (136 .. 256)
@@ -41,20 +50,12 @@ __host__ __device__ constexpr int wide_dim(int Dh) { return Dh <= 192 ? 192 : 25
 constexpr long long kWideL2Share = 16ll << 20;
 constexpr long long kWideL2ShareCausal = 32ll << 20;
 
-// K tiles are loaded and released one 64-column box at a time: box c of
-// K(j+1) is loaded as soon as the four K steps of S(j) that read box c of
-// K(j) have run, so the load overlaps the rest of S(j) (1: on; 0: the whole
-// tile at once).
-#ifndef FA_WIDE_KBOX
-#define FA_WIDE_KBOX 1
-#endif
-
 struct WideBars {
     uint64_t q_full;
-    uint64_t kv_full[3];    // slot 0: K(j) (whole-tile mode), slots 1, 2: V(j)
-    uint64_t kv_empty[3];
-    uint64_t kbox_full[kWideAtoms];    // per-box mode: box c of K(j) landed
-    uint64_t kbox_empty[kWideAtoms];   // ... and read by S(j)
+    uint64_t kbox_full[kWideMaxKSlots];    // K slot holds its box
+    uint64_t kbox_empty[kWideMaxKSlots];   // ... and S has read it
+    uint64_t v_full[kWideMaxVSlots];       // V slot holds its piece
+    uint64_t v_empty[kWideMaxVSlots];      // ... and P V has read it
     uint64_t s_full[2];     // S(j) complete in buffer j % 2 (and every MMA before it)
     // P(j) stored in buffer j % 2 by the 128 softmax threads.  One barrier
     // per buffer: S(j+1) is issued before the MMA warp waits for P(j), so the
@@ -77,12 +78,21 @@ struct WideSmem {
     static_assert(kBN + D <= static_cast<int>(kWideS1), "O overlaps the second S/P buffer");
     static constexpr int kAtoms = D / 64;              // 64-column boxes per row
     static constexpr int kTileBytes = kBM * D * 2;     // one 128 x D 16-bit tile
-    // V slots: V(j) waits for P V(j - kVSlots) to have read its slot
-    static constexpr int kVSlots = D == 192 ? 2 : 1;
+    // K ring: kKSlots boxes.  V ring: kVSlots pieces, each kVRows keys of a
+    // tile (a V tile in kVSplit pieces).  Sized to fill the 227 KiB.
+    static constexpr int kKSlots = D == 192 ? 5 : 4;
+    static constexpr int kVSplit = D == 192 ? 1 : 2;
+    static constexpr int kVSlots = D == 192 ? 2 : 3;
+    static constexpr int kVRows = kBN / kVSplit;
+    static constexpr int kVBoxBytes = kVRows * 128;    // one 64-column box of a piece
+    static constexpr int kVPieceBytes = kAtoms * kVBoxBytes;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kTileBytes;          // K, then the V slots
-    static constexpr int kOffBar = kOffKV + (1 + kVSlots) * kTileBytes;
+    static constexpr int kOffK = kTileBytes;
+    static constexpr int kOffV = kOffK + kKSlots * kWideBoxBytes;
+    static constexpr int kOffBar = kOffV + kVSlots * kVPieceBytes;
     static constexpr int kAlloc = kOffBar + static_cast<int>(sizeof(WideBars)) + 1024;
+    static_assert(kKSlots >= kAtoms && kKSlots <= kWideMaxKSlots, "K ring");
+    static_assert(kVSlots >= kVSplit && kVSlots <= kWideMaxVSlots && kVRows % 64 == 0, "V ring");
     static_assert(kAlloc <= 232448, "shared memory beyond the 227 KiB a CTA may use");
 };
 
@@ -106,7 +116,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     using L = WideSmem<D>;
     constexpr int kAtoms = L::kAtoms;
     constexpr int kTileBytes = L::kTileBytes;
-    constexpr int kVSlots = L::kVSlots;
     WideBars* bars = reinterpret_cast<WideBars*>(smem + L::kOffBar);
     volatile int* abort_flag = &bars->abort;
     auto bar = [&](const uint64_t* b) { return ptx::smem_addr(b); };
@@ -167,13 +176,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
     if (threadIdx.x == 32 * 5) {
         ptx::mbar_init(bar(&bars->q_full), 1);
-        for (int s = 0; s < 3; ++s) {
-            ptx::mbar_init(bar(&bars->kv_full[s]), 1);
-            ptx::mbar_init(bar(&bars->kv_empty[s]), 1);
+        for (int s = 0; s < L::kKSlots; ++s) {
+            ptx::mbar_init(bar(&bars->kbox_full[s]), 1);
+            ptx::mbar_init(bar(&bars->kbox_empty[s]), 1);
         }
-        for (int c = 0; c < kAtoms; ++c) {
-            ptx::mbar_init(bar(&bars->kbox_full[c]), 1);
-            ptx::mbar_init(bar(&bars->kbox_empty[c]), 1);
+        for (int s = 0; s < L::kVSlots; ++s) {
+            ptx::mbar_init(bar(&bars->v_full[s]), 1);
+            ptx::mbar_init(bar(&bars->v_empty[s]), 1);
         }
         ptx::mbar_init(bar(&bars->s_full[0]), 1);
         ptx::mbar_init(bar(&bars->s_full[1]), 1);
@@ -203,133 +212,93 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     };
 
     if (warp == 5) {
-        // ---------------------------------------------------- TMA producer
+        // ---------------------------------------------------- Q and K copies
         ptx::grid_dependency_wait();   // the previous kernel may write Q, K, V
-        const uint32_t q_dst = sbase + L::kOffQ;
-        const uint32_t slot0 = sbase + L::kOffKV;
-        auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int head, int row0) {
+        const bool q_issued = n_tiles > 0 && !p.drop_first_q;
+        if (lane == 0 && q_issued) {
+            const uint32_t full = bar(&bars->q_full);
             ptx::mbar_arrive_expect_tx(full, kTileBytes);
             for (int c = 0; c < kAtoms; ++c)
-                ptx::tma_load_4d(dst + c * (kBM * 128), map, full, c * 64, head, base + row0, tb);
-        };
-        if (lane == 0 && n_tiles > 0) {
-            if (!p.drop_first_q) load_tile(&tmQ, q_dst, bar(&bars->q_full), h, r0);
+                ptx::tma_load_4d(sbase + L::kOffQ + c * (kBM * 128), &tmQ, full, c * 64, h, base + r0, tb);
         }
-        // K(j+1) is needed before V(j) (the MMA order is S(j+1), P V(j)).
-        // One V slot: K(0), V(0), K(1), then K(j+1), V(j).  Two: K(j), V(j),
-        // the order in which their slots are released (V(j) waits for
-        // P V(j-2), which runs before S(j), which K(j+1) waits for).  A tile
-        // waits for the previous tile of its slot to be consumed.
-        bool ok = true;
-        int nk = 0, nv = 0;   // K / V tiles issued
-        int nkb[kAtoms] = {};   // per-box mode: boxes of K issued
-        auto load_k = [&](int i) {
-            if constexpr (FA_WIDE_KBOX != 0) {
-#pragma unroll 1
-                for (int c = 0; c < kAtoms; ++c) {
-                    const uint32_t full = bar(&bars->kbox_full[c]);
-                    if (i > 0 &&
-                        !(ok = wait_warp(bar(&bars->kbox_empty[c]), static_cast<uint32_t>((i - 1) & 1))))
-                        return;
-                    if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(full, kTileBytes / kAtoms);
-                        ptx::tma_load_4d(slot0 + c * (kBN * 128), &tmK, full, c * 64, hkv, base + (jb + i) * kBN, tb);
-                    }
-                    ++nkb[c];
-                }
-            } else {
-                if (i > 0 && !(ok = wait_warp(bar(&bars->kv_empty[0]), static_cast<uint32_t>((i - 1) & 1)))) return;
-                if (lane == 0) load_tile(&tmK, slot0, bar(&bars->kv_full[0]), hkv, (jb + i) * kBN);
-            }
-            ++nk;
-        };
-        auto load_v = [&](int i) {
-            const int vs = i % kVSlots;
-            if (i >= kVSlots && !(ok = wait_warp(bar(&bars->kv_empty[1 + vs]),
-                                                 static_cast<uint32_t>((i / kVSlots - 1) & 1))))
-                return;
-            if (lane == 0)
-                load_tile(&tmV, slot0 + (1 + vs) * kTileBytes, bar(&bars->kv_full[1 + vs]), hkv, (jb + i) * kBN);
-            ++nv;
-        };
-        if constexpr (kVSlots == 2) {
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                load_k(j);
-                if (ok) load_v(j);
-            }
-        } else {
-            if (n_tiles > 0) load_k(0);
-            if (ok && n_tiles > 0) load_v(0);
-            if (ok && n_tiles > 1) load_k(1);
-            for (int j = 1; j < n_tiles && ok; ++j) {
-                if (j + 1 < n_tiles) load_k(j + 1);
-                if (ok) load_v(j);
+        // box n = i * kAtoms + c (box c of K(i)) goes to slot n % kKSlots as
+        // its (n / kKSlots)-th box, once S has read the slot's previous one
+        const uint32_t k0 = sbase + L::kOffK;
+        const int nbox = n_tiles * kAtoms;
+        int n = 0;
+        for (; n < nbox; ++n) {
+            const int slot = n % L::kKSlots;
+            const int use = n / L::kKSlots;
+            if (use > 0 && !wait_warp(bar(&bars->kbox_empty[slot]), static_cast<uint32_t>((use - 1) & 1))) break;
+            if (lane == 0) {
+                const int i = n / kAtoms;
+                const int c = n - i * kAtoms;
+                const uint32_t full = bar(&bars->kbox_full[slot]);
+                ptx::mbar_arrive_expect_tx(full, kWideBoxBytes);
+                ptx::tma_load_4d(k0 + slot * kWideBoxBytes, &tmK, full, c * 64, hkv, base + (jb + i) * kBN, tb);
             }
         }
         if (*abort_flag) {
             // let every copy this warp started land before the CTA exits
-            // (only the last of each slot can still be in flight)
-            if (n_tiles > 0) wait_warp(bar(&bars->q_full), 0, false);
-            if (FA_WIDE_KBOX == 0 && nk > 0)
-                wait_warp(bar(&bars->kv_full[0]), static_cast<uint32_t>((nk - 1) & 1), false);
-            for (int c = 0; c < kAtoms; ++c)
-                if (FA_WIDE_KBOX != 0 && nkb[c] > 0)
-                    wait_warp(bar(&bars->kbox_full[c]), static_cast<uint32_t>((nkb[c] - 1) & 1), false);
-            // the last V tile of each slot: tile i went to slot i % kVSlots as
-            // its (i / kVSlots)-th
-            for (int i = max(0, nv - kVSlots); i < nv; ++i)
-                wait_warp(bar(&bars->kv_full[1 + i % kVSlots]), static_cast<uint32_t>((i / kVSlots) & 1), false);
+            // (only the last box of each slot can still be in flight)
+            if (q_issued) wait_warp(bar(&bars->q_full), 0, false);
+            for (int m = max(0, n - L::kKSlots); m < n; ++m)
+                wait_warp(bar(&bars->kbox_full[m % L::kKSlots]), static_cast<uint32_t>((m / L::kKSlots) & 1), false);
         }
+    } else if (warp == 6) {
+        // ---------------------------------------------------------- V copies
+        ptx::grid_dependency_wait();
+        // piece m = i * kVSplit + e (keys [e * kVRows, (e + 1) * kVRows) of
+        // V(i)) goes to slot m % kVSlots, once P V has read the slot's
+        // previous piece
+        const uint32_t v0 = sbase + L::kOffV;
+        const int npiece = n_tiles * L::kVSplit;
+        int m = 0;
+        for (; m < npiece; ++m) {
+            const int slot = m % L::kVSlots;
+            const int use = m / L::kVSlots;
+            if (use > 0 && !wait_warp(bar(&bars->v_empty[slot]), static_cast<uint32_t>((use - 1) & 1))) break;
+            if (lane == 0) {
+                const int i = m / L::kVSplit;
+                const int e = m - i * L::kVSplit;
+                const uint32_t full = bar(&bars->v_full[slot]);
+                ptx::mbar_arrive_expect_tx(full, L::kVPieceBytes);
+                for (int c = 0; c < kAtoms; ++c)
+                    ptx::tma_load_4d(v0 + slot * L::kVPieceBytes + c * L::kVBoxBytes, &tmV, full, c * 64, hkv,
+                                     base + (jb + i) * kBN + e * L::kVRows, tb);
+            }
+        }
+        if (*abort_flag)
+            for (int q = max(0, m - L::kVSlots); q < m; ++q)
+                wait_warp(bar(&bars->v_full[q % L::kVSlots]), static_cast<uint32_t>((q / L::kVSlots) & 1), false);
     } else if (warp == 4) {
         // ------------------------------------------------------ MMA issue
         constexpr uint32_t kIdescQK = ptx::idesc_f16_f32(kBM, kBN, BF16, false);
         constexpr uint32_t kIdescPV = ptx::idesc_f16_f32(kBM, D, BF16, true);
-        const uint32_t slot0 = sbase + L::kOffKV;
+        const uint32_t hi = ptx::sdesc_sw128_hi(1024);
+        const uint32_t qlo = ptx::sdesc_sw128_lo(sbase + L::kOffQ, 16);
+        const uint32_t klo = ptx::sdesc_sw128_lo(sbase + L::kOffK, 16);
+        // V MN-major (rows are keys): the 64-column boxes of a piece
+        // kVBoxBytes apart
+        const uint32_t vlo = ptx::sdesc_sw128_lo(sbase + L::kOffV, L::kVBoxBytes);
         bool ok = n_tiles == 0 || wait_warp(bar(&bars->q_full), 0);
-        const uint64_t qd = ptx::sdesc_sw128(sbase + L::kOffQ, 16, 1024);
-        const uint64_t kd = ptx::sdesc_sw128(slot0, 16, 1024);
-        const uint64_t vd0 = ptx::sdesc_sw128(slot0 + kTileBytes, kBN * 128, 1024);
-        // S(i) into buffer i % 2: Q K(i)^T over the D columns, K=16 steps
-        // through the D / 64 boxes of 64 columns (32 bytes per step inside a box)
+        // S(i) into buffer i % 2: Q K(i)^T over the D columns, box by box
+        // (four K=16 steps of 32 bytes inside a box), each box handed back
+        // to the K ring once its steps have run
         auto issue_s = [&](int i) {
             const uint32_t d = tmem + ((i & 1) ? kWideS1 : 0u);
-            if constexpr (FA_WIDE_KBOX != 0) {
-                // box by box: wait for box c of K(i), run its four K steps, and
-                // hand the box back to the producer once they have run
-                const uint32_t hi = ptx::sdesc_sw128_hi(1024);
-                const uint32_t qlo = ptx::sdesc_sw128_lo(sbase + L::kOffQ, 16);
-                const uint32_t klo = ptx::sdesc_sw128_lo(slot0, 16);
 #pragma unroll
-                for (int c = 0; c < kAtoms; ++c) {
-                    if (!(ok = wait_warp(bar(&bars->kbox_full[c]), static_cast<uint32_t>(i & 1)))) return;
-                    ptx::tc_fence_after_sync();
-                    ptx::mma_ss_x4_lo(d, qlo + c * (kBM * 128 / 16), klo + c * (kBN * 128 / 16), hi, 2u,
-                                      kIdescQK, c > 0 ? 1u : 0u);
-                    ptx::tc_commit_warp(bar(&bars->kbox_empty[c]));
-                }
-                ptx::tc_commit_warp(bar(&bars->s_full[i & 1]));
-                return;
-            }
-            if (!(ok = wait_warp(bar(&bars->kv_full[0]), static_cast<uint32_t>(i & 1)))) return;
-            ptx::tc_fence_after_sync();
-            if constexpr (FA_MMA_BATCH != 0) {
-                // four K steps (one 64-column box) per election
-                const uint32_t hi = ptx::sdesc_sw128_hi(1024);
-                const uint32_t qlo = ptx::sdesc_sw128_lo(sbase + L::kOffQ, 16);
-                const uint32_t klo = ptx::sdesc_sw128_lo(slot0, 16);
-#pragma unroll
-                for (int c = 0; c < kAtoms; ++c)
-                    ptx::mma_ss_x4_lo(d, qlo + c * (kBM * 128 / 16), klo + c * (kBN * 128 / 16), hi, 2u,
-                                      kIdescQK, c > 0 ? 1u : 0u);
-            } else {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-                    ptx::mma_ss_warp(d, qd + (off >> 4), kd + (off >> 4), kIdescQK, kk > 0);
-                }
+            for (int c = 0; c < kAtoms; ++c) {
+                const int n = i * kAtoms + c;
+                const int slot = n % L::kKSlots;
+                if (!(ok = wait_warp(bar(&bars->kbox_full[slot]), static_cast<uint32_t>((n / L::kKSlots) & 1))))
+                    return;
+                ptx::tc_fence_after_sync();
+                ptx::mma_ss_x4_lo(d, qlo + c * (kBM * 128 / 16), klo + slot * (kWideBoxBytes / 16), hi, 2u, kIdescQK,
+                                  c > 0 ? 1u : 0u);
+                ptx::tc_commit_warp(bar(&bars->kbox_empty[slot]));
             }
             ptx::tc_commit_warp(bar(&bars->s_full[i & 1]));
-            ptx::tc_commit_warp(bar(&bars->kv_empty[0]));
         };
         if (ok && n_tiles > 0) issue_s(0);
         for (int j = 0; j < n_tiles && ok; ++j) {
@@ -337,28 +306,26 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 issue_s(j + 1);
                 if (!ok) break;
             }
-            // O (+)= P(j) V(j): P from the first 64 columns of S(j)'s buffer,
-            // V MN-major (64-column boxes 128*128 bytes apart)
+            // O (+)= P(j) V(j): P from the first 64 columns of S(j)'s buffer
+            // (8 columns per K step of 16 keys), V piece by piece
             if (!(ok = wait_warp(bar(&bars->p_full[j & 1]), static_cast<uint32_t>((j >> 1) & 1)))) break;
-            const int vs = j % kVSlots;
-            if (!(ok = wait_warp(bar(&bars->kv_full[1 + vs]), static_cast<uint32_t>((j / kVSlots) & 1)))) break;
-            ptx::tc_fence_after_sync();
             const uint32_t pa = tmem + ((j & 1) ? kWideS1 : 0u);
-            const uint32_t vslot = slot0 + (1 + vs) * kTileBytes;
-            if constexpr (FA_MMA_BATCH != 0) {
-                const uint32_t hi = ptx::sdesc_sw128_hi(1024);
-                const uint32_t vlo = ptx::sdesc_sw128_lo(vslot, kBN * 128);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; kk += 4)
-                    ptx::mma_ts_x4_lo(tmem + kBN, pa + kk * 8, vlo + kk * (16 * 128 / 16), hi, 8u,
-                                      16u * 128u / 16u, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-            } else {
+            for (int e = 0; e < L::kVSplit; ++e) {
+                const int m = j * L::kVSplit + e;
+                const int slot = m % L::kVSlots;
+                if (!(ok = wait_warp(bar(&bars->v_full[slot]), static_cast<uint32_t>((m / L::kVSlots) & 1)))) break;
+                ptx::tc_fence_after_sync();
+                const uint32_t vs = vlo + slot * (L::kVPieceBytes / 16);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    ptx::mma_ts_warp(tmem + kBN, pa + kk * 8, vd0 + ((vs * kTileBytes + kk * 16 * 128) >> 4), kIdescPV,
-                                     (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < L::kVRows / 16; kk += 4) {
+                    const int kg = e * (L::kVRows / 16) + kk;   // K step within the tile
+                    ptx::mma_ts_x4_lo(tmem + kBN, pa + kg * 8, vs + kk * (16 * 128 / 16), hi, 8u, 16u * 128u / 16u,
+                                      kIdescPV, (j > 0 || kg > 0) ? 1u : 0u);
+                }
+                ptx::tc_commit_warp(bar(&bars->v_empty[slot]));
             }
-            ptx::tc_commit_warp(bar(&bars->kv_empty[1 + vs]));
+            if (!ok) break;
             ptx::tc_commit_warp(bar(&bars->o_done));
             if (j + 1 == n_tiles) ptx::tc_commit_warp(bar(&bars->o_last));
         }
