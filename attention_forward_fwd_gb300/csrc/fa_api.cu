@@ -512,10 +512,11 @@ int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE
     // packed variable-length tensors are one batch of `total` rows
     const int mb = opt.cu_seqlens ? 1 : B;
     const int ms = opt.cu_seqlens ? opt.total : S;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     // V is copied in pieces of kVRows keys
     if (!make_map(&mq, Q, BF16, mb, ms, H, Dh, fa::kBM) || !make_map(&mk, K, BF16, mb, ms, Hkv, Dh, fa::kBN) ||
-        !make_map(&mv, V, BF16, mb, ms, Hkv, Dh, fa::WideSmem<D>::kVRows))
+        !make_map(&mv, V, BF16, mb, ms, Hkv, Dh, fa::WideSmem<D>::kVRows) ||
+        !make_map(&mo, O, BF16, mb, ms, H, Dh, fa::kBM))
         return FA_ERR_CUDA;
     fa::FwdParams p = {};
     p.B = B;
@@ -560,7 +561,7 @@ int launch_wide(const void* Q, const void* K, const void* V, void* O, float* LSE
     cfg.stream = stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, p) != cudaSuccess) return FA_ERR_CUDA;
     if (plan.chunk == 0) return FA_OK;
     return launch_combine<D, BF16>(p, O, B, H, ntq, stream);
 }

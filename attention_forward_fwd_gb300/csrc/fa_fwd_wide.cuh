@@ -50,6 +50,12 @@ __host__ __device__ constexpr int wide_dim(int Dh) { return Dh <= 192 ? 192 : 25
 constexpr long long kWideL2Share = 16ll << 20;
 constexpr long long kWideL2ShareCausal = 32ll << 20;
 
+// The final O tile is staged in shared memory and stored by TMA (1), or
+// each softmax thread stores its row from registers (0).
+#ifndef FA_WIDE_STAGE_O
+#define FA_WIDE_STAGE_O 1
+#endif
+
 struct WideBars {
     uint64_t q_full;
     uint64_t kbox_full[kWideMaxKSlots];    // K slot holds its box
@@ -108,7 +114,8 @@ struct WideSmem {
 template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(kWideThreads, 1)
     fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                       const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -196,6 +203,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         ptx::tma_prefetch_map(&tmQ);
         ptx::tma_prefetch_map(&tmK);
         ptx::tma_prefetch_map(&tmV);
+        ptx::tma_prefetch_map(&tmO);
     }
     if (warp == 4) {
         ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kWideTmemCols);
@@ -248,16 +256,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     } else if (warp == 6) {
         // ---------------------------------------------------------- V copies
         ptx::grid_dependency_wait();
+        // V(0) is first read after S(0), S(1) and the softmax of tile 0:
+        // its copies wait for Q, whose copy and K(0)'s they would slow
+        bool ok = n_tiles == 0 || wait_warp(bar(&bars->q_full), 0);
         // piece m = i * kVSplit + e (keys [e * kVRows, (e + 1) * kVRows) of
         // V(i)) goes to slot m % kVSlots, once P V has read the slot's
         // previous piece
         const uint32_t v0 = sbase + L::kOffV;
         const int npiece = n_tiles * L::kVSplit;
         int m = 0;
-        for (; m < npiece; ++m) {
+        for (; m < npiece && ok; ++m) {
             const int slot = m % L::kVSlots;
             const int use = m / L::kVSlots;
-            if (use > 0 && !wait_warp(bar(&bars->v_empty[slot]), static_cast<uint32_t>((use - 1) & 1))) break;
+            if (use > 0 && !(ok = wait_warp(bar(&bars->v_empty[slot]), static_cast<uint32_t>((use - 1) & 1)))) break;
             if (lane == 0) {
                 const int i = m / L::kVSplit;
                 const int e = m - i * L::kVSplit;
@@ -458,32 +469,72 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 ml[r] = -INFINITY;
                 ml[kBM + r] = 0.f;
             }
-        } else if (ok && n_tiles > 0) {
-            ptx::tc_fence_after_sync();
+        } else if (n_tiles > 0) {
+            // final result: staged as the 128-byte-swizzled TMA boxes in the
+            // V ring (every P V is complete, so nothing reads it any more),
+            // each box stored by one thread once all rows have written it;
+            // rows past S are dropped by the store.  The last tile of a packed sequence is stored row by row
+            // instead (the rows after it belong to the next sequence).
+            const bool direct = FA_WIDE_STAGE_O == 0 || (p.cu_seqlens != nullptr && r0 + kBM > S_b);
+            uint8_t* stage = smem + L::kOffV;
             float inv_l = 1.f / l;
             if constexpr (DROP) inv_l *= p.drop_inv_keep;   // kept P scaled by 1 / (1 - p)
             // row of O: batch tb (0 when packed) of S rows, then the sequence
             // start `base` (0 unless packed)
             uint16_t* orow = static_cast<uint16_t*>(p.o_ptr) +
                              ((static_cast<size_t>(tb) * p.S + base + row) * p.H + h) * p.d_head;
+            // eight values of O's row, scaled and rounded to 16 bits
+            auto pack8 = [&](const uint32_t* o) {
+                uint4 v;
+                v.x = pack2<BF16>(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l);
+                v.y = pack2<BF16>(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l);
+                v.z = pack2<BF16>(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l);
+                v.w = pack2<BF16>(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l);
+                return v;
+            };
+            if (!direct) {
+                // box by box (64 columns per TMEM round trip): box c is
+                // stored while box c + 1 is staged
+                if (ptx::named_barrier_and(1, kBM, ok)) {
+                    ptx::tc_fence_after_sync();
 #pragma unroll 1
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t o[32];
-                ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
-                ptx::tmem_ld_wait();
-                ptx::reg_fence<32>(o);
+                    for (int cb = 0; cb < kAtoms; ++cb) {
+                        uint32_t o[64];
+                        ptx::tmem_ld_32x32b_x32(tO + cb * 64, o);
+                        ptx::tmem_ld_32x32b_x32(tO + cb * 64 + 32, o + 32);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence<64>(o);
+                        uint8_t* box = stage + cb * (kBM * 128) + r * 128;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int col = q * 32 + u * 8;
-                    uint4 v;
-                    v.x = pack2<BF16>(__uint_as_float(o[u * 8 + 0]) * inv_l, __uint_as_float(o[u * 8 + 1]) * inv_l);
-                    v.y = pack2<BF16>(__uint_as_float(o[u * 8 + 2]) * inv_l, __uint_as_float(o[u * 8 + 3]) * inv_l);
-                    v.z = pack2<BF16>(__uint_as_float(o[u * 8 + 4]) * inv_l, __uint_as_float(o[u * 8 + 5]) * inv_l);
-                    v.w = pack2<BF16>(__uint_as_float(o[u * 8 + 6]) * inv_l, __uint_as_float(o[u * 8 + 7]) * inv_l);
-                    if (row < S_b && col < p.d_head) *reinterpret_cast<uint4*>(orow + col) = v;
+                        for (int u = 0; u < 8; ++u)
+                            *reinterpret_cast<uint4*>(box + ((u ^ (r & 7)) * 16)) = pack8(o + u * 8);
+                        ptx::fence_proxy_async_smem();
+                        ptx::named_barrier_sync(1, kBM);
+                        if (threadIdx.x == 0) {
+                            ptx::tma_store_4d(&tmO, ptx::smem_addr(stage + cb * (kBM * 128)), cb * 64, h, base + r0, tb);
+                            ptx::bulk_commit_group();
+                        }
+                    }
+                    // the CTA's shared memory must outlive the stores' reads
+                    if (threadIdx.x == 0) ptx::bulk_wait_group_read_all();
+                }
+            } else if (ok) {
+                ptx::tc_fence_after_sync();
+#pragma unroll 1
+                for (int q = 0; q < D / 32; q += 2) {
+                    uint32_t o[64];
+                    ptx::tmem_ld_32x32b_x32(tO + q * 32, o);
+                    ptx::tmem_ld_32x32b_x32(tO + q * 32 + 32, o + 32);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence<64>(o);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int col = q * 32 + u * 8;
+                        if (row < S_b && col < p.d_head) *reinterpret_cast<uint4*>(orow + col) = pack8(o + u * 8);
+                    }
                 }
             }
-            if (p.lse != nullptr && row < S_b) {
+            if (ok && p.lse != nullptr && row < S_b) {
                 const size_t li = p.cu_seqlens != nullptr ? static_cast<size_t>(h) * p.total + base + row
                                                           : static_cast<size_t>(bh) * p.S + row;
                 p.lse[li] = (m_use * c + log2f(l)) * 0.69314718055994530942f;
