@@ -19,7 +19,8 @@
 // keys x D columns (P V(j) reads a piece in the K steps over its keys).  A
 // copy is issued as soon as the slot it goes to is released, several key
 // tiles ahead of its use: a copy from L2 under load takes about as long as
-// two of the MMAs.
+// two of the MMAs.  Once the last P V is complete the V ring stages the
+// final O tile for its TMA stores.
 //
 // Warps 0-3: softmax, thread = query row = TMEM lane.  Warp 4: TMEM
 // allocation and MMA issue (converged warp, one elected lane).  Warp 5: Q

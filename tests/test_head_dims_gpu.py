@@ -253,3 +253,19 @@ def test_wide_partial_last_head_group(H, H_kv, causal):
         rows = np.sort(np.concatenate([rng.choice(S, 12, replace=False), [0, S - 1]]))
         Oref, Lref = attention_rows(qb, kb, vb, "bf16", causal, D ** -0.5, 0, h, rows)
         assert_close(O[0, rows, h, :], L[0, h, rows], Oref, Lref, "bf16", f"D256 h={h}")
+
+
+@pytest.mark.parametrize("D,width", [(136, 192), (176, 192), (192, 192), (200, 256), (256, 256)])
+def test_wide_split_workspace_has_the_kernel_width(D, width):
+    """D = 136 .. 192 run on the 192-column kernel, 200 .. 256 on the
+    256-column one; a split call's partials have the kernel's width (fp32 o~
+    of 128 x width plus m and l per slot), so the workspace scales with it."""
+    import torch
+    import attention_forward_fwd_gb300 as fa
+    B, H, S = 1, 2, 1000
+    n = fa.fa_splitkv_workspace_size(B, H, S, D, False)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    splits, _ = fa.fa_split_plan(B, H, S, D, False, sms)
+    assert max(splits) > 1
+    slots = B * H * ((S + 127) // 128) * max(splits)
+    assert n == slots * (128 * width + 2 * 128) * 4
